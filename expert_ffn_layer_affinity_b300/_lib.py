@@ -1,0 +1,140 @@
+"""ctypes binding of libmoe_b300.so: the C ABI of include/moe.h with the same
+names.  Argument marshalling only -- every step runs in the library's CUDA
+kernels.  Loading fails loudly when the library is missing; there is no
+other implementation to fall back to."""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libmoe_b300.so")
+
+MOE_OK = 0
+MOE_ERR_INVALID_ARG = -1
+MOE_ERR_UNSUPPORTED_SHAPE = -2
+MOE_ERR_CUDA = -3
+MOE_ERR_WORKSPACE = -4
+MOE_DEV_TIMEOUT = 1
+MOE_DEV_NONFINITE = 2
+MOE_DEV_BAD_INDEX = 4
+
+_STATUS_NAMES = {
+    MOE_ERR_INVALID_ARG: "MOE_ERR_INVALID_ARG",
+    MOE_ERR_UNSUPPORTED_SHAPE: "MOE_ERR_UNSUPPORTED_SHAPE",
+    MOE_ERR_CUDA: "MOE_ERR_CUDA",
+    MOE_ERR_WORKSPACE: "MOE_ERR_WORKSPACE",
+}
+
+# name -> (restype, argtypes); every pointer is passed as c_void_p
+P, I, F, Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+SIGNATURES = {
+    "moe_abi_version": (I, []),
+    "moe_workspace_bytes": (Z, [I, I, I, I, I]),
+    "moe_router_prepare": (I, [P, I, I, P, P]),
+    "moe_router_topk": (I, [P, P, P, P, P, I, I, I, I, I, I, F, P, P, P, P, P, P, Z, P]),
+    "moe_permute": (I, [P, I, I, I, P, I, P, P, P, P, P, P, Z, P]),
+    "moe_grouped_swiglu": (I, [P, P, I, I, I, I, P, P, P, P, P, P, P]),
+    "moe_combine": (I, [P, P, P, P, I, I, I, P, P]),
+    "moe_bias_update": (I, [P, P, I, I, I, F, P, P]),
+}
+
+_lib = None
+
+
+class MoEError(RuntimeError):
+    def __init__(self, fn, code):
+        super().__init__(f"{fn} returned {code} ({_STATUS_NAMES.get(code, 'unknown')})")
+        self.code = code
+
+
+def lib() -> ctypes.CDLL:
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise ImportError(f"{LIB_PATH} is missing: build it with "
+                              "`python -m expert_ffn_layer_affinity_b300.build`")
+        L = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in SIGNATURES.items():
+            fn = getattr(L, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = L
+    return _lib
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(name, code):
+    if code != MOE_OK:
+        raise MoEError(name, code)
+    return code
+
+
+# ---------------------------------------------------------------- raw calls
+def moe_abi_version() -> int:
+    return lib().moe_abi_version()
+
+
+def moe_workspace_bytes(T, d, E, K, I) -> int:
+    return lib().moe_workspace_bytes(T, d, E, K, I)
+
+
+def moe_router_prepare(w_r, E, d, w_split, stream=None, check=True):
+    r = lib().moe_router_prepare(_ptr(w_r), E, d, _ptr(w_split), _stream(stream))
+    return _check("moe_router_prepare", r) if check else r
+
+
+def moe_router_topk(x, w_split, scores_in, logit_offset, bias, T, d, E, K, n_groups,
+                    topk_groups, route_scale, topk_idx, topk_gate, expert_load,
+                    affinity_out, status_dev, ws, ws_bytes, stream=None, check=True):
+    r = lib().moe_router_topk(_ptr(x), _ptr(w_split), _ptr(scores_in), _ptr(logit_offset),
+                              _ptr(bias), T, d, E, K, n_groups, topk_groups,
+                              float(route_scale), _ptr(topk_idx), _ptr(topk_gate),
+                              _ptr(expert_load), _ptr(affinity_out), _ptr(status_dev),
+                              _ptr(ws), ws_bytes, _stream(stream))
+    return _check("moe_router_topk", r) if check else r
+
+
+def moe_permute(topk_idx, T, K, E, x, d, expert_offsets, row_of, tok_of, x_perm,
+                status_dev, ws, ws_bytes, stream=None, check=True):
+    r = lib().moe_permute(_ptr(topk_idx), T, K, E, _ptr(x), d, _ptr(expert_offsets),
+                          _ptr(row_of), _ptr(tok_of), _ptr(x_perm), _ptr(status_dev),
+                          _ptr(ws), ws_bytes, _stream(stream))
+    return _check("moe_permute", r) if check else r
+
+
+def moe_grouped_swiglu(a, group_offsets, n_groups, R, d, I, w1, w3, w2, h, y, status_dev,
+                       stream=None, check=True):
+    r = lib().moe_grouped_swiglu(_ptr(a), _ptr(group_offsets), n_groups, R, d, I, _ptr(w1),
+                                 _ptr(w3), _ptr(w2), _ptr(h), _ptr(y), _ptr(status_dev),
+                                 _stream(stream))
+    return _check("moe_grouped_swiglu", r) if check else r
+
+
+def moe_combine(y_perm, row_of, topk_gate, y_shared, T, K, d, out, stream=None, check=True):
+    r = lib().moe_combine(_ptr(y_perm), _ptr(row_of), _ptr(topk_gate), _ptr(y_shared), T, K, d,
+                          _ptr(out), _stream(stream))
+    return _check("moe_combine", r) if check else r
+
+
+def moe_bias_update(expert_load, bias, T, K, E, gamma, stats_out, stream=None, check=True):
+    r = lib().moe_bias_update(_ptr(expert_load), _ptr(bias), T, K, E, float(gamma),
+                              _ptr(stats_out), _stream(stream))
+    return _check("moe_bias_update", r) if check else r

@@ -1,0 +1,54 @@
+// Internal launch interface between the C ABI (moe_api.cu) and the kernels.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cstddef>
+#include <cstdint>
+
+namespace moe {
+
+int sm_count();  // SMs of the current device (cached per device)
+
+// ---- router selection (router_topk.cu)
+struct TopkArgs {
+  const float* scores;     // [T, E] affinities
+  const float* bias;       // [E]
+  int T, E, K, n_groups, topk_groups;
+  float route_scale;
+  int32_t* idx;            // [T, K]
+  float* gate;             // [T, K]
+  int32_t* load;           // [E], zeroed before the launch
+  int32_t* status;
+};
+cudaError_t launch_topk(const TopkArgs& a, cudaStream_t s);
+
+// ---- router weight split (router_topk.cu)
+cudaError_t launch_router_split(const float* w_r, int E, int d, uint16_t* w_split, cudaStream_t s);
+
+// ---- permute (permute.cu)
+constexpr int kPermuteTile = 1024;   // (token, slot) entries per counting tile
+size_t permute_ws_bytes(int T, int K, int E);
+cudaError_t launch_permute(const int32_t* idx, int T, int K, int E, const uint16_t* x, int d,
+                           int32_t* offsets, int32_t* row_of, int32_t* tok_of, uint16_t* x_perm,
+                           int32_t* status, int32_t* tile_counts, cudaStream_t s);
+
+// ---- combine + bias update (combine.cu)
+cudaError_t launch_combine(const uint16_t* y_perm, const int32_t* row_of, const float* gate,
+                           const uint16_t* y_shared, int T, int K, int d, uint16_t* out,
+                           cudaStream_t s);
+cudaError_t launch_bias_update(const int32_t* load, float* bias, int T, int K, int E, float gamma,
+                               float* stats, cudaStream_t s);
+
+// ---- tensor-core GEMMs (gemm_tc.cu)
+// Router logits + sigmoid: s[t, e] = sigmoid(sum_j x[t,j] w[e,j] + o[e]) with
+// w given as the exact bf16 split [E, 3d].
+cudaError_t launch_router_gemm(const uint16_t* x, const uint16_t* w_split, const float* offset,
+                               int T, int d, int E, float* scores, int32_t* status,
+                               cudaStream_t s);
+// Grouped SwiGLU experts (GEMM1 + fused SwiGLU, then GEMM2).
+cudaError_t launch_grouped_swiglu(const uint16_t* a, const int32_t* offsets, int G, int R, int d,
+                                  int I, const uint16_t* w1, const uint16_t* w3,
+                                  const uint16_t* w2, uint16_t* h, uint16_t* y, int32_t* status,
+                                  cudaStream_t s);
+
+}  // namespace moe

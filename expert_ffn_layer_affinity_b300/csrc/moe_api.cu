@@ -1,0 +1,190 @@
+// C ABI of libmoe_b300.so (declared in include/moe.h): argument checks, the
+// workspace layout, and the kernel launches of each step.
+#include <cuda_runtime.h>
+#include <cstdint>
+#include <cstring>
+
+#include "internal.h"
+#include "../../include/moe.h"
+
+namespace moe {
+
+int sm_count() {
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+  if (dev >= 0 && dev < 64 && cached[dev] > 0) return cached[dev];
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+    n = 148;
+  if (dev >= 0 && dev < 64) cached[dev] = n;
+  return n;
+}
+
+namespace {
+
+constexpr size_t kAlign = 256;
+size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+moe_status cuda_status(cudaError_t e) {
+  if (e == cudaSuccess) return MOE_OK;
+  if (e == cudaErrorInvalidValue) return MOE_ERR_INVALID_ARG;
+  return MOE_ERR_CUDA;
+}
+
+// Workspace layout: [router scores T*E fp32][permute tile counts].
+size_t ws_router_bytes(int T, int E) { return align_up(static_cast<size_t>(T) * E * sizeof(float)); }
+
+bool routing_shape_ok(int T, int E, int K, int G, int M) {
+  if (T < 0 || E < 1 || E > 512 || K < 1 || K > E || K > 32) return false;
+  if (G < 1 || M < 1 || M > G || E % G) return false;
+  if (static_cast<long long>(T) * K >= (1ll << 31)) return false;
+  if (G > 1) {
+    const int vpl = E <= 32 ? 1 : E <= 64 ? 2 : E <= 128 ? 4 : E <= 256 ? 8 : 16;
+    const int gsz = E / G;
+    if (gsz % vpl) return false;
+    const int lanes = gsz / vpl;
+    if (lanes & (lanes - 1)) return false;
+    const int n_top = (K + M - 1) / M;
+    if (n_top > 4 || n_top > gsz || K > M * gsz) return false;
+  }
+  return true;
+}
+
+}  // namespace
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+int moe_abi_version(void) { return 1; }
+
+size_t moe_workspace_bytes(int T, int d, int E, int K, int I) {
+  (void)d;
+  (void)I;
+  if (T < 0 || E < 1 || K < 1) return 0;
+  return ws_router_bytes(T, E) + align_up(permute_ws_bytes(T, K, E));
+}
+
+moe_status moe_router_prepare(const float* w_r, int E, int d, void* w_split_bf16,
+                              moe_stream_t stream) {
+  if (!w_r || !w_split_bf16 || E < 1 || d < 1) return MOE_ERR_INVALID_ARG;
+  if (d % 64 || E > 512) return MOE_ERR_UNSUPPORTED_SHAPE;
+  return cuda_status(launch_router_split(w_r, E, d, static_cast<uint16_t*>(w_split_bf16),
+                                         static_cast<cudaStream_t>(stream)));
+}
+
+moe_status moe_router_topk(const void* x_bf16, const void* w_split_bf16, const float* scores_in,
+                           const float* logit_offset, const float* bias, int T, int d, int E,
+                           int K, int n_groups, int topk_groups, float route_scale,
+                           int32_t* topk_idx, float* topk_gate, int32_t* expert_load,
+                           float* affinity_out, int32_t* status_dev, void* ws, size_t ws_bytes,
+                           moe_stream_t stream) {
+  if (!bias || !expert_load || T < 0) return MOE_ERR_INVALID_ARG;
+  if (T > 0 && (!topk_idx || !topk_gate)) return MOE_ERR_INVALID_ARG;
+  if (!routing_shape_ok(T, E, K, n_groups, topk_groups)) return MOE_ERR_UNSUPPORTED_SHAPE;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const float* scores = scores_in;
+  if (x_bf16 != nullptr) {
+    if (!w_split_bf16) return MOE_ERR_INVALID_ARG;
+    if (d < 64 || d % 64) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (!aligned16(x_bf16) || !aligned16(w_split_bf16)) return MOE_ERR_UNSUPPORTED_SHAPE;
+    float* buf = affinity_out;
+    if (buf == nullptr) {
+      if (!ws || ws_bytes < ws_router_bytes(T, E)) return MOE_ERR_WORKSPACE;
+      buf = static_cast<float*>(ws);
+    }
+    const cudaError_t e = launch_router_gemm(static_cast<const uint16_t*>(x_bf16),
+                                             static_cast<const uint16_t*>(w_split_bf16),
+                                             logit_offset, T, d, E, buf, status_dev, s);
+    if (e != cudaSuccess) return cuda_status(e);
+    scores = buf;
+  } else if (scores_in == nullptr && T > 0) {
+    return MOE_ERR_INVALID_ARG;
+  }
+  TopkArgs a{};
+  a.scores = scores;
+  a.bias = bias;
+  a.T = T;
+  a.E = E;
+  a.K = K;
+  a.n_groups = n_groups;
+  a.topk_groups = topk_groups;
+  a.route_scale = route_scale;
+  a.idx = topk_idx;
+  a.gate = topk_gate;
+  a.load = expert_load;
+  a.status = status_dev;
+  return cuda_status(launch_topk(a, s));
+}
+
+moe_status moe_permute(const int32_t* topk_idx, int T, int K, int E, const void* x_bf16, int d,
+                       int32_t* expert_offsets, int32_t* row_of, int32_t* tok_of,
+                       void* x_perm_bf16, int32_t* status_dev, void* ws, size_t ws_bytes,
+                       moe_stream_t stream) {
+  if (T < 0 || K < 1 || E < 1 || !expert_offsets) return MOE_ERR_INVALID_ARG;
+  if (T > 0 && (!topk_idx || !row_of || !tok_of)) return MOE_ERR_INVALID_ARG;
+  if (E > 512 || K > 32 || static_cast<long long>(T) * K >= (1ll << 31))
+    return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (x_bf16 != nullptr) {
+    if (!x_perm_bf16) return MOE_ERR_INVALID_ARG;
+    if (d < 8 || d % 8 || !aligned16(x_bf16) || !aligned16(x_perm_bf16))
+      return MOE_ERR_UNSUPPORTED_SHAPE;
+  }
+  const size_t need = permute_ws_bytes(T, K, E);
+  const size_t off = ws_router_bytes(T, E);
+  if (T > 0 && (!ws || ws_bytes < off + need)) return MOE_ERR_WORKSPACE;
+  int32_t* tile_counts =
+      T > 0 ? reinterpret_cast<int32_t*>(static_cast<char*>(ws) + off) : nullptr;
+  return cuda_status(launch_permute(topk_idx, T, K, E, static_cast<const uint16_t*>(x_bf16), d,
+                                    expert_offsets, row_of, tok_of,
+                                    static_cast<uint16_t*>(x_perm_bf16), status_dev, tile_counts,
+                                    static_cast<cudaStream_t>(stream)));
+}
+
+moe_status moe_grouped_swiglu(const void* a_bf16, const int32_t* group_offsets, int n_groups,
+                              int R, int d, int I, const void* w1_bf16, const void* w3_bf16,
+                              const void* w2_bf16, void* h_bf16, void* y_bf16,
+                              int32_t* status_dev, moe_stream_t stream) {
+  if (R < 0 || n_groups < 1 || d < 1 || I < 1) return MOE_ERR_INVALID_ARG;
+  if (R > 0 && (!a_bf16 || !group_offsets || !w1_bf16 || !w3_bf16 || !w2_bf16 || !h_bf16 ||
+                !y_bf16))
+    return MOE_ERR_INVALID_ARG;
+  if (d % 64 || I % 64 || n_groups > 512) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (R > 0 && (!aligned16(a_bf16) || !aligned16(w1_bf16) || !aligned16(w3_bf16) ||
+                !aligned16(w2_bf16) || !aligned16(h_bf16) || !aligned16(y_bf16)))
+    return MOE_ERR_UNSUPPORTED_SHAPE;
+  return cuda_status(launch_grouped_swiglu(
+      static_cast<const uint16_t*>(a_bf16), group_offsets, n_groups, R, d, I,
+      static_cast<const uint16_t*>(w1_bf16), static_cast<const uint16_t*>(w3_bf16),
+      static_cast<const uint16_t*>(w2_bf16), static_cast<uint16_t*>(h_bf16),
+      static_cast<uint16_t*>(y_bf16), status_dev, static_cast<cudaStream_t>(stream)));
+}
+
+moe_status moe_combine(const void* y_perm_bf16, const int32_t* row_of, const float* topk_gate,
+                       const void* y_shared_bf16, int T, int K, int d, void* out_bf16,
+                       moe_stream_t stream) {
+  if (T < 0 || K < 1 || d < 1) return MOE_ERR_INVALID_ARG;
+  if (T > 0 && (!y_perm_bf16 || !row_of || !topk_gate || !out_bf16)) return MOE_ERR_INVALID_ARG;
+  if (d % 8 || K > 32) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (T > 0 && (!aligned16(y_perm_bf16) || !aligned16(out_bf16) ||
+                (y_shared_bf16 && !aligned16(y_shared_bf16))))
+    return MOE_ERR_UNSUPPORTED_SHAPE;
+  return cuda_status(launch_combine(static_cast<const uint16_t*>(y_perm_bf16), row_of, topk_gate,
+                                    static_cast<const uint16_t*>(y_shared_bf16), T, K, d,
+                                    static_cast<uint16_t*>(out_bf16),
+                                    static_cast<cudaStream_t>(stream)));
+}
+
+moe_status moe_bias_update(const int32_t* expert_load, float* bias, int T, int K, int E,
+                           float gamma, float* stats_out, moe_stream_t stream) {
+  if (!expert_load || !bias || T < 0 || K < 1 || E < 1) return MOE_ERR_INVALID_ARG;
+  if (E > 1024) return MOE_ERR_UNSUPPORTED_SHAPE;
+  return cuda_status(launch_bias_update(expert_load, bias, T, K, E, gamma, stats_out,
+                                        static_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

@@ -103,34 +103,61 @@ def zipf_logit_offset(E: int, s: float) -> torch.Tensor:
     return (o - o.mean()).to(torch.float32)
 
 
-def make_params(cfg: LayerConfig, device="cpu", seed: int | None = None,
-                chunk_experts: int = 8) -> dict:
-    """Router and expert weights of one layer.  Generation order: w_r, bias,
-    routed w1, w3, w2 (in chunks of experts), shared ws1, ws3, ws2."""
+def _expert_seed(seed: int, e: int) -> int:
+    return seed * 1000003 + 7919 + e
+
+
+def make_expert(cfg: LayerConfig, e: int, device="cpu", seed: int | None = None):
+    """(w1 [I, d], w3 [I, d], w2 [d, I]) of routed expert e, from its own seed,
+    so any single expert can be made without the others."""
+    seed = cfg.seed if seed is None else seed
+    g = _gen(_expert_seed(seed, e), device)
+    bf = torch.bfloat16
+    w1 = _normal((cfg.I, cfg.d), cfg.weight_std, g, device, bf)
+    w3 = _normal((cfg.I, cfg.d), cfg.weight_std, g, device, bf)
+    w2 = _normal((cfg.d, cfg.I), cfg.weight_std, g, device, bf)
+    return w1, w3, w2
+
+
+def make_router(cfg: LayerConfig, device="cpu", seed: int | None = None):
+    """(w_r fp32 [E, d], bias fp32 [E], logit offset [E] or None)."""
     seed = cfg.seed if seed is None else seed
     g = _gen(seed, device)
-    E, d, I, ns = cfg.E, cfg.d, cfg.I, cfg.n_shared
-    p = {}
-    p["w_r"] = _normal((E, d), cfg.router_std, g, device, torch.float32)
+    w_r = _normal((cfg.E, cfg.d), cfg.router_std, g, device, torch.float32)
     if cfg.bias_std > 0:
-        p["bias"] = _normal((E,), cfg.bias_std, g, device, torch.float32)
+        bias = _normal((cfg.E,), cfg.bias_std, g, device, torch.float32)
     else:
-        p["bias"] = torch.zeros(E, dtype=torch.float32, device=device)
+        bias = torch.zeros(cfg.E, dtype=torch.float32, device=device)
+    off = zipf_logit_offset(cfg.E, cfg.zipf_s).to(device) if cfg.zipf_s else None
+    return w_r, bias, off
+
+
+def make_shared(cfg: LayerConfig, device="cpu", seed: int | None = None):
+    """Shared experts side by side: ws1, ws3 [n_s*I, d], ws2 [d, n_s*I]."""
+    seed = cfg.seed if seed is None else seed
+    g = _gen(_expert_seed(seed, -1000), device)
     bf = torch.bfloat16
+    n = cfg.n_shared * cfg.I
+    return (_normal((n, cfg.d), cfg.weight_std, g, device, bf),
+            _normal((n, cfg.d), cfg.weight_std, g, device, bf),
+            _normal((cfg.d, n), cfg.weight_std, g, device, bf))
+
+
+def make_params(cfg: LayerConfig, device="cpu", seed: int | None = None) -> dict:
+    """Router and expert weights of one layer (router from `seed`, each
+    routed expert and the shared block from seeds of their own)."""
+    seed = cfg.seed if seed is None else seed
+    p = {}
+    p["w_r"], p["bias"], p["logit_offset"] = make_router(cfg, device, seed)
+    bf = torch.bfloat16
+    E, d, I = cfg.E, cfg.d, cfg.I
     w1 = torch.empty(E, I, d, dtype=bf, device=device)
     w3 = torch.empty(E, I, d, dtype=bf, device=device)
     w2 = torch.empty(E, d, I, dtype=bf, device=device)
-    for e0 in range(0, E, chunk_experts):
-        e1 = min(E, e0 + chunk_experts)
-        w1[e0:e1] = _normal((e1 - e0, I, d), cfg.weight_std, g, device, bf)
-        w3[e0:e1] = _normal((e1 - e0, I, d), cfg.weight_std, g, device, bf)
-        w2[e0:e1] = _normal((e1 - e0, d, I), cfg.weight_std, g, device, bf)
+    for e in range(E):
+        w1[e], w3[e], w2[e] = make_expert(cfg, e, device, seed)
     p["w1"], p["w3"], p["w2"] = w1, w3, w2
-    p["ws1"] = _normal((ns * I, d), cfg.weight_std, g, device, bf)
-    p["ws3"] = _normal((ns * I, d), cfg.weight_std, g, device, bf)
-    p["ws2"] = _normal((d, ns * I), cfg.weight_std, g, device, bf)
-    p["logit_offset"] = (zipf_logit_offset(E, cfg.zipf_s).to(device)
-                         if cfg.zipf_s else None)
+    p["ws1"], p["ws3"], p["ws2"] = make_shared(cfg, device, seed)
     return p
 
 

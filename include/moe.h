@@ -1,0 +1,152 @@
+/*
+ * moe.h -- C ABI of libmoe_b300.so: the forward pass of a DeepSeekMoE layer
+ * with auxiliary-loss-free load balancing, on one NVIDIA B300 (sm_103a).
+ *
+ * The layer (one step over a batch of T tokens):
+ *   1. affinity   s[t,e] = sigmoid(x[t,:] . w_r[e,:] (+ o[e]))
+ *   2. selection  top-K experts of the biased score z = s + b (the bias only
+ *                 chooses experts), optionally limited to M of G expert groups
+ *   3. gates      g[t,k] = scale * s[t,idx_k] / sum_j s[t,idx_j]  (raw s only)
+ *   4. dispatch   rows grouped by expert, SwiGLU experts + shared experts,
+ *                 weighted combine
+ *   5. feedback   per-expert load over the batch; b_e -= gamma if overloaded,
+ *                 b_e += gamma if underloaded
+ * Sources: "Score = Affinity + Bias" and "Bias 仅用于路由" (DeepSeek V3,
+ * deepseekmodel1.org, section 公式解密); the bias update and node-limited
+ * routing (DeepSeek-V3 Technical Report reading notes, chenshi221.pages.dev,
+ * section "Auxiliary-loss-free 负载均衡"); §3 of "DeepSeek-V3 Technical Report：
+ * 中英对照解读" (weigao.cc); dispatch/combine (same page, §2.2 table row
+ * "Expert parallelism requires token dispatch and combine").
+ *
+ * Conventions shared by every call:
+ *  - All pointers are DEVICE pointers owned by the caller unless a comment says
+ *    otherwise; the library never allocates, frees or synchronises (except the
+ *    one-time per-device set-up noted below) and keeps no state between calls.
+ *  - Every call is asynchronous on `stream` (0 = legacy default stream).
+ *  - Arguments are validated synchronously; a negative moe_status is returned
+ *    and nothing is launched.  Conditions only the device can see (a bounded
+ *    wait that ran out, non-finite scores, out-of-range expert indices) are
+ *    OR-ed as MOE_DEV_* bits into the caller's int32 `status_dev` word, which
+ *    the caller zeroes and reads back when it chooses.
+ *  - Dtypes: bf16 = IEEE bfloat16 bit patterns (uint16), fp32 = float,
+ *    indices int32.  Matrices are row-major with the reduction dimension
+ *    contiguous; base pointers must be 16-byte aligned.
+ *  - Shape limits: d % 64 == 0, I % 64 == 0, 1 <= K <= E <= 512, E % n_groups
+ *    == 0, 1 <= topk_groups <= n_groups, T*K < 2^31.  Anything else returns
+ *    MOE_ERR_UNSUPPORTED_SHAPE; there is no fallback path.
+ */
+#ifndef MOE_B300_H
+#define MOE_B300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef int moe_status;
+typedef void* moe_stream_t; /* a cudaStream_t */
+
+#define MOE_OK 0
+#define MOE_ERR_INVALID_ARG (-1)       /* null pointer, negative size, bad enum */
+#define MOE_ERR_UNSUPPORTED_SHAPE (-2) /* outside the limits above */
+#define MOE_ERR_CUDA (-3)              /* a CUDA runtime/driver call failed */
+#define MOE_ERR_WORKSPACE (-4)         /* workspace smaller than required */
+
+/* Bits OR-ed into *status_dev by the kernels. */
+#define MOE_DEV_TIMEOUT 1u    /* a bounded mbarrier wait ran out (the kernel returned early) */
+#define MOE_DEV_NONFINITE 2u  /* a NaN/Inf affinity or bias was seen (selection still completes, NaN ranks lowest) */
+#define MOE_DEV_BAD_INDEX 4u  /* an expert index outside [0, E) was given to moe_permute (entry skipped) */
+
+/* ABI version of this header: 1. */
+int moe_abi_version(void);
+
+/* Bytes of device workspace the calls below need for a layer of this shape
+ * (the caller allocates it once; 256-byte aligned).  Covers the router's
+ * affinity buffer (T*E fp32) and the permute's per-tile expert counts. */
+size_t moe_workspace_bytes(int T, int d, int E, int K, int I);
+
+/* One-time router weight preparation: splits fp32 w_r [E, d] exactly into
+ * three bf16 parts hi + mid + lo (each the bf16 rounding of the remainder),
+ * stored side by side as w_split [E, 3*d] bf16, so the tensor-core router
+ * GEMM forms every product x*w exactly and only accumulates in fp32.  The
+ * report keeps MoE gating in high precision (qwbw.cn essay on the report,
+ * "MoE门控...依然保留BF16或者FP32高精度"). */
+moe_status moe_router_prepare(const float* w_r, int E, int d, void* w_split_bf16,
+                              moe_stream_t stream);
+
+/* Steps 1-3 and the load count of step 5.
+ *  x_bf16        [T, d] activations, or NULL to select from `scores_in`.
+ *  w_split_bf16  [E, 3d] from moe_router_prepare (ignored when x is NULL).
+ *  scores_in     [T, E] fp32 affinities s, used when x is NULL (this is how
+ *                the selection is checked bit-for-bit against a reference).
+ *  logit_offset  [E] fp32 added to the logits before the sigmoid, or NULL.
+ *  bias          [E] fp32 per-expert selection bias b.
+ *  n_groups, topk_groups  G and M of the group limit (1, 1 = no limit).  A
+ *                group's score is the sum of its ceil(K/M) largest z.
+ *  route_scale   multiplies the normalised gates.
+ * Outputs: topk_idx [T, K] int32 in rank order (z descending, lower expert
+ *  index first on equal z, -0 == +0, NaN below every number); topk_gate
+ *  [T, K] fp32; expert_load [E] int32 (overwritten: zeroed then counted);
+ *  affinity_out [T, E] fp32 or NULL (the s used, when x is given).
+ * Fp32 rule (bit-exact against a reference fed the same s): z = s + b; group
+ *  score = top1 + top2 (+ ...); denom = s_1 + s_2 + ... in rank order;
+ *  g = (s_k / denom) * scale, each one IEEE fp32 operation.
+ * Workspace: `ws` of `ws_bytes` >= moe_workspace_bytes(...). */
+moe_status moe_router_topk(const void* x_bf16, const void* w_split_bf16,
+                           const float* scores_in, const float* logit_offset,
+                           const float* bias, int T, int d, int E, int K,
+                           int n_groups, int topk_groups, float route_scale,
+                           int32_t* topk_idx, float* topk_gate, int32_t* expert_load,
+                           float* affinity_out, int32_t* status_dev, void* ws,
+                           size_t ws_bytes, moe_stream_t stream);
+
+/* Step 4a, dispatch.  Rows of expert e are the (t, k) pairs with
+ * topk_idx[t,k] == e, in ascending (t, k) order; experts follow one another
+ * in ascending order.
+ *  expert_offsets [E+1] int32: row range of each expert (exclusive scan of loads).
+ *  row_of [T, K] int32: row of x_perm holding (t, k).
+ *  tok_of [T*K] int32: token of each row.
+ *  x_perm [T*K, d] bf16: x_perm[row_of[t,k]] = x[t]  (skipped when x_bf16 is NULL). */
+moe_status moe_permute(const int32_t* topk_idx, int T, int K, int E, const void* x_bf16,
+                       int d, int32_t* expert_offsets, int32_t* row_of, int32_t* tok_of,
+                       void* x_perm_bf16, int32_t* status_dev, void* ws, size_t ws_bytes,
+                       moe_stream_t stream);
+
+/* Step 4b, grouped SwiGLU experts: for each group g and each row r in
+ * [group_offsets[g], group_offsets[g+1]):
+ *   h[r]  = silu(a[r] . w1[g]^T) * (a[r] . w3[g]^T)      (bf16 [R, I], fp32 accumulate)
+ *   y[r]  = h[r] . w2[g]^T                                (bf16 [R, d])
+ * with silu(v) = v / (1 + exp(-v)).  a [R, d], w1/w3 [G, I, d], w2 [G, d, I],
+ * all bf16.  group_offsets is a DEVICE array of G+1 non-decreasing row
+ * offsets with group_offsets[G] <= R.  The routed experts use G = E with the
+ * offsets of moe_permute; shared experts use G = 1, offsets {0, T}, a = x and
+ * their weights side by side (width n_shared*I), which equals summing them.
+ * Runs on the tensor cores (tcgen05, TMEM accumulators, TMA-fed). */
+moe_status moe_grouped_swiglu(const void* a_bf16, const int32_t* group_offsets, int n_groups,
+                              int R, int d, int I, const void* w1_bf16, const void* w3_bf16,
+                              const void* w2_bf16, void* h_bf16, void* y_bf16,
+                              int32_t* status_dev, moe_stream_t stream);
+
+/* Step 4c, combine:
+ *   out[t] = bf16( y_shared[t] + sum_k topk_gate[t,k] * y_perm[row_of[t,k]] )
+ * accumulated in fp32 in rank order (y_shared may be NULL).  Gather form:
+ * no atomics, deterministic. */
+moe_status moe_combine(const void* y_perm_bf16, const int32_t* row_of, const float* topk_gate,
+                       const void* y_shared_bf16, int T, int K, int d, void* out_bf16,
+                       moe_stream_t stream);
+
+/* Step 5, bias feedback after the step:
+ *   bias[e] = bias[e] - gamma  if E*load[e] > T*K   (overloaded)
+ *   bias[e] = bias[e] + gamma  if E*load[e] < T*K   (underloaded)
+ *   unchanged                  if equal
+ * each one fp32 operation.  stats_out [4] fp32 (max load, mean load,
+ * max/mean, coefficient of variation) or NULL. */
+moe_status moe_bias_update(const int32_t* expert_load, float* bias, int T, int K, int E,
+                           float gamma, float* stats_out, moe_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_B300_H */

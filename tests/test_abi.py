@@ -1,0 +1,89 @@
+"""The C-ABI library loads without a GPU, exports every function that
+include/moe.h declares, and rejects bad arguments before touching the device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import expert_ffn_layer_affinity_b300 as moe
+from expert_ffn_layer_affinity_b300 import _lib
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(__file__)), "include", "moe.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(moe_\w+)\s*\(", text)))
+
+
+def test_library_exports_every_declared_symbol():
+    names = declared_functions()
+    assert "moe_router_topk" in names and len(names) >= 8
+    L = ctypes.CDLL(_lib.LIB_PATH)
+    for n in names:
+        assert hasattr(L, n), n
+    assert set(names) == set(_lib.SIGNATURES), "binding and header disagree"
+
+
+def test_version_and_workspace():
+    assert moe.moe_abi_version() == 1
+    T, d, E, K, I = 8192, 7168, 256, 8, 2048
+    ws = moe.moe_workspace_bytes(T, d, E, K, I)
+    assert ws >= T * E * 4 + ((T * K + 1023) // 1024) * E * 4
+    assert ws % 256 == 0
+    assert moe.moe_workspace_bytes(-1, d, E, K, I) == 0
+
+
+FAKE = 1 << 20  # never dereferenced: every call below fails validation first
+
+
+@pytest.mark.parametrize("T,E,K,G,M,code", [
+    (16, 16, 17, 1, 1, moe.MOE_ERR_UNSUPPORTED_SHAPE),   # K > E
+    (16, 24, 2, 5, 1, moe.MOE_ERR_UNSUPPORTED_SHAPE),    # E % G
+    (16, 64, 2, 4, 5, moe.MOE_ERR_UNSUPPORTED_SHAPE),    # M > G
+    (16, 1024, 8, 1, 1, moe.MOE_ERR_UNSUPPORTED_SHAPE),  # E too large
+    (16, 64, 33, 1, 1, moe.MOE_ERR_UNSUPPORTED_SHAPE),   # K > 32
+    (16, 256, 8, 64, 4, moe.MOE_ERR_UNSUPPORTED_SHAPE),  # group narrower than a lane's slice
+    (16, 16, 8, 8, 1, moe.MOE_ERR_UNSUPPORTED_SHAPE),    # K > M * group size
+    (-1, 16, 2, 1, 1, moe.MOE_ERR_INVALID_ARG),
+])
+def test_router_rejects_bad_shapes(T, E, K, G, M, code):
+    r = moe.moe_router_topk(None, None, FAKE, None, FAKE, T, 64, E, K, G, M, 1.0, FAKE, FAKE,
+                            FAKE, None, None, None, 0, stream=0, check=False)
+    assert r == code
+
+
+def test_router_rejects_null_bias():
+    r = moe.moe_router_topk(None, None, FAKE, None, None, 4, 64, 16, 2, 1, 1, 1.0, FAKE, FAKE,
+                            FAKE, None, None, None, 0, stream=0, check=False)
+    assert r == moe.MOE_ERR_INVALID_ARG
+
+
+def test_other_calls_reject_bad_arguments():
+    assert moe.moe_grouped_swiglu(FAKE, FAKE, 4, 128, 100, 128, FAKE, FAKE, FAKE, FAKE, FAKE,
+                                  None, stream=0, check=False) == moe.MOE_ERR_UNSUPPORTED_SHAPE
+    assert moe.moe_grouped_swiglu(FAKE, FAKE, 4, 128, 128, 96, FAKE, FAKE, FAKE, FAKE, FAKE,
+                                  None, stream=0, check=False) == moe.MOE_ERR_UNSUPPORTED_SHAPE
+    assert moe.moe_grouped_swiglu(FAKE + 8, FAKE, 4, 128, 128, 128, FAKE, FAKE, FAKE, FAKE,
+                                  FAKE, None, stream=0, check=False) == moe.MOE_ERR_UNSUPPORTED_SHAPE
+    assert moe.moe_grouped_swiglu(None, FAKE, 4, 128, 128, 128, FAKE, FAKE, FAKE, FAKE, FAKE,
+                                  None, stream=0, check=False) == moe.MOE_ERR_INVALID_ARG
+    assert moe.moe_combine(FAKE, FAKE, FAKE, None, 4, 2, 12, FAKE, stream=0,
+                           check=False) == moe.MOE_ERR_UNSUPPORTED_SHAPE
+    assert moe.moe_combine(None, FAKE, FAKE, None, 4, 2, 16, FAKE, stream=0,
+                           check=False) == moe.MOE_ERR_INVALID_ARG
+    assert moe.moe_bias_update(None, FAKE, 4, 2, 16, 1e-3, None, stream=0,
+                               check=False) == moe.MOE_ERR_INVALID_ARG
+    assert moe.moe_permute(FAKE, 4, 2, 16, FAKE, 12, FAKE, FAKE, FAKE, FAKE, None, FAKE, 1 << 20,
+                           stream=0, check=False) == moe.MOE_ERR_UNSUPPORTED_SHAPE
+    assert moe.moe_permute(FAKE, 4, 2, 16, None, 0, FAKE, FAKE, FAKE, None, None, FAKE, 0,
+                           stream=0, check=False) == moe.MOE_ERR_WORKSPACE
+    assert moe.moe_router_prepare(None, 16, 64, FAKE, stream=0, check=False) == moe.MOE_ERR_INVALID_ARG
+    assert moe.moe_router_prepare(FAKE, 16, 65, FAKE, stream=0, check=False) == moe.MOE_ERR_UNSUPPORTED_SHAPE
+
+
+def test_binding_raises_on_error():
+    with pytest.raises(moe.MoEError):
+        moe.moe_combine(None, FAKE, FAKE, None, 4, 2, 16, FAKE, stream=0)
