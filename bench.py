@@ -1,0 +1,428 @@
+#!/usr/bin/env python
+"""Throughput of the DeepSeekMoE layer pass (router GEMM + biased group-limited
+top-K, permute, grouped SwiGLU experts on the tensor cores, shared expert,
+combine, bias update) on B300.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config v3]
+  python bench.py --impl reference ...     (the CPU oracle, timed on host cores)
+
+One step = one pass of the whole path over one batch of T tokens plus the
+bias update.  For N > 1 (launched with torch.distributed.run), every rank
+runs a replica on its own T tokens; the per-expert loads are summed over the
+ranks before the bias update (scaling "weak").  Prints one JSON line on rank 0.
+"""
+from __future__ import annotations
+
+import argparse
+import datetime
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MoE-layer tokens/s (V3-shaped, bf16) and % of tensor-core / HBM roofline"
+CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+                "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+KERNELS_PER_STEP = 12  # router GEMM, selection, 4 permute, 2+2 grouped GEMM, combine, bias update
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=60)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", default="v3",
+                    help="tiny | mid | v3 | v3_drift | v3_decode:<T>")
+    ap.add_argument("--cpu-sample", type=int, default=8,
+                    help="tokens the CPU oracle baseline processes (rank 0, N=1)")
+    ap.add_argument("--ref-sample", type=int, default=2,
+                    help="tokens per step for --impl reference")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--shared-stream", action="store_true",
+                    help="run the shared expert on a second stream")
+    return ap.parse_args()
+
+
+def load_config(name):
+    from expert_ffn_layer_affinity_b300 import synth
+    if name.startswith("v3_decode"):
+        T = int(name.split(":")[1]) if ":" in name else 1024
+        return synth.CONFIGS["v3_decode"].with_T(T)
+    return synth.CONFIGS[name]
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return dict(hbm=p["hbm_gbs"], bf16=p["bf16_tflops"],
+                    bf16_sust=p.get("bf16_tflops_sustained", p["bf16_tflops"]), src="measured")
+    return dict(hbm=6400.0, bf16=1800.0, bf16_sust=1400.0, src="fallback")
+
+
+def blas_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads", 0) for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n:
+            return max(n)
+    except Exception:
+        pass
+    return os.cpu_count()
+
+
+class ClockSampler:
+    """nvidia-smi samples every 50 ms; stop() keeps those taken between
+    mark_start() and mark_stop() (host wall clock)."""
+
+    def __init__(self, index):
+        self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        self.t0 = self.t1 = None
+        try:
+            self.p = subprocess.Popen(["nvidia-smi", f"--query-gpu=timestamp,{CLOCK_FIELDS}",
+                                       "--format=csv,noheader,nounits", "-lms", "50",
+                                       "-i", str(index)], stdout=self.f,
+                                      stderr=subprocess.DEVNULL)
+        except OSError:
+            self.p = None
+            return
+        deadline = time.time() + 5
+        while time.time() < deadline and os.path.getsize(self.f.name) == 0:
+            time.sleep(0.02)
+
+    def mark_start(self):
+        self.t0 = datetime.datetime.now()
+
+    def mark_stop(self):
+        self.t1 = datetime.datetime.now()
+
+    def stop(self):
+        if self.p is None:
+            return None
+        time.sleep(0.1)
+        self.p.terminate()
+        try:
+            self.p.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.p.kill()
+        self.f.flush()
+        self.f.seek(0)
+        rows = [r.split(",") for r in self.f.read().strip().splitlines() if r.strip()]
+        os.unlink(self.f.name)
+        mhz, mx, reasons, power = [], 0.0, set(), []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            r = [x.strip() for x in r]
+            try:
+                ts = datetime.datetime.strptime(r[0], "%Y/%m/%d %H:%M:%S.%f")
+                if self.t0 and self.t1 and not (self.t0 <= ts <= self.t1):
+                    continue
+                mhz.append(float(r[2]))
+                mx = max(mx, float(r[3]))
+                power.append(float(r[4]))
+            except (ValueError, IndexError):
+                continue
+            for n, v in zip(names, r[6:10]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not mhz:
+            return None
+        return {"sm_mhz": statistics.median(mhz), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(mhz), "power_w_max": max(power) if power else None,
+                "power_w_median": statistics.median(power) if power else None}
+
+
+# --------------------------------------------------------------------------
+def algorithmic(cfg, touched):
+    """Per-call algorithmic work (bytes moved at least once, dense FLOPs)."""
+    T, d, E, K, I, ns = cfg.T, cfg.d, cfg.E, cfg.K, cfg.I, cfg.n_shared
+    R = T * K
+    return {
+        "route": dict(flops=2.0 * T * d * E * 3,
+                      bytes=T * d * 2 + 3 * E * d * 2 + 2 * T * E * 4 + T * K * 8),
+        "permute": dict(flops=0.0, bytes=2 * R * 4 + T * d * 2 + R * d * 2 + 2 * R * 4),
+        "routed": dict(flops=6.0 * d * I * R,
+                       bytes=3.0 * touched * I * d * 2 + R * d * 2 + 2 * R * I * 2 + R * d * 2),
+        "shared": dict(flops=6.0 * d * I * ns * T,
+                       bytes=3.0 * ns * I * d * 2 + T * d * 2 + 2 * T * ns * I * 2 + T * d * 2),
+        "combine": dict(flops=0.0, bytes=(R + 2 * T) * d * 2 + T * K * 8),
+    }
+
+
+def cpu_baseline(cfg, layer, x, n_tokens):
+    """The oracle as it stands, timed on the host on `n_tokens` tokens of the
+    first batch (expert weights are fetched to host memory before timing)."""
+    import numpy as np
+    import torch
+    from oracle import moe_ref as ref
+
+    def f64(t):
+        return ref.bf16_to_f64(t.cpu().contiguous().view(torch.int16).numpy().view(np.uint16))
+
+    rng = np.random.default_rng(0)
+    tok = np.sort(rng.choice(x.shape[0], n_tokens, replace=False))
+    x_h = x[torch.from_numpy(tok).to(x.device)].cpu()
+    w_r = layer.w_r.cpu().numpy()
+    bias = layer.bias.cpu().numpy()
+    off = layer.logit_offset.cpu().numpy() if layer.logit_offset is not None else None
+    # which experts the oracle will need: from its own routing (untimed pre-pass)
+    s = ref.router_affinity64(f64(x_h), w_r, off)
+    idx, _ = ref.select_experts(s, bias.astype(np.float64), cfg.K, cfg.n_groups, cfg.topk_groups,
+                                cfg.route_scale, precision="fp64")
+    host = {int(e): (layer.w1[e].cpu(), layer.w3[e].cpu(), layer.w2[e].cpu())
+            for e in np.unique(idx)}
+    shared_h = (layer.ws1.cpu(), layer.ws3.cpu(), layer.ws2.cpu())
+    t0 = time.perf_counter()
+    x64 = f64(x_h)
+    s = ref.router_affinity64(x64, w_r, off)
+    idx, gate = ref.select_experts(s, bias.astype(np.float64), cfg.K, cfg.n_groups,
+                                   cfg.topk_groups, cfg.route_scale, precision="fp64")
+    load = ref.expert_load(idx, cfg.E)
+    ref.bias_update(load, bias, n_tokens, cfg.K, cfg.E, cfg.gamma)
+    ref.moe_output64(x64, idx, gate, lambda e: tuple(f64(w) for w in host[e]),
+                     tuple(f64(w) for w in shared_h), cfg.n_shared)
+    dt = time.perf_counter() - t0
+    return {"value": n_tokens / dt, "unit": "tokens/s", "cores": blas_threads(), "kind": "oracle",
+            "sample": f"{n_tokens} random tokens of the first {cfg.T}-token batch, full layer "
+                      f"(routing, {cfg.K} routed + {cfg.n_shared} shared SwiGLU experts in fp64, "
+                      f"load count, bias update); {dt:.1f} s"}
+
+
+# --------------------------------------------------------------------------
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+    from expert_ffn_layer_affinity_b300 import synth
+    from expert_ffn_layer_affinity_b300.layer import MoELayer
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    group = None
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+        group = dist.group.WORLD
+    cfg = load_config(args.config)
+    p = synth.make_params(cfg, "cuda")            # identical replicas on every rank
+    layer = MoELayer(cfg, p, device=f"cuda:{local}", shared_stream=args.shared_stream)
+    del p
+    n_batches = 2
+    xs = [synth.make_tokens(cfg, step=i, device="cuda", seed=cfg.seed + 7777 * rank)
+          for i in range(n_batches)]
+    stream = torch.cuda.current_stream()
+
+    def barrier():
+        if group is not None:
+            dist.barrier(device_ids=[local])
+
+    for i in range(args.warmup):
+        layer.step(xs[i % n_batches], group=group)
+    torch.cuda.synchronize()
+    if layer.device_status() != 0:
+        raise RuntimeError(f"device status {layer.device_status()} during warm-up")
+    names = ["route", "permute", "routed", "shared", "combine"]
+    marks = [{n: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for n in names} for _ in range(args.steps)]
+    touched = int((layer.load > 0).sum().item())
+    clocks = ClockSampler(local)
+    barrier()
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks.mark_start()
+    ev0.record(stream)
+    for i in range(args.steps):
+        layer.step(xs[i % n_batches], group=group, marks=marks[i])
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    clocks.mark_stop()
+    barrier()
+    clk = clocks.stop()
+    ms = ev0.elapsed_time(ev1)
+    if group is not None:
+        t = torch.tensor([ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    status = layer.device_status()
+    per = {n: statistics.mean(m[n][0].elapsed_time(m[n][1]) for m in marks) for n in names}
+    ms_step = ms / args.steps
+    value = cfg.T * world * args.steps / (ms / 1e3)
+
+    # end to end: host (pinned) -> device copy of the step's tokens, the pass
+    # and bias update, device -> host copy of the output, every step
+    e2e = None
+    if not args.no_e2e:
+        x_host = [x.cpu().pin_memory() for x in xs]
+        out_host = torch.empty(cfg.T, cfg.d, dtype=torch.bfloat16).pin_memory()
+        x_dev = torch.empty_like(xs[0])
+        for i in range(2):
+            x_dev.copy_(x_host[i % n_batches], non_blocking=True)
+            out = layer.step(x_dev, group=group)
+            out_host.copy_(out, non_blocking=True)
+        barrier()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(args.steps):
+            x_dev.copy_(x_host[i % n_batches], non_blocking=True)
+            out = layer.step(x_dev, group=group)
+            out_host.copy_(out, non_blocking=True)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+        ems = e0.elapsed_time(e1)
+        if group is not None:
+            t = torch.tensor([ems], device="cuda")
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            ems = float(t.item())
+        nbytes = cfg.T * cfg.d * 2
+        e2e = {"value": cfg.T * world * args.steps / (ems / 1e3), "unit": "tokens/s",
+               "h2d_bytes_per_step": nbytes, "d2h_bytes_per_step": nbytes,
+               "ms_per_step": ems / args.steps}
+
+    if rank != 0:
+        if group is not None:
+            dist.destroy_process_group()
+        return
+    pk = peaks()
+    alg = algorithmic(cfg, touched)
+    kernels = {}
+    for n in names:
+        a = alg[n]
+        k = {"ms": round(per[n], 4)}
+        if a["flops"]:
+            k["tflops"] = round(a["flops"] / (per[n] * 1e-3) / 1e12, 2)
+        k["gbs"] = round(a["bytes"] / (per[n] * 1e-3) / 1e9, 1)
+        kernels[n] = k
+    routed_tf = alg["routed"]["flops"] / (per["routed"] * 1e-3) / 1e12
+    roofline = {"bound": "tensor", "achieved": round(routed_tf, 1), "peak": pk["bf16_sust"],
+                "unit": "TFLOP/s", "frac": round(routed_tf / pk["bf16_sust"], 4),
+                "traffic": None,
+                "kernel": "moe_grouped_swiglu (routed experts: GEMM1+SwiGLU and GEMM2 launches)",
+                "peak_kind": f"bf16 sustained, {pk['src']}",
+                "frac_of_burst": round(routed_tf / pk["bf16"], 4)}
+    layer_tf = cfg.expert_flops() / (ms_step * 1e-3) / 1e12
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) tokens, N(0,0.02) weights, random-init)",
+        "config": {"workload": f"{cfg.name}: T={cfg.T} d={cfg.d} E={cfg.E} K={cfg.K} "
+                               f"shared={cfg.n_shared} I={cfg.I} groups={cfg.n_groups}/"
+                               f"{cfg.topk_groups} scale={cfg.route_scale}",
+                   "tokens_per_rank": cfg.T, "parallelism": f"dp{world} (replicas, load all-reduce)",
+                   "l2": "inputs larger than L2: 22.6 GB of expert weights streamed per step"
+                   if cfg.d == 7168 else "two alternating token batches",
+                   "shared_stream": bool(args.shared_stream)},
+        "roofline": roofline,
+        "layer_tensor_frac": {"expert_tflops": round(layer_tf, 1),
+                              "frac_of_sustained": round(layer_tf / pk["bf16_sust"], 4),
+                              "frac_of_burst": round(layer_tf / pk["bf16"], 4)},
+        "kernels": kernels,
+        "experts_touched": touched,
+        "gpu_launches": KERNELS_PER_STEP * args.steps,
+        "device_status": status,
+        "clocks": clk,
+        "e2e": e2e,
+    }
+    if not args.no_cpu_baseline and world == 1:
+        line["cpu_baseline"] = cpu_baseline(cfg, layer, xs[0], args.cpu_sample)
+    print(json.dumps(line), flush=True)
+    if group is not None:
+        dist.destroy_process_group()
+
+
+# --------------------------------------------------------------------------
+def run_reference(args):
+    """The CPU oracle on the host cores, one bounded sample of the workload per
+    step: `ref_sample` tokens routed and run through their experts in fp64,
+    then the load count and bias update."""
+    import numpy as np
+    import torch
+    from expert_ffn_layer_affinity_b300 import synth
+    from oracle import moe_ref as ref
+
+    if int(os.environ.get("RANK", "0")) != 0:
+        return
+    cfg = load_config(args.config)
+    n = args.ref_sample
+
+    def f64(t):
+        return ref.bf16_to_f64(t.contiguous().view(torch.int16).numpy().view(np.uint16))
+
+    w_r, bias, off = synth.make_router(cfg, "cpu")
+    w_r, bias = w_r.numpy(), bias.numpy()
+    off = off.numpy() if off is not None else None
+    shared = tuple(f64(w) for w in synth.make_shared(cfg, "cpu"))
+    cache = {}
+
+    def expert(e):
+        if e not in cache:
+            if len(cache) >= 48:
+                cache.pop(next(iter(cache)))
+            cache[e] = synth.make_expert(cfg, e, "cpu")
+        return cache[e]
+
+    times = []
+    for step in range(args.warmup + args.steps):
+        x = synth.make_tokens(cfg, step, "cpu", T=n)
+        s = ref.router_affinity64(f64(x), w_r, off)
+        pre_idx, _ = ref.select_experts(s, bias.astype(np.float64), cfg.K, cfg.n_groups,
+                                        cfg.topk_groups, cfg.route_scale, precision="fp64")
+        for e in np.unique(pre_idx):
+            expert(int(e))                      # input generation, untimed
+        t0 = time.perf_counter()
+        x64 = f64(x)
+        s = ref.router_affinity64(x64, w_r, off)
+        idx, gate = ref.select_experts(s, bias.astype(np.float64), cfg.K, cfg.n_groups,
+                                       cfg.topk_groups, cfg.route_scale, precision="fp64")
+        ref.moe_output64(x64, idx, gate, lambda e: tuple(f64(w) for w in expert(e)), shared,
+                         cfg.n_shared)
+        load = ref.expert_load(idx, cfg.E)
+        bias = ref.bias_update(load, bias, n, cfg.K, cfg.E, cfg.gamma)
+        dt = time.perf_counter() - t0
+        if step >= args.warmup:
+            times.append(dt)
+    total = sum(times)
+    value = n * len(times) / total
+    cores = blas_threads()
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": "tokens/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(1e3 * total / len(times), 2), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded, random-init)",
+        "config": {"workload": f"{cfg.name}: T={cfg.T} d={cfg.d} E={cfg.E} K={cfg.K} "
+                               f"shared={cfg.n_shared} I={cfg.I} groups={cfg.n_groups}/"
+                               f"{cfg.topk_groups} scale={cfg.route_scale}",
+                   "sample_tokens_per_step": n},
+        "cpu_baseline": {"value": round(value, 3), "unit": "tokens/s", "cores": cores,
+                         "kind": "oracle",
+                         "sample": f"{n} tokens per step of the {cfg.T}-token workload, "
+                                   f"full layer in fp64 on the host"},
+        "e2e": {"value": round(value, 3), "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

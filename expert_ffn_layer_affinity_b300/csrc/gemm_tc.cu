@@ -1,34 +1,43 @@
 // Grouped GEMMs on the fifth-generation tensor cores (tcgen05 + TMEM), fed
-// by TMA.  One persistent kernel template serves the three dense
-// contractions of the layer:
+// by TMA.  One persistent, warp-specialised kernel template serves the three
+// dense contractions of the layer:
 //
-//   EPI_SWIGLU   h[r, :] = silu(a[r] . w1[g]^T) * (a[r] . w3[g]^T)  -> bf16
-//                (expert up-projections; SwiGLU applied in the epilogue)
-//   EPI_BF16     y[r, :] = h[r] . w2[g]^T                            -> bf16
-//                (expert down-projection)
-//   EPI_SIGMOID  s[t, e] = sigmoid(x[t] . w_r[e] + o[e])             -> fp32
-//                (router; w_r given as an exact 3-term bf16 split laid
-//                 out along K, so A's K coordinate wraps every d columns)
+//   MODE_SWIGLU  h[r, :] = silu(a[r] . w1[g]^T) * (a[r] . w3[g]^T)  -> bf16
+//   MODE_DOWN    y[r, :] = h[r] . w2[g]^T                            -> bf16
+//   MODE_ROUTER  s[t, e] = sigmoid(x[t] . w_r[e] + o[e])             -> fp32
 //
-// Experts as "shared + fine-grained routed FFNs" follow weigao.cc
-// "DeepSeek-V3 Technical Report：中英对照解读", §2 table rows "DeepSeekMoE" and
-// "Shared experts and routed experts"; the routed groups are the rows that
-// the dispatch step assigned to each expert.
+// Experts as shared + fine-grained routed FFNs follow weigao.cc "DeepSeek-V3
+// Technical Report：中英对照解读", §2 table rows "DeepSeekMoE" and "Shared
+// experts and routed experts"; a group is the run of rows the dispatch step
+// gave to one expert.
+//
+// Expert modes put the WEIGHTS on the MMA's M side (128 weight rows per tile)
+// and the group's TOKENS on the N side, with N chosen per tile as the tokens
+// left rounded up to 16.  An expert with 300 rows thus costs 300 -> 304 rows
+// of MMA work instead of 384 with 128-row token tiles; at the V3 shape the
+// padding drops from about 23% to about 3%.  The epilogue reads the
+// [weight-row x token] accumulator, transposes 32x32 blocks through shared
+// memory and writes token-major rows.
+//
+// Router mode keeps tokens on M (128) and experts on N (128).  Its K loop is
+// cut into chunks of 4 k-blocks; each chunk is accumulated by the tensor core
+// into its own TMEM buffer and the epilogue adds the chunk partials in fp32
+// registers.  Long tensor-core accumulation chains lose precision; the short
+// chains keep the logits' error well inside the 1e-5 near-tie margin used to
+// judge routing.
 //
 // CTA layout (192 threads, one CTA per SM, persistent):
 //   warp 0      TMA producer: fills a STAGES-deep shared-memory ring
-//   warp 1      TMEM allocator; lane 0 issues tcgen05.mma (M=128, N=BN, K=16)
+//   warp 1      TMEM allocator; lane 0 issues tcgen05.mma and commits
 //   warps 2..5  epilogue: tcgen05.ld from TMEM, activation, global stores
-// Two TMEM accumulators (2 x BN columns) let the epilogue of one tile run
-// while the next tile accumulates.  Work items are (group, n-tile, m-tile)
-// triples, group-major and m-tile fastest so that the CTAs working on the
-// same weight tile run side by side and share it through L2.
+// Work items are (group, column tile, token tile), group-major and token
+// tile fastest, so CTAs that need the same weight tile run side by side and
+// share it through L2.
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
 #include <cstdint>
-#include <cstdio>
 
 #include "internal.h"
 #include "ptx.cuh"
@@ -36,49 +45,59 @@
 namespace moe {
 namespace {
 
-constexpr int BM = 128;
 constexpr int BK = 64;
 constexpr int UMMA_K = 16;
 constexpr int kThreads = 192;
 constexpr int kMaxGroups = 512;
+constexpr int kRouterChunkKb = 4;
 
-enum Epi : int { EPI_SWIGLU = 0, EPI_BF16 = 1, EPI_SIGMOID = 2 };
+enum Mode : int { MODE_SWIGLU = 0, MODE_DOWN = 1, MODE_ROUTER = 2 };
+
+template <int MODE>
+struct Tr;
+template <>
+struct Tr<MODE_SWIGLU> {
+  static constexpr int kTokTile = 128, kColTile = 128, kStages = 4, kBufs = 2, kBufCols = 256;
+  static constexpr int kA = 2 * 128 * BK * 2, kB = 128 * BK * 2;  // W1|W3 tiles, token tile
+};
+template <>
+struct Tr<MODE_DOWN> {
+  static constexpr int kTokTile = 256, kColTile = 128, kStages = 4, kBufs = 2, kBufCols = 256;
+  static constexpr int kA = 128 * BK * 2, kB = 256 * BK * 2;
+};
+template <>
+struct Tr<MODE_ROUTER> {
+  static constexpr int kTokTile = 128, kColTile = 128, kStages = 6, kBufs = 4, kBufCols = 128;
+  static constexpr int kA = 128 * BK * 2, kB = 128 * BK * 2;      // token tile, w_split tile
+};
+
+template <int MODE>
+struct Cfg : Tr<MODE> {
+  using T = Tr<MODE>;
+  static constexpr int kStageBytes = T::kA + T::kB;
+  static constexpr int kTmemCols = T::kBufs * T::kBufCols;
+  static constexpr int kNumBars = 2 * T::kStages + 2 * T::kBufs + 1;
+  static constexpr int kXposeBytes = (MODE == MODE_ROUTER) ? 0 : 4 * 32 * 80;
+  static constexpr int kSmem = 1024 + T::kStages * kStageBytes + kXposeBytes + kNumBars * 8 + 16 +
+                               2 * (kMaxGroups + 1) * 4;
+  static_assert(kStageBytes % 1024 == 0, "stages must keep 1024-byte alignment");
+  static_assert(kTmemCols <= 512, "tensor memory");
+  static_assert(kSmem <= 227 * 1024, "shared memory");
+};
 
 struct GemmParams {
   const int32_t* group_offsets;  // [G+1] device; nullptr = one group of rows [0, dense_rows)
   int dense_rows;
   int G;
   int N;                 // output columns of a group
-  int R;                 // rows of A and of the output (stores beyond are dropped)
+  int R;                 // rows of the token operand and of the output
   int num_kb;            // reduction length / BK
-  int a_k_wrap_kb;       // A's k-block = kb % a_k_wrap_kb
-  int b_rows_per_group;  // rows of B's 2-D view that belong to one group
+  int a_k_wrap_kb;       // router: x's k-block = kb % a_k_wrap_kb
+  int w_rows_per_group;  // rows of the weight operand's 2-D view per group
   void* out;
   int ldo;               // output row stride in elements
-  const float* col_offset;  // EPI_SIGMOID: per-column logit offset or nullptr
+  const float* col_offset;  // router: per-expert logit offset or nullptr
   int32_t* status;
-};
-
-constexpr int tmem_cols_for(int n) {
-  int c = 32;
-  while (c < n) c <<= 1;
-  return c;
-}
-
-template <int BN, int EPI, int STAGES>
-struct Cfg {
-  static constexpr int kBnOut = (EPI == EPI_SWIGLU) ? BN / 2 : BN;
-  static constexpr int kABytes = BM * BK * 2;
-  static constexpr int kBBytes = BN * BK * 2;
-  static constexpr int kStageBytes = kABytes + kBBytes;
-  static constexpr int kTmemCols = tmem_cols_for(2 * BN);
-  static constexpr int kNumBars = 2 * STAGES + 5;
-  static constexpr int kSmem = 1024 + STAGES * kStageBytes + kNumBars * 8 + 16 +
-                               2 * (kMaxGroups + 1) * 4;
-  static constexpr uint32_t kIdesc = umma_idesc_bf16(BM, BN);
-  static_assert(BN % 16 == 0 && BN >= 32 && BN <= 256, "UMMA N for M=128");
-  static_assert(kStageBytes % 1024 == 0, "stages must keep 1024-byte alignment");
-  static_assert(kSmem <= 227 * 1024, "shared memory");
 };
 
 __device__ __forceinline__ int group_offset(const GemmParams& p, int g) {
@@ -112,21 +131,49 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<const uint32_t*>(&v);
 }
 
-template <int BN, int EPI, int STAGES>
+// Tokens of this tile the MMA must cover, rounded up to the N granularity.
+__device__ __forceinline__ int tile_n(int rows_left, int tok_tile) {
+  const int n = rows_left < tok_tile ? rows_left : tok_tile;
+  return (n + 15) & ~15;
+}
+
+// Writes a 32 (weight row = output column) x 32 (token) block, held one
+// output column per lane as 16 packed bf16 pairs along tokens, as 32 token
+// rows of 64 bytes.  `xp` is this warp's 32 x 80-byte staging area.
+__device__ __forceinline__ void store_block_transposed(const uint32_t (&v)[32], uint8_t* xp,
+                                                       int lane, __nv_bfloat16* out, long long row0,
+                                                       int rows_valid, int ldo, int col) {
+  // v[j] holds the value for token j of column `lane`, as fp32 bits
+  __nv_bfloat16* x = reinterpret_cast<__nv_bfloat16*>(xp);
+#pragma unroll
+  for (int j = 0; j < 32; ++j) x[j * 40 + lane] = __float2bfloat16_rn(__uint_as_float(v[j]));
+  __syncwarp();
+  if (lane < rows_valid) {
+    const uint4* src = reinterpret_cast<const uint4*>(xp + lane * 80);
+    uint4* dst = reinterpret_cast<uint4*>(out + (row0 + lane) * ldo + col);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) dst[k] = src[k];
+  }
+  __syncwarp();
+}
+
+template <int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
-    gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                const __grid_constant__ CUtensorMap tmB2, const GemmParams p) {
-  using C = Cfg<BN, EPI, STAGES>;
+    gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA2,
+                const __grid_constant__ CUtensorMap tmB, const GemmParams p) {
+  using C = Cfg<MODE>;
+  constexpr int S = C::kStages, NB = C::kBufs;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   const uint32_t tiles = (raw_addr + 1023u) & ~1023u;
-  uint8_t* meta = smem_raw + (tiles - raw_addr) + STAGES * C::kStageBytes;
+  uint8_t* xpose = smem_raw + (tiles - raw_addr) + S * C::kStageBytes;
+  uint8_t* meta = xpose + C::kXposeBytes;
   const uint32_t bars = smem_u32(meta);
   auto full_bar = [&](int s) { return bars + 8u * s; };
-  auto empty_bar = [&](int s) { return bars + 8u * (STAGES + s); };
-  auto accf_bar = [&](int b) { return bars + 8u * (2 * STAGES + b); };
-  auto acce_bar = [&](int b) { return bars + 8u * (2 * STAGES + 2 + b); };
-  const uint32_t drain_bar = bars + 8u * (2 * STAGES + 4);
+  auto empty_bar = [&](int s) { return bars + 8u * (S + s); };
+  auto accf_bar = [&](int b) { return bars + 8u * (2 * S + b); };
+  auto acce_bar = [&](int b) { return bars + 8u * (2 * S + NB + b); };
+  const uint32_t drain_bar = bars + 8u * (2 * S + 2 * NB);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(meta + 8 * C::kNumBars);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   int* mt_prefix = reinterpret_cast<int*>(meta + 8 * C::kNumBars + 16);
@@ -136,7 +183,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int G = p.G;
 
   if (warp == 0) {
-    // per-group m-tile prefix and row starts
     int carry = 0;
     for (int g0 = 0; g0 < G; g0 += 32) {
       const int g = g0 + lane;
@@ -144,7 +190,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (g < G) {
         const int a = group_offset(p, g), b = group_offset(p, g + 1);
         const int rows = b > a ? b - a : 0;
-        mt = (rows + BM - 1) / BM;
+        mt = (rows + C::kTokTile - 1) / C::kTokTile;
         row_start[g] = a;
       }
       int incl = mt;
@@ -160,16 +206,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       mt_prefix[G] = carry;
       row_start[G] = group_offset(p, G);
       tma_prefetch_desc(&tmA);
+      if (MODE == MODE_SWIGLU) tma_prefetch_desc(&tmA2);
       tma_prefetch_desc(&tmB);
-      if (EPI == EPI_SWIGLU) tma_prefetch_desc(&tmB2);
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      for (int s = 0; s < STAGES; ++s) {
+      for (int s = 0; s < S; ++s) {
         mbar_init(full_bar(s), 1);
         mbar_init(empty_bar(s), 1);
       }
-      for (int b = 0; b < 2; ++b) {
+      for (int b = 0; b < NB; ++b) {
         mbar_init(accf_bar(b), 1);
         mbar_init(acce_bar(b), 128);
       }
@@ -187,81 +233,101 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
-  const int NT = (p.N + C::kBnOut - 1) / C::kBnOut;
+  const int NT = (p.N + C::kColTile - 1) / C::kColTile;
   const int total = mt_prefix[G] * NT;
+  const int chunk_kb = (MODE == MODE_ROUTER) ? kRouterChunkKb : p.num_kb;
 
   if (warp == 0) {
+    // ------------------------------------------------------------ producer
     if (lane == 0) {
-      const uint64_t pol_a = l2_policy_evict_last();
-      const uint64_t pol_b = l2_policy_evict_normal();
+      const uint64_t pol_tok = l2_policy_evict_last();
+      const uint64_t pol_w = l2_policy_evict_normal();
       uint32_t it = 0;
       bool ok = true;
       for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
         int g, n, m;
         decode_work(w, NT, mt_prefix, G, g, n, m);
-        const int a_row = row_start[g] + m * BM;
-        const int b_row = g * p.b_rows_per_group + n * C::kBnOut;
+        const int tok_row = row_start[g] + m * C::kTokTile;
+        const int w_row = g * p.w_rows_per_group + n * C::kColTile;
         for (int kb = 0; kb < p.num_kb; ++kb, ++it) {
-          const int s = static_cast<int>(it % STAGES);
-          const uint32_t ph = (it / STAGES) & 1u;
+          const int s = static_cast<int>(it % S);
+          const uint32_t ph = (it / S) & 1u;
           if (!mbar_wait(empty_bar(s), ph ^ 1u, abort_flag, p.status)) {
             ok = false;
             break;
           }
           const uint32_t sa = tiles + s * C::kStageBytes;
-          const uint32_t sb = sa + C::kABytes;
+          const uint32_t sb = sa + C::kA;
           mbar_arrive_expect_tx(full_bar(s), C::kStageBytes);
-          tma_load_2d(sa, &tmA, full_bar(s), (kb % p.a_k_wrap_kb) * BK, a_row, pol_a);
-          if (EPI == EPI_SWIGLU) {
-            tma_load_2d(sb, &tmB, full_bar(s), kb * BK, b_row, pol_b);
-            tma_load_2d(sb + C::kBBytes / 2, &tmB2, full_bar(s), kb * BK, b_row, pol_b);
+          if (MODE == MODE_ROUTER) {
+            tma_load_2d(sa, &tmA, full_bar(s), (kb % p.a_k_wrap_kb) * BK, tok_row, pol_tok);
+            tma_load_2d(sb, &tmB, full_bar(s), kb * BK, w_row, pol_w);
           } else {
-            tma_load_2d(sb, &tmB, full_bar(s), kb * BK, b_row, pol_b);
+            tma_load_2d(sa, &tmA, full_bar(s), kb * BK, w_row, pol_w);
+            if (MODE == MODE_SWIGLU)
+              tma_load_2d(sa + C::kA / 2, &tmA2, full_bar(s), kb * BK, w_row, pol_w);
+            tma_load_2d(sb, &tmB, full_bar(s), kb * BK, tok_row, pol_tok);
           }
         }
       }
       if (!ok) {
-        // let the copies already in flight land before the CTA exits
-        const uint32_t first = it > STAGES ? it - STAGES : 0u;
+        const uint32_t first = it > S ? it - S : 0u;
         for (uint32_t j = first; j < it; ++j)
-          wait_plain(full_bar(static_cast<int>(j % STAGES)), (j / STAGES) & 1u, 200000000ull);
+          wait_plain(full_bar(static_cast<int>(j % S)), (j / S) & 1u, 200000000ull);
       }
     }
     __syncwarp();
   } else if (warp == 1) {
+    // ---------------------------------------------------------- MMA issuer
     if (lane == 0) {
-      uint32_t it = 0, tile = 0;
-      bool ok = true;
-      bool issued = false;
-      for (int w = blockIdx.x; w < total && ok; w += gridDim.x, ++tile) {
-        const int ab = static_cast<int>(tile & 1u);
-        const uint32_t aph = (tile >> 1) & 1u;
-        if (!mbar_wait(acce_bar(ab), aph ^ 1u, abort_flag, p.status)) {
-          ok = false;
-          break;
+      uint32_t it = 0, unit = 0;
+      bool ok = true, issued = false;
+      for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
+        int g, n, m;
+        decode_work(w, NT, mt_prefix, G, g, n, m);
+        uint32_t idesc;
+        if (MODE == MODE_ROUTER) {
+          idesc = umma_idesc_bf16(128, C::kColTile);
+        } else {
+          const int rows_g = row_start[g + 1] - row_start[g];
+          idesc = umma_idesc_bf16(128, tile_n(rows_g - m * C::kTokTile, C::kTokTile));
         }
-        tc_fence_after();
-        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(ab * BN);
-        for (int kb = 0; kb < p.num_kb; ++kb, ++it) {
-          const int s = static_cast<int>(it % STAGES);
-          const uint32_t ph = (it / STAGES) & 1u;
-          if (!mbar_wait(full_bar(s), ph, abort_flag, p.status)) {
+        for (int kb0 = 0; kb0 < p.num_kb && ok; kb0 += chunk_kb, ++unit) {
+          const int b = static_cast<int>(unit % NB);
+          const uint32_t bph = (unit / NB) & 1u;
+          if (!mbar_wait(acce_bar(b), bph ^ 1u, abort_flag, p.status)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t sa = tiles + s * C::kStageBytes;
-          const uint64_t adesc = umma_sdesc_sw128(sa);
-          const uint64_t bdesc = umma_sdesc_sw128(sa + C::kABytes);
+          const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(b * C::kBufCols);
+          const int kb1 = (kb0 + chunk_kb < p.num_kb) ? kb0 + chunk_kb : p.num_kb;
+          for (int kb = kb0; kb < kb1; ++kb, ++it) {
+            const int s = static_cast<int>(it % S);
+            const uint32_t ph = (it / S) & 1u;
+            if (!mbar_wait(full_bar(s), ph, abort_flag, p.status)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t sa = tiles + s * C::kStageBytes;
+            const uint64_t adesc = umma_sdesc_sw128(sa);
+            const uint64_t bdesc = umma_sdesc_sw128(sa + C::kA);
 #pragma unroll
-          for (int k = 0; k < BK / UMMA_K; ++k)
-            umma_bf16(d_tmem, adesc + 2ull * k, bdesc + 2ull * k, C::kIdesc,
-                      (kb > 0 || k > 0) ? 1u : 0u);
-          issued = true;
-          umma_commit(empty_bar(s));
+            for (int k = 0; k < BK / UMMA_K; ++k) {
+              const uint32_t acc = (kb > kb0 || k > 0) ? 1u : 0u;
+              umma_bf16(d_tmem, adesc + 2ull * k, bdesc + 2ull * k, idesc, acc);
+              if (MODE == MODE_SWIGLU) {
+                const uint64_t adesc3 = umma_sdesc_sw128(sa + C::kA / 2);
+                umma_bf16(d_tmem + 128u, adesc3 + 2ull * k, bdesc + 2ull * k, idesc, acc);
+              }
+            }
+            issued = true;
+            umma_commit(empty_bar(s));
+          }
+          if (!ok) break;
+          umma_commit(accf_bar(b));
         }
-        if (!ok) break;
-        umma_commit(accf_bar(ab));
       }
       if (!ok && issued) {
         umma_commit(drain_bar);
@@ -270,92 +336,93 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     __syncwarp();
   } else {
-    // epilogue warps 2..5; warp w may read TMEM lanes 32*(w%4) .. +31
-    const int q = warp & 3;
-    const int r_in_tile = q * 32 + lane;
-    uint32_t tile = 0;
-    for (int w = blockIdx.x; w < total; w += gridDim.x, ++tile) {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;  // this warp may read TMEM lanes 32q .. 32q+31
+    uint8_t* xp = xpose + q * 32 * 80;
+    uint32_t unit = 0;
+    bool ok = true;
+    for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
       int g, n, m;
       decode_work(w, NT, mt_prefix, G, g, n, m);
-      const int ab = static_cast<int>(tile & 1u);
-      const uint32_t aph = (tile >> 1) & 1u;
-      bool ok = mbar_wait(accf_bar(ab), aph, abort_flag, p.status);
-      ok = __all_sync(0xFFFFFFFFu, ok);
-      if (!ok) break;
-      tc_fence_after();
       const int rows_g = row_start[g + 1] - row_start[g];
-      const int local_row = m * BM + r_in_tile;
-      const long long orow = static_cast<long long>(row_start[g]) + local_row;
-      const bool row_ok = local_row < rows_g && orow < p.R;
-      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
-                             static_cast<uint32_t>(ab * BN);
-      if (EPI == EPI_SWIGLU) {
-        __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out);
-#pragma unroll 1
-        for (int c = 0; c < C::kBnOut; c += 32) {
-          uint32_t ra[32], rc[32];
-          tmem_ld32(taddr + c, ra);
-          tmem_ld32(taddr + C::kBnOut + c, rc);
-          tmem_ld_wait();
-          const int col = n * C::kBnOut + c;
-          if (row_ok && col < p.N) {
-            uint32_t pk[16];
+      const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
+      if (MODE == MODE_ROUTER) {
+        float acc[128];
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              const float a0 = __uint_as_float(ra[2 * i]), a1 = __uint_as_float(ra[2 * i + 1]);
-              const float c0 = __uint_as_float(rc[2 * i]), c1 = __uint_as_float(rc[2 * i + 1]);
-              const float h0 = a0 * __frcp_rn(1.0f + __expf(-a0)) * c0;
-              const float h1 = a1 * __frcp_rn(1.0f + __expf(-a1)) * c1;
-              pk[i] = pack_bf16x2(h0, h1);
-            }
-            uint4* dst = reinterpret_cast<uint4*>(out + orow * p.ldo + col);
+        for (int i = 0; i < 128; ++i) acc[i] = 0.0f;
+        for (int kb0 = 0; kb0 < p.num_kb; kb0 += chunk_kb, ++unit) {
+          const int b = static_cast<int>(unit % NB);
+          const uint32_t bph = (unit / NB) & 1u;
+          ok = __all_sync(0xFFFFFFFFu, mbar_wait(accf_bar(b), bph, abort_flag, p.status));
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t taddr = tmem_base + lane_base + static_cast<uint32_t>(b * C::kBufCols);
 #pragma unroll
-            for (int v = 0; v < 4; ++v)
-              dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+          for (int c = 0; c < 128; c += 32) {
+            uint32_t r[32];
+            tmem_ld32(taddr + c, r);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) acc[c + i] = __fadd_rn(acc[c + i], __uint_as_float(r[i]));
           }
+          tc_fence_before();
+          mbar_arrive(acce_bar(b));
         }
-      } else if (EPI == EPI_BF16) {
-        __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out);
-#pragma unroll 1
-        for (int c = 0; c < BN; c += 32) {
-          uint32_t ra[32];
-          tmem_ld32(taddr + c, ra);
-          tmem_ld_wait();
-          const int col = n * BN + c;
-          if (row_ok && col < p.N) {
-            uint32_t pk[16];
+        if (!ok) break;
+        const int row_local = m * 128 + q * 32 + lane;
+        if (row_local < rows_g && row_local < p.R) {
+          float* out = reinterpret_cast<float*>(p.out) + static_cast<long long>(row_local) * p.ldo;
+          const int col0 = n * 128;
 #pragma unroll
-            for (int i = 0; i < 16; ++i)
-              pk[i] = pack_bf16x2(__uint_as_float(ra[2 * i]), __uint_as_float(ra[2 * i + 1]));
-            uint4* dst = reinterpret_cast<uint4*>(out + orow * p.ldo + col);
-#pragma unroll
-            for (int v = 0; v < 4; ++v)
-              dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+          for (int i = 0; i < 128; ++i) {
+            const int cc = col0 + i;
+            if (cc < p.N) {
+              float u = acc[i];
+              if (p.col_offset) u = __fadd_rn(u, p.col_offset[cc]);
+              out[cc] = 1.0f / (1.0f + expf(-u));
+            }
           }
         }
       } else {
-        float* out = reinterpret_cast<float*>(p.out);
-#pragma unroll 1
-        for (int c = 0; c < BN; c += 32) {
-          uint32_t ra[32];
-          tmem_ld32(taddr + c, ra);
-          tmem_ld_wait();
-          const int col = n * BN + c;
-          if (row_ok) {
+        const int b = static_cast<int>(unit % NB);
+        const uint32_t bph = (unit / NB) & 1u;
+        ++unit;
+        ok = __all_sync(0xFFFFFFFFu, mbar_wait(accf_bar(b), bph, abort_flag, p.status));
+        if (!ok) break;
+        tc_fence_after();
+        const int tok0 = m * C::kTokTile;
+        const int n_eff = tile_n(rows_g - tok0, C::kTokTile);
+        const int rows_tile = (rows_g - tok0) < C::kTokTile ? rows_g - tok0 : C::kTokTile;
+        const int col = n * C::kColTile + q * 32;
+        const long long row0 = static_cast<long long>(row_start[g]) + tok0;
+        const bool col_ok = col < p.N;
+        const uint32_t taddr = tmem_base + lane_base + static_cast<uint32_t>(b * C::kBufCols);
+        __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out);
+        for (int c = 0; c < n_eff; c += 32) {
+          uint32_t v[32];
+          if (MODE == MODE_SWIGLU) {
+            uint32_t u3[32];
+            tmem_ld32(taddr + c, v);
+            tmem_ld32(taddr + 128 + c, u3);
+            tmem_ld_wait();
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              const int cc = col + i;
-              if (cc < p.N) {
-                float u = __uint_as_float(ra[i]);
-                if (p.col_offset) u = u + p.col_offset[cc];
-                out[orow * p.ldo + cc] = 1.0f / (1.0f + expf(-u));
-              }
+            for (int j = 0; j < 32; ++j) {
+              const float a = __uint_as_float(v[j]), up = __uint_as_float(u3[j]);
+              v[j] = __float_as_uint(a * __frcp_rn(1.0f + __expf(-a)) * up);
             }
+          } else {
+            tmem_ld32(taddr + c, v);
+            tmem_ld_wait();
           }
+          int valid = rows_tile - c;
+          if (valid > 32) valid = 32;
+          const long long last = row0 + c + valid;
+          if (last > p.R) valid -= static_cast<int>(last - p.R);
+          if (col_ok) store_block_transposed(v, xp, lane, out, row0 + c, valid, p.ldo, col);
         }
+        tc_fence_before();
+        mbar_arrive(acce_bar(b));
       }
-      tc_fence_before();
-      mbar_arrive(acce_bar(ab));
     }
     __syncwarp();
   }
@@ -396,15 +463,15 @@ bool make_map(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer, u
   return r == CUDA_SUCCESS;
 }
 
-template <int BN, int EPI, int STAGES>
-cudaError_t launch_gemm(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& b2,
+template <int MODE>
+cudaError_t launch_gemm(const CUtensorMap& a, const CUtensorMap& a2, const CUtensorMap& b,
                         const GemmParams& p, int max_works, cudaStream_t s) {
-  using C = Cfg<BN, EPI, STAGES>;
+  using C = Cfg<MODE>;
   static bool attr_done[64] = {false};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 64 && !attr_done[dev]) {
-    const cudaError_t e = cudaFuncSetAttribute(gemm_kernel<BN, EPI, STAGES>,
+    const cudaError_t e = cudaFuncSetAttribute(gemm_kernel<MODE>,
                                                cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
     if (e != cudaSuccess) return e;
     attr_done[dev] = true;
@@ -412,7 +479,7 @@ cudaError_t launch_gemm(const CUtensorMap& a, const CUtensorMap& b, const CUtens
   int grid = sm_count();
   if (max_works < grid) grid = max_works;
   if (grid < 1) grid = 1;
-  gemm_kernel<BN, EPI, STAGES><<<grid, kThreads, C::kSmem, s>>>(a, b, b2, p);
+  gemm_kernel<MODE><<<grid, kThreads, C::kSmem, s>>>(a, a2, b, p);
   return cudaGetLastError();
 }
 
@@ -424,12 +491,15 @@ cudaError_t launch_grouped_swiglu(const uint16_t* a, const int32_t* offsets, int
                                   cudaStream_t s) {
   if (R == 0 || G == 0) return cudaSuccess;
   if (G > kMaxGroups) return cudaErrorInvalidValue;
-  CUtensorMap ta, tb1, tb3, th, tb2;
-  if (!make_map(&ta, a, d, R, BM) || !make_map(&tb1, w1, d, static_cast<uint64_t>(G) * I, 128) ||
-      !make_map(&tb3, w3, d, static_cast<uint64_t>(G) * I, 128) || !make_map(&th, h, I, R, BM) ||
-      !make_map(&tb2, w2, I, static_cast<uint64_t>(G) * d, 256))
+  using C1 = Cfg<MODE_SWIGLU>;
+  using C2 = Cfg<MODE_DOWN>;
+  CUtensorMap tw1, tw3, tx, tw2, th;
+  if (!make_map(&tw1, w1, d, static_cast<uint64_t>(G) * I, 128) ||
+      !make_map(&tw3, w3, d, static_cast<uint64_t>(G) * I, 128) ||
+      !make_map(&tx, a, d, R, C1::kTokTile) ||
+      !make_map(&tw2, w2, I, static_cast<uint64_t>(G) * d, 128) ||
+      !make_map(&th, h, I, R, C2::kTokTile))
     return cudaErrorInvalidValue;
-  const int m_tiles_max = (R + BM - 1) / BM + G;
   GemmParams p1{};
   p1.group_offsets = offsets;
   p1.G = G;
@@ -437,29 +507,30 @@ cudaError_t launch_grouped_swiglu(const uint16_t* a, const int32_t* offsets, int
   p1.R = R;
   p1.num_kb = d / BK;
   p1.a_k_wrap_kb = d / BK;
-  p1.b_rows_per_group = I;
+  p1.w_rows_per_group = I;
   p1.out = h;
   p1.ldo = I;
   p1.status = status;
-  cudaError_t e = launch_gemm<256, EPI_SWIGLU, 4>(ta, tb1, tb3, p1, m_tiles_max * ((I + 127) / 128), s);
+  const int mt1 = (R + C1::kTokTile - 1) / C1::kTokTile + G;
+  cudaError_t e = launch_gemm<MODE_SWIGLU>(tw1, tw3, tx, p1, mt1 * ((I + 127) / 128), s);
   if (e != cudaSuccess) return e;
   GemmParams p2 = p1;
   p2.N = d;
   p2.num_kb = I / BK;
   p2.a_k_wrap_kb = I / BK;
-  p2.b_rows_per_group = d;
+  p2.w_rows_per_group = d;
   p2.out = y;
   p2.ldo = d;
-  return launch_gemm<256, EPI_BF16, 4>(th, tb2, tb2, p2, m_tiles_max * ((d + 255) / 256), s);
+  const int mt2 = (R + C2::kTokTile - 1) / C2::kTokTile + G;
+  return launch_gemm<MODE_DOWN>(tw2, tw2, th, p2, mt2 * ((d + 127) / 128), s);
 }
 
 cudaError_t launch_router_gemm(const uint16_t* x, const uint16_t* w_split, const float* offset,
                                int T, int d, int E, float* scores, int32_t* status,
                                cudaStream_t s) {
   if (T == 0) return cudaSuccess;
-  const int BNr = E <= 32 ? 32 : (E <= 64 ? 64 : 128);
   CUtensorMap ta, tb;
-  if (!make_map(&ta, x, d, T, BM) || !make_map(&tb, w_split, 3ull * d, E, BNr))
+  if (!make_map(&ta, x, d, T, 128) || !make_map(&tb, w_split, 3ull * d, E, 128))
     return cudaErrorInvalidValue;
   GemmParams p{};
   p.group_offsets = nullptr;
@@ -469,15 +540,13 @@ cudaError_t launch_router_gemm(const uint16_t* x, const uint16_t* w_split, const
   p.R = T;
   p.num_kb = 3 * d / BK;
   p.a_k_wrap_kb = d / BK;
-  p.b_rows_per_group = 0;
+  p.w_rows_per_group = 0;
   p.out = scores;
   p.ldo = E;
   p.col_offset = offset;
   p.status = status;
-  const int works = ((T + BM - 1) / BM) * ((E + BNr - 1) / BNr);
-  if (BNr == 32) return launch_gemm<32, EPI_SIGMOID, 8>(ta, tb, tb, p, works, s);
-  if (BNr == 64) return launch_gemm<64, EPI_SIGMOID, 8>(ta, tb, tb, p, works, s);
-  return launch_gemm<128, EPI_SIGMOID, 6>(ta, tb, tb, p, works, s);
+  const int works = ((T + 127) / 128) * ((E + 127) / 128);
+  return launch_gemm<MODE_ROUTER>(ta, ta, tb, p, works, s);
 }
 
 }  // namespace moe

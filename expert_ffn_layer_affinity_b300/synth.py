@@ -77,6 +77,10 @@ CONFIGS = {
     "v3_drift": LayerConfig("v3_drift", T=16384, d=7168, E=256, K=8, n_shared=1,
                             I=2048, n_groups=8, topk_groups=4, route_scale=2.5,
                             bias_std=0.01, steps=100, clusters=4, rotate_every=25),
+    # V3 expert shape with 16 experts and 256 rows per expert: the profiling
+    # case (1.4 GB of weights, larger than L2, small enough for a full capture)
+    "v3_e16": LayerConfig("v3_e16", T=512, d=7168, E=16, K=8, n_shared=1, I=2048,
+                          n_groups=8, topk_groups=4, route_scale=2.5, bias_std=0.01),
 }
 DECODE_T = (64, 256, 1024)
 

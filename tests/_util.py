@@ -1,4 +1,5 @@
-"""Small conversions shared by the tests (no layer arithmetic here)."""
+"""Conversions and comparison helpers shared by the tests (the layer's
+arithmetic comes from the oracle only)."""
 import numpy as np
 import torch
 
@@ -19,3 +20,92 @@ def f32_bits(a) -> np.ndarray:
 def sync_status(status: torch.Tensor) -> int:
     torch.cuda.synchronize()
     return int(status.item())
+
+
+class HostExperts:
+    """Oracle-side view of the expert weights: exact fp64 values fetched one
+    expert at a time (the full V3 set does not fit comfortably in host RAM as
+    fp64)."""
+
+    def __init__(self, p):
+        self.p = p
+
+    def __call__(self, e):
+        return (bf16_to_np64(self.p["w1"][e]), bf16_to_np64(self.p["w3"][e]),
+                bf16_to_np64(self.p["w2"][e]))
+
+    def shared(self):
+        return (bf16_to_np64(self.p["ws1"]), bf16_to_np64(self.p["ws3"]),
+                bf16_to_np64(self.p["ws2"]))
+
+
+def check_pass(cfg, p, x, layer, out, sample=None, bias=None):
+    """Compare one pass: routing on every token, output on `sample` tokens."""
+    T = x.shape[0]
+    x64 = bf16_to_np64(x)
+    off = p["logit_offset"].cpu().numpy() if p["logit_offset"] is not None else None
+    b = (bias if bias is not None else p["bias"]).cpu().numpy()
+    s64 = ref.router_affinity64(x64, p["w_r"].cpu().numpy(), off)
+    idx64, gate64 = ref.select_experts(s64, b.astype(np.float64), cfg.K, cfg.n_groups,
+                                       cfg.topk_groups, cfg.route_scale, precision="fp64")
+    kth, grp = ref.near_tie_tokens(s64, b, cfg.K, cfg.n_groups, cfg.topk_groups)
+    gidx = layer.idx[:T].cpu().numpy()
+    mism = np.any(np.sort(gidx, 1) != np.sort(idx64, 1), axis=1)
+    assert not np.any(mism & ~(kth | grp)), np.nonzero(mism & ~(kth | grp))[0][:10]
+    tokens = np.arange(T) if sample is None else sample
+    tokens = tokens[~mism[tokens]]
+    host = HostExperts(p)
+    want = ref.moe_output64(x64, idx64, gate64, host, host.shared(), cfg.n_shared, tokens)
+    got = bf16_to_np64(out[torch.from_numpy(tokens).to(out.device)])
+    err = ref.rel_l2(got, want)
+    assert err < 1e-2, err
+    return dict(rel_l2=err, mismatched_tokens=int(mism.sum()), near_tie=int((kth | grp).sum()),
+                idx64=idx64)
+
+
+def sign_rule_holds(load, b_before, b_after, T, K, E, gamma) -> bool:
+    """Property of the bias feedback on any (load, bias) pair: each expert's
+    bias moved by exactly one fp32 step of gamma in the direction of
+    T*K - E*load, or not at all when the two are equal."""
+    load = np.asarray(load, dtype=np.int64)
+    b0 = np.asarray(b_before, dtype=np.float32)
+    b1 = np.asarray(b_after, dtype=np.float32)
+    g = np.float32(gamma)
+    diff = T * K - E * load
+    want = np.where(diff > 0, b0 + g, np.where(diff < 0, b0 - g, b0)).astype(np.float32)
+    return bool(np.array_equal(want.view(np.uint32), b1.view(np.uint32)))
+
+
+class Trajectory:
+    """The oracle's own bias-feedback trajectory next to the GPU's: loads from
+    the oracle's fp64 routing, updates by the oracle's fp32 rule.  The two are
+    compared bit for bit until a near-tie token (counted) makes a load differ;
+    after that the trajectories may legitimately part and only the sign-rule
+    property of the GPU's own updates is checked."""
+
+    def __init__(self, cfg, bias0):
+        self.cfg = cfg
+        self.b = np.asarray(bias0, dtype=np.float32).copy()
+        self.diverged_at = None
+        self.near_tie_mismatches = 0
+
+    def step(self, step, T, s64, gpu_idx, gpu_load, gpu_b_before, gpu_b_after):
+        c = self.cfg
+        assert sign_rule_holds(gpu_load, gpu_b_before, gpu_b_after, T, c.K, c.E, c.gamma)
+        if self.diverged_at is not None:
+            return
+        idx64, _ = ref.select_experts(s64, self.b.astype(np.float64), c.K, c.n_groups,
+                                      c.topk_groups, c.route_scale, precision="fp64")
+        kth, grp = ref.near_tie_tokens(s64, self.b, c.K, c.n_groups, c.topk_groups)
+        mism = np.any(np.sort(gpu_idx, 1) != np.sort(idx64, 1), axis=1)
+        assert not np.any(mism & ~(kth | grp)), np.nonzero(mism & ~(kth | grp))[0][:10]
+        self.near_tie_mismatches += int(mism.sum())
+        load = ref.expert_load(idx64, c.E)
+        new_b = ref.bias_update(load, self.b, T, c.K, c.E, c.gamma)
+        if np.array_equal(load, np.asarray(gpu_load)):
+            assert np.array_equal(new_b.view(np.uint32),
+                                  np.asarray(gpu_b_after, dtype=np.float32).view(np.uint32))
+        else:
+            assert mism.any()
+            self.diverged_at = step
+        self.b = new_b
