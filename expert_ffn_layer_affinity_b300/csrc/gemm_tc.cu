@@ -11,13 +11,16 @@
 // experts and routed experts"; a group is the run of rows the dispatch step
 // gave to one expert.
 //
-// Expert modes put the WEIGHTS on the MMA's M side (128 weight rows per tile)
-// and the group's TOKENS on the N side, with N chosen per tile as the tokens
-// left rounded up to 16.  An expert with 300 rows thus costs 300 -> 304 rows
-// of MMA work instead of 384 with 128-row token tiles; at the V3 shape the
-// padding drops from about 23% to about 3%.  The epilogue reads the
-// [weight-row x token] accumulator, transposes 32x32 blocks through shared
-// memory and writes token-major rows.
+// Expert modes run on CTA PAIRS (clusters of two, tcgen05 .cta_group::2).
+// The pair puts 256 WEIGHT rows on the MMA's M side (128 in each CTA) and up
+// to 256 of the group's TOKENS on the N side (half staged in each CTA), with
+// N chosen per tile as the tokens left rounded up to 32.  Each CTA thus
+// stages 16 KB of weights and 16 KB of tokens per 64-deep k-block for a
+// 256 x 256 x 64 MMA step: a third less shared-memory fill traffic per FLOP
+// than one CTA can reach, which is what the L2 -> SM path limits.  Padding
+// with N rounded to 32 costs about 6% at the V3 loads (23% with 128-row token
+// tiles).  The epilogue reads the [weight row x token] accumulator of its
+// own CTA, transposes it through shared memory and writes token-major rows.
 //
 // Router mode keeps tokens on M (128) and experts on N (128).  Its K loop is
 // cut into chunks of 4 k-blocks; each chunk is accumulated by the tensor core
@@ -28,7 +31,8 @@
 //
 // CTA layout (192 threads, one CTA per SM, persistent):
 //   warp 0      TMA producer: fills a STAGES-deep shared-memory ring
-//   warp 1      TMEM allocator; lane 0 issues tcgen05.mma and commits
+//   warp 1      TMEM allocator; lane 0 issues tcgen05.mma and commits (in a
+//               pair, only the even CTA issues; its commits reach both CTAs)
 //   warps 2..5  epilogue: tcgen05.ld from TMEM, activation, global stores
 // Work items are (group, column tile, token tile), group-major and token
 // tile fastest, so CTAs that need the same weight tile run side by side and
@@ -55,18 +59,26 @@ enum Mode : int { MODE_SWIGLU = 0, MODE_DOWN = 1, MODE_ROUTER = 2 };
 
 template <int MODE>
 struct Tr;
+// SwiGLU pair tile: 128 output columns x up to 256 tokens.  Each CTA's 128
+// M rows are the 64 w1 rows and the 64 matching w3 rows of its 64 columns,
+// interleaved in blocks of 16 (w1 c..c+15, w3 c..c+15, w1 c+16..c+31, ...),
+// so each 32-lane TMEM quarter holds 16 gate rows and their 16 up rows.
 template <>
 struct Tr<MODE_SWIGLU> {
-  static constexpr int kTokTile = 128, kColTile = 128, kStages = 4, kBufs = 2, kBufCols = 256;
-  static constexpr int kA = 2 * 128 * BK * 2, kB = 128 * BK * 2;  // W1|W3 tiles, token tile
+  static constexpr bool kPair = true;
+  static constexpr int kTokTile = 256, kColTile = 128, kStages = 6, kBufs = 2, kBufCols = 256;
+  static constexpr int kA = 128 * BK * 2, kB = 128 * BK * 2;  // per CTA
 };
+// Down-projection pair tile: 256 output columns x up to 256 tokens.
 template <>
 struct Tr<MODE_DOWN> {
-  static constexpr int kTokTile = 256, kColTile = 128, kStages = 4, kBufs = 2, kBufCols = 256;
-  static constexpr int kA = 128 * BK * 2, kB = 256 * BK * 2;
+  static constexpr bool kPair = true;
+  static constexpr int kTokTile = 256, kColTile = 256, kStages = 6, kBufs = 2, kBufCols = 256;
+  static constexpr int kA = 128 * BK * 2, kB = 128 * BK * 2;
 };
 template <>
 struct Tr<MODE_ROUTER> {
+  static constexpr bool kPair = false;
   static constexpr int kTokTile = 128, kColTile = 128, kStages = 6, kBufs = 4, kBufCols = 128;
   static constexpr int kA = 128 * BK * 2, kB = 128 * BK * 2;      // token tile, w_split tile
 };
@@ -77,7 +89,7 @@ struct Cfg : Tr<MODE> {
   static constexpr int kStageBytes = T::kA + T::kB;
   static constexpr int kTmemCols = T::kBufs * T::kBufCols;
   static constexpr int kNumBars = 2 * T::kStages + 2 * T::kBufs + 1;
-  static constexpr int kXposeBytes = (MODE == MODE_ROUTER) ? 0 : 4 * 32 * 80;
+  static constexpr int kXposeBytes = (MODE == MODE_ROUTER) ? 0 : 4 * 32 * 80;  // per-warp staging
   static constexpr int kSmem = 1024 + T::kStages * kStageBytes + kXposeBytes + kNumBars * 8 + 16 +
                                2 * (kMaxGroups + 1) * 4;
   static_assert(kStageBytes % 1024 == 0, "stages must keep 1024-byte alignment");
@@ -131,10 +143,11 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<const uint32_t*>(&v);
 }
 
-// Tokens of this tile the MMA must cover, rounded up to the N granularity.
+// Tokens of this tile the MMA must cover, rounded up to 32 (16 rows staged
+// in each CTA of the pair).
 __device__ __forceinline__ int tile_n(int rows_left, int tok_tile) {
   const int n = rows_left < tok_tile ? rows_left : tok_tile;
-  return (n + 15) & ~15;
+  return (n + 31) & ~31;
 }
 
 // Writes a 32 (weight row = output column) x 32 (token) block, held one
@@ -157,11 +170,43 @@ __device__ __forceinline__ void store_block_transposed(const uint32_t (&v)[32], 
   __syncwarp();
 }
 
+// SwiGLU on one 32-lane TMEM quarter: lanes 0..15 hold the gate (w1) rows of
+// 16 output columns and lanes 16..31 the up (w3) rows of the same columns,
+// 32 tokens each.  Lane l keeps tokens 16*(l/16) .. +15 of column l%16 and
+// trades the other half with its partner lane l^16.  The 16 x 32 bf16 block
+// goes out as 32 token rows of 32 bytes.
+__device__ __forceinline__ void swiglu_block(const uint32_t (&v)[32], uint8_t* xp, int lane,
+                                             __nv_bfloat16* out, long long row0, int rows_valid,
+                                             int ldo, int col) {
+  const bool gate_lane = lane < 16;
+  const int half = lane >> 4, cl = lane & 15;
+  __nv_bfloat16* x = reinterpret_cast<__nv_bfloat16*>(xp);
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    const uint32_t send = gate_lane ? v[16 + j] : v[j];
+    const uint32_t recv = __shfl_xor_sync(0xFFFFFFFFu, send, 16);
+    const uint32_t mine = gate_lane ? v[j] : v[16 + j];
+    const float a = __uint_as_float(gate_lane ? mine : recv);
+    const float up = __uint_as_float(gate_lane ? recv : mine);
+    const float h = a * __frcp_rn(1.0f + __expf(-a)) * up;
+    x[(half * 16 + j) * 24 + cl] = __float2bfloat16_rn(h);  // row pitch 48 bytes
+  }
+  __syncwarp();
+  if (lane < rows_valid) {
+    const uint4* src = reinterpret_cast<const uint4*>(xp + lane * 48);
+    uint4* dst = reinterpret_cast<uint4*>(out + (row0 + lane) * ldo + col);
+    dst[0] = src[0];
+    dst[1] = src[1];
+  }
+  __syncwarp();
+}
+
 template <int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA2,
                 const __grid_constant__ CUtensorMap tmB, const GemmParams p) {
   using C = Cfg<MODE>;
+  constexpr bool PAIR = C::kPair;
   constexpr int S = C::kStages, NB = C::kBufs;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
@@ -181,6 +226,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = p.G;
+  // CTA pairs: rank 0 issues the MMAs; both iterate the same work list.
+  const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
+  const int unit_id = PAIR ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
+  const int n_units = PAIR ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
 
   if (warp == 0) {
     int carry = 0;
@@ -217,7 +266,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       for (int b = 0; b < NB; ++b) {
         mbar_init(accf_bar(b), 1);
-        mbar_init(acce_bar(b), 128);
+        mbar_init(acce_bar(b), PAIR ? 256 : 128);
       }
       mbar_init(drain_bar, 1);
       *abort_flag = 0;
@@ -225,11 +274,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     }
     __syncwarp();
-    tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
-    tmem_relinquish();
+    if (PAIR) {
+      tmem_alloc_pair(smem_u32(tmem_slot), C::kTmemCols);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
+      tmem_relinquish();
+    }
   }
   tc_fence_before();
   __syncthreads();
+  if (PAIR) cluster_sync_all();  // the peer's barriers are initialised before any remote use
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
@@ -244,11 +299,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t pol_w = l2_policy_evict_normal();
       uint32_t it = 0;
       bool ok = true;
-      for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
+      for (int w = unit_id; w < total && ok; w += n_units) {
         int g, n, m;
         decode_work(w, NT, mt_prefix, G, g, n, m);
-        const int tok_row = row_start[g] + m * C::kTokTile;
-        const int w_row = g * p.w_rows_per_group + n * C::kColTile;
+        const int rows_g = row_start[g + 1] - row_start[g];
+        int tok_row = row_start[g] + m * C::kTokTile;
+        int w_row = g * p.w_rows_per_group + n * C::kColTile;
+        if (PAIR) {
+          tok_row += static_cast<int>(rank) * (tile_n(rows_g - m * C::kTokTile, C::kTokTile) / 2);
+          w_row += static_cast<int>(rank) * (MODE == MODE_SWIGLU ? 64 : 128);
+        }
         for (int kb = 0; kb < p.num_kb; ++kb, ++it) {
           const int s = static_cast<int>(it % S);
           const uint32_t ph = (it / S) & 1u;
@@ -258,19 +318,29 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           const uint32_t sa = tiles + s * C::kStageBytes;
           const uint32_t sb = sa + C::kA;
-          mbar_arrive_expect_tx(full_bar(s), C::kStageBytes);
           if (MODE == MODE_ROUTER) {
+            mbar_arrive_expect_tx(full_bar(s), C::kStageBytes);
             tma_load_2d(sa, &tmA, full_bar(s), (kb % p.a_k_wrap_kb) * BK, tok_row, pol_tok);
             tma_load_2d(sb, &tmB, full_bar(s), kb * BK, w_row, pol_w);
           } else {
-            tma_load_2d(sa, &tmA, full_bar(s), kb * BK, w_row, pol_w);
-            if (MODE == MODE_SWIGLU)
-              tma_load_2d(sa + C::kA / 2, &tmA2, full_bar(s), kb * BK, w_row, pol_w);
-            tma_load_2d(sb, &tmB, full_bar(s), kb * BK, tok_row, pol_tok);
+            // both CTAs' copies complete on the even CTA's barrier
+            if (rank == 0) mbar_arrive_expect_tx(full_bar(s), 2 * C::kStageBytes);
+            const uint32_t fb = mapa_shared(full_bar(s), 0);
+            if (MODE == MODE_SWIGLU) {
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                const uint32_t dst = sa + static_cast<uint32_t>(j * 32 * 128);
+                tma_load_2d_pair(dst, &tmA, fb, kb * BK, w_row + 16 * j, pol_w);
+                tma_load_2d_pair(dst + 16 * 128, &tmA2, fb, kb * BK, w_row + 16 * j, pol_w);
+              }
+            } else {
+              tma_load_2d_pair(sa, &tmA, fb, kb * BK, w_row, pol_w);
+            }
+            tma_load_2d_pair(sb, &tmB, fb, kb * BK, tok_row, pol_tok);
           }
         }
       }
-      if (!ok) {
+      if (!ok && rank == 0) {
         const uint32_t first = it > S ? it - S : 0u;
         for (uint32_t j = first; j < it; ++j)
           wait_plain(full_bar(static_cast<int>(j % S)), (j / S) & 1u, 200000000ull);
@@ -279,10 +349,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issuer
-    if (lane == 0) {
+    if (lane == 0 && rank == 0) {
       uint32_t it = 0, unit = 0;
       bool ok = true, issued = false;
-      for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
+      for (int w = unit_id; w < total && ok; w += n_units) {
         int g, n, m;
         decode_work(w, NT, mt_prefix, G, g, n, m);
         uint32_t idesc;
@@ -290,7 +360,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           idesc = umma_idesc_bf16(128, C::kColTile);
         } else {
           const int rows_g = row_start[g + 1] - row_start[g];
-          idesc = umma_idesc_bf16(128, tile_n(rows_g - m * C::kTokTile, C::kTokTile));
+          idesc = umma_idesc_bf16(256, tile_n(rows_g - m * C::kTokTile, C::kTokTile));
         }
         for (int kb0 = 0; kb0 < p.num_kb && ok; kb0 += chunk_kb, ++unit) {
           const int b = static_cast<int>(unit % NB);
@@ -316,21 +386,21 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int k = 0; k < BK / UMMA_K; ++k) {
               const uint32_t acc = (kb > kb0 || k > 0) ? 1u : 0u;
-              umma_bf16(d_tmem, adesc + 2ull * k, bdesc + 2ull * k, idesc, acc);
-              if (MODE == MODE_SWIGLU) {
-                const uint64_t adesc3 = umma_sdesc_sw128(sa + C::kA / 2);
-                umma_bf16(d_tmem + 128u, adesc3 + 2ull * k, bdesc + 2ull * k, idesc, acc);
-              }
+              if (PAIR) umma_bf16_pair(d_tmem, adesc + 2ull * k, bdesc + 2ull * k, idesc, acc);
+              else umma_bf16(d_tmem, adesc + 2ull * k, bdesc + 2ull * k, idesc, acc);
             }
             issued = true;
-            umma_commit(empty_bar(s));
+            if (PAIR) umma_commit_pair_mc(empty_bar(s), 0x3);
+            else umma_commit(empty_bar(s));
           }
           if (!ok) break;
-          umma_commit(accf_bar(b));
+          if (PAIR) umma_commit_pair_mc(accf_bar(b), 0x3);
+          else umma_commit(accf_bar(b));
         }
       }
       if (!ok && issued) {
-        umma_commit(drain_bar);
+        if (PAIR) umma_commit_pair_mc(drain_bar, 0x1);
+        else umma_commit(drain_bar);
         wait_plain(drain_bar, 0u, 200000000ull);
       }
     }
@@ -341,7 +411,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* xp = xpose + q * 32 * 80;
     uint32_t unit = 0;
     bool ok = true;
-    for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
+    for (int w = unit_id; w < total && ok; w += n_units) {
       int g, n, m;
       decode_work(w, NT, mt_prefix, G, g, n, m);
       const int rows_g = row_start[g + 1] - row_start[g];
@@ -393,35 +463,28 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int tok0 = m * C::kTokTile;
         const int n_eff = tile_n(rows_g - tok0, C::kTokTile);
         const int rows_tile = (rows_g - tok0) < C::kTokTile ? rows_g - tok0 : C::kTokTile;
-        const int col = n * C::kColTile + q * 32;
+        const int col = n * C::kColTile +
+                        (MODE == MODE_SWIGLU ? 64 * static_cast<int>(rank) + 16 * q
+                                             : 128 * static_cast<int>(rank) + 32 * q);
         const long long row0 = static_cast<long long>(row_start[g]) + tok0;
         const bool col_ok = col < p.N;
         const uint32_t taddr = tmem_base + lane_base + static_cast<uint32_t>(b * C::kBufCols);
         __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out);
         for (int c = 0; c < n_eff; c += 32) {
           uint32_t v[32];
-          if (MODE == MODE_SWIGLU) {
-            uint32_t u3[32];
-            tmem_ld32(taddr + c, v);
-            tmem_ld32(taddr + 128 + c, u3);
-            tmem_ld_wait();
-#pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              const float a = __uint_as_float(v[j]), up = __uint_as_float(u3[j]);
-              v[j] = __float_as_uint(a * __frcp_rn(1.0f + __expf(-a)) * up);
-            }
-          } else {
-            tmem_ld32(taddr + c, v);
-            tmem_ld_wait();
-          }
+          tmem_ld32(taddr + c, v);
+          tmem_ld_wait();
           int valid = rows_tile - c;
           if (valid > 32) valid = 32;
           const long long last = row0 + c + valid;
           if (last > p.R) valid -= static_cast<int>(last - p.R);
-          if (col_ok) store_block_transposed(v, xp, lane, out, row0 + c, valid, p.ldo, col);
+          if (col_ok) {
+            if (MODE == MODE_SWIGLU) swiglu_block(v, xp, lane, out, row0 + c, valid, p.ldo, col);
+            else store_block_transposed(v, xp, lane, out, row0 + c, valid, p.ldo, col);
+          }
         }
         tc_fence_before();
-        mbar_arrive(acce_bar(b));
+        mbar_arrive_cluster(mapa_shared(acce_bar(b), 0));
       }
     }
     __syncwarp();
@@ -429,8 +492,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   tc_fence_before();
   __syncthreads();
+  if (PAIR) cluster_sync_all();  // no CTA frees TMEM or exits while its peer still uses it
   tc_fence_after();
-  if (warp == 1) tmem_dealloc(tmem_base, C::kTmemCols);
+  if (warp == 1) {
+    if (PAIR) tmem_dealloc_pair(tmem_base, C::kTmemCols);
+    else tmem_dealloc(tmem_base, C::kTmemCols);
+  }
 }
 
 // ------------------------------------------------------------------ host side
@@ -465,7 +532,7 @@ bool make_map(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer, u
 
 template <int MODE>
 cudaError_t launch_gemm(const CUtensorMap& a, const CUtensorMap& a2, const CUtensorMap& b,
-                        const GemmParams& p, int max_works, cudaStream_t s) {
+                        const GemmParams& p, int max_units, cudaStream_t s) {
   using C = Cfg<MODE>;
   static bool attr_done[64] = {false};
   int dev = 0;
@@ -476,11 +543,23 @@ cudaError_t launch_gemm(const CUtensorMap& a, const CUtensorMap& a2, const CUten
     if (e != cudaSuccess) return e;
     attr_done[dev] = true;
   }
-  int grid = sm_count();
-  if (max_works < grid) grid = max_works;
-  if (grid < 1) grid = 1;
-  gemm_kernel<MODE><<<grid, kThreads, C::kSmem, s>>>(a, a2, b, p);
-  return cudaGetLastError();
+  const int per_unit = C::kPair ? 2 : 1;
+  int units = sm_count() / per_unit;
+  if (max_units < units) units = max_units;
+  if (units < 1) units = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(units * per_unit), 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = C::kSmem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = static_cast<unsigned>(per_unit);
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, gemm_kernel<MODE>, a, a2, b, p);
 }
 
 }  // namespace
@@ -494,11 +573,11 @@ cudaError_t launch_grouped_swiglu(const uint16_t* a, const int32_t* offsets, int
   using C1 = Cfg<MODE_SWIGLU>;
   using C2 = Cfg<MODE_DOWN>;
   CUtensorMap tw1, tw3, tx, tw2, th;
-  if (!make_map(&tw1, w1, d, static_cast<uint64_t>(G) * I, 128) ||
-      !make_map(&tw3, w3, d, static_cast<uint64_t>(G) * I, 128) ||
-      !make_map(&tx, a, d, R, C1::kTokTile) ||
+  if (!make_map(&tw1, w1, d, static_cast<uint64_t>(G) * I, 16) ||
+      !make_map(&tw3, w3, d, static_cast<uint64_t>(G) * I, 16) ||
+      !make_map(&tx, a, d, R, 128) ||
       !make_map(&tw2, w2, I, static_cast<uint64_t>(G) * d, 128) ||
-      !make_map(&th, h, I, R, C2::kTokTile))
+      !make_map(&th, h, I, R, 128))
     return cudaErrorInvalidValue;
   GemmParams p1{};
   p1.group_offsets = offsets;
@@ -522,7 +601,7 @@ cudaError_t launch_grouped_swiglu(const uint16_t* a, const int32_t* offsets, int
   p2.out = y;
   p2.ldo = d;
   const int mt2 = (R + C2::kTokTile - 1) / C2::kTokTile + G;
-  return launch_gemm<MODE_DOWN>(tw2, tw2, th, p2, mt2 * ((d + 127) / 128), s);
+  return launch_gemm<MODE_DOWN>(tw2, tw2, th, p2, mt2 * ((d + 255) / 256), s);
 }
 
 cudaError_t launch_router_gemm(const uint16_t* x, const uint16_t* w_split, const float* offset,
