@@ -60,9 +60,10 @@ enum Mode : int { MODE_SWIGLU = 0, MODE_DOWN = 1, MODE_ROUTER = 2 };
 template <int MODE>
 struct Tr;
 // SwiGLU pair tile: 128 output columns x up to 256 tokens.  Each CTA's 128
-// M rows are the 64 w1 rows and the 64 matching w3 rows of its 64 columns,
-// interleaved in blocks of 16 (w1 c..c+15, w3 c..c+15, w1 c+16..c+31, ...),
-// so each 32-lane TMEM quarter holds 16 gate rows and their 16 up rows.
+// M rows are the 64 w1 rows (TMEM lanes 0..63, the gate) and the 64 matching
+// w3 rows (lanes 64..127, the up projection) of its 64 output columns.  The
+// epilogue warps reading lanes 64..127 hand their values to the warps
+// reading lanes 0..63 through a double-buffered shared-memory exchange.
 template <>
 struct Tr<MODE_SWIGLU> {
   static constexpr bool kPair = true;
@@ -90,8 +91,10 @@ struct Cfg : Tr<MODE> {
   static constexpr int kTmemCols = T::kBufs * T::kBufCols;
   static constexpr int kNumBars = 2 * T::kStages + 2 * T::kBufs + 1;
   static constexpr int kXposeBytes = (MODE == MODE_ROUTER) ? 0 : 4 * 32 * 80;  // per-warp staging
-  static constexpr int kSmem = 1024 + T::kStages * kStageBytes + kXposeBytes + kNumBars * 8 + 16 +
-                               2 * (kMaxGroups + 1) * 4;
+  // SwiGLU: 2 warp pairs x 2 buffers x 32 lanes x 33 fp32 (one padded row per lane)
+  static constexpr int kXchgBytes = (MODE == MODE_SWIGLU) ? 2 * 2 * 32 * 33 * 4 : 0;
+  static constexpr int kSmem = 1024 + T::kStages * kStageBytes + kXposeBytes + kXchgBytes +
+                               (kNumBars + 8) * 8 + 16 + 2 * (kMaxGroups + 1) * 4;
   static_assert(kStageBytes % 1024 == 0, "stages must keep 1024-byte alignment");
   static_assert(kTmemCols <= 512, "tensor memory");
   static_assert(kSmem <= 227 * 1024, "shared memory");
@@ -138,11 +141,6 @@ __device__ __forceinline__ bool wait_plain(uint32_t bar, uint32_t parity, unsign
   return true;
 }
 
-__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
-  const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
-  return *reinterpret_cast<const uint32_t*>(&v);
-}
-
 // Tokens of this tile the MMA must cover, rounded up to 32 (16 rows staged
 // in each CTA of the pair).
 __device__ __forceinline__ int tile_n(int rows_left, int tok_tile) {
@@ -170,37 +168,6 @@ __device__ __forceinline__ void store_block_transposed(const uint32_t (&v)[32], 
   __syncwarp();
 }
 
-// SwiGLU on one 32-lane TMEM quarter: lanes 0..15 hold the gate (w1) rows of
-// 16 output columns and lanes 16..31 the up (w3) rows of the same columns,
-// 32 tokens each.  Lane l keeps tokens 16*(l/16) .. +15 of column l%16 and
-// trades the other half with its partner lane l^16.  The 16 x 32 bf16 block
-// goes out as 32 token rows of 32 bytes.
-__device__ __forceinline__ void swiglu_block(const uint32_t (&v)[32], uint8_t* xp, int lane,
-                                             __nv_bfloat16* out, long long row0, int rows_valid,
-                                             int ldo, int col) {
-  const bool gate_lane = lane < 16;
-  const int half = lane >> 4, cl = lane & 15;
-  __nv_bfloat16* x = reinterpret_cast<__nv_bfloat16*>(xp);
-#pragma unroll
-  for (int j = 0; j < 16; ++j) {
-    const uint32_t send = gate_lane ? v[16 + j] : v[j];
-    const uint32_t recv = __shfl_xor_sync(0xFFFFFFFFu, send, 16);
-    const uint32_t mine = gate_lane ? v[j] : v[16 + j];
-    const float a = __uint_as_float(gate_lane ? mine : recv);
-    const float up = __uint_as_float(gate_lane ? recv : mine);
-    const float h = a * __frcp_rn(1.0f + __expf(-a)) * up;
-    x[(half * 16 + j) * 24 + cl] = __float2bfloat16_rn(h);  // row pitch 48 bytes
-  }
-  __syncwarp();
-  if (lane < rows_valid) {
-    const uint4* src = reinterpret_cast<const uint4*>(xp + lane * 48);
-    uint4* dst = reinterpret_cast<uint4*>(out + (row0 + lane) * ldo + col);
-    dst[0] = src[0];
-    dst[1] = src[1];
-  }
-  __syncwarp();
-}
-
 template <int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA2,
@@ -212,16 +179,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t raw_addr = smem_u32(smem_raw);
   const uint32_t tiles = (raw_addr + 1023u) & ~1023u;
   uint8_t* xpose = smem_raw + (tiles - raw_addr) + S * C::kStageBytes;
-  uint8_t* meta = xpose + C::kXposeBytes;
+  float* xchg = reinterpret_cast<float*>(xpose + C::kXposeBytes);
+  uint8_t* meta = xpose + C::kXposeBytes + C::kXchgBytes;
   const uint32_t bars = smem_u32(meta);
   auto full_bar = [&](int s) { return bars + 8u * s; };
   auto empty_bar = [&](int s) { return bars + 8u * (S + s); };
   auto accf_bar = [&](int b) { return bars + 8u * (2 * S + b); };
   auto acce_bar = [&](int b) { return bars + 8u * (2 * S + NB + b); };
   const uint32_t drain_bar = bars + 8u * (2 * S + 2 * NB);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(meta + 8 * C::kNumBars);
+  // SwiGLU exchange: xfull / xempty for (warp pair, buffer)
+  auto xfull_bar = [&](int pr, int b) { return bars + 8u * (C::kNumBars + 2 * pr + b); };
+  auto xempty_bar = [&](int pr, int b) { return bars + 8u * (C::kNumBars + 4 + 2 * pr + b); };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(meta + 8 * (C::kNumBars + 8));
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  int* mt_prefix = reinterpret_cast<int*>(meta + 8 * C::kNumBars + 16);
+  int* mt_prefix = reinterpret_cast<int*>(meta + 8 * (C::kNumBars + 8) + 16);
   int* row_start = mt_prefix + (kMaxGroups + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -269,6 +240,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(acce_bar(b), PAIR ? 256 : 128);
       }
       mbar_init(drain_bar, 1);
+      for (int i = 0; i < 8; ++i) mbar_init(bars + 8u * (C::kNumBars + i), 1);
       *abort_flag = 0;
       fence_mbar_init();
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -327,12 +299,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (rank == 0) mbar_arrive_expect_tx(full_bar(s), 2 * C::kStageBytes);
             const uint32_t fb = mapa_shared(full_bar(s), 0);
             if (MODE == MODE_SWIGLU) {
-#pragma unroll
-              for (int j = 0; j < 4; ++j) {
-                const uint32_t dst = sa + static_cast<uint32_t>(j * 32 * 128);
-                tma_load_2d_pair(dst, &tmA, fb, kb * BK, w_row + 16 * j, pol_w);
-                tma_load_2d_pair(dst + 16 * 128, &tmA2, fb, kb * BK, w_row + 16 * j, pol_w);
-              }
+              tma_load_2d_pair(sa, &tmA, fb, kb * BK, w_row, pol_w);
+              tma_load_2d_pair(sa + 64 * 128, &tmA2, fb, kb * BK, w_row, pol_w);
             } else {
               tma_load_2d_pair(sa, &tmA, fb, kb * BK, w_row, pol_w);
             }
@@ -409,7 +377,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;  // this warp may read TMEM lanes 32q .. 32q+31
     uint8_t* xp = xpose + q * 32 * 80;
-    uint32_t unit = 0;
+    uint32_t unit = 0, xchunk = 0;
     bool ok = true;
     for (int w = unit_id; w < total && ok; w += n_units) {
       int g, n, m;
@@ -464,13 +432,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int n_eff = tile_n(rows_g - tok0, C::kTokTile);
         const int rows_tile = (rows_g - tok0) < C::kTokTile ? rows_g - tok0 : C::kTokTile;
         const int col = n * C::kColTile +
-                        (MODE == MODE_SWIGLU ? 64 * static_cast<int>(rank) + 16 * q
+                        (MODE == MODE_SWIGLU ? 64 * static_cast<int>(rank) + 32 * (q & 1)
                                              : 128 * static_cast<int>(rank) + 32 * q);
         const long long row0 = static_cast<long long>(row_start[g]) + tok0;
         const bool col_ok = col < p.N;
         const uint32_t taddr = tmem_base + lane_base + static_cast<uint32_t>(b * C::kBufCols);
         __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out);
-        for (int c = 0; c < n_eff; c += 32) {
+        for (int c = 0; c < n_eff && ok; c += 32, ++xchunk) {
           uint32_t v[32];
           tmem_ld32(taddr + c, v);
           tmem_ld_wait();
@@ -478,11 +446,36 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (valid > 32) valid = 32;
           const long long last = row0 + c + valid;
           if (last > p.R) valid -= static_cast<int>(last - p.R);
-          if (col_ok) {
-            if (MODE == MODE_SWIGLU) swiglu_block(v, xp, lane, out, row0 + c, valid, p.ldo, col);
-            else store_block_transposed(v, xp, lane, out, row0 + c, valid, p.ldo, col);
+          if (MODE == MODE_SWIGLU) {
+            // pair (q, q + 2): lanes 64..127 (up) hand over to lanes 0..63 (gate)
+            const int pr = q & 1, xb = static_cast<int>(xchunk & 1u);
+            const uint32_t xph = (xchunk >> 1) & 1u;
+            float* xrow = xchg + ((pr * 2 + xb) * 32 + lane) * 33;
+            if (q >= 2) {
+              ok = __all_sync(0xFFFFFFFFu,
+                              mbar_wait(xempty_bar(pr, xb), xph ^ 1u, abort_flag, p.status));
+              if (!ok) break;
+#pragma unroll
+              for (int j = 0; j < 32; ++j) xrow[j] = __uint_as_float(v[j]);
+              __syncwarp();
+              if (lane == 0) mbar_arrive(xfull_bar(pr, xb));
+            } else {
+              ok = __all_sync(0xFFFFFFFFu, mbar_wait(xfull_bar(pr, xb), xph, abort_flag, p.status));
+              if (!ok) break;
+#pragma unroll
+              for (int j = 0; j < 32; ++j) {
+                const float a = __uint_as_float(v[j]);
+                v[j] = __float_as_uint(a * __frcp_rn(1.0f + __expf(-a)) * xrow[j]);
+              }
+              __syncwarp();
+              if (lane == 0) mbar_arrive(xempty_bar(pr, xb));
+              if (col_ok) store_block_transposed(v, xp, lane, out, row0 + c, valid, p.ldo, col);
+            }
+          } else if (col_ok) {
+            store_block_transposed(v, xp, lane, out, row0 + c, valid, p.ldo, col);
           }
         }
+        if (!ok) break;
         tc_fence_before();
         mbar_arrive_cluster(mapa_shared(acce_bar(b), 0));
       }
@@ -573,8 +566,8 @@ cudaError_t launch_grouped_swiglu(const uint16_t* a, const int32_t* offsets, int
   using C1 = Cfg<MODE_SWIGLU>;
   using C2 = Cfg<MODE_DOWN>;
   CUtensorMap tw1, tw3, tx, tw2, th;
-  if (!make_map(&tw1, w1, d, static_cast<uint64_t>(G) * I, 16) ||
-      !make_map(&tw3, w3, d, static_cast<uint64_t>(G) * I, 16) ||
+  if (!make_map(&tw1, w1, d, static_cast<uint64_t>(G) * I, 64) ||
+      !make_map(&tw3, w3, d, static_cast<uint64_t>(G) * I, 64) ||
       !make_map(&tx, a, d, R, 128) ||
       !make_map(&tw2, w2, I, static_cast<uint64_t>(G) * d, 128) ||
       !make_map(&th, h, I, R, 128))
