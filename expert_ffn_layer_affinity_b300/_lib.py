@@ -17,6 +17,7 @@ MOE_ERR_INVALID_ARG = -1
 MOE_ERR_UNSUPPORTED_SHAPE = -2
 MOE_ERR_CUDA = -3
 MOE_ERR_WORKSPACE = -4
+MOE_ERR_SCRATCH_LIMIT = -5
 MOE_DEV_TIMEOUT = 1
 MOE_DEV_NONFINITE = 2
 MOE_DEV_BAD_INDEX = 4
@@ -26,6 +27,7 @@ _STATUS_NAMES = {
     MOE_ERR_UNSUPPORTED_SHAPE: "MOE_ERR_UNSUPPORTED_SHAPE",
     MOE_ERR_CUDA: "MOE_ERR_CUDA",
     MOE_ERR_WORKSPACE: "MOE_ERR_WORKSPACE",
+    MOE_ERR_SCRATCH_LIMIT: "MOE_ERR_SCRATCH_LIMIT",
 }
 
 # name -> (restype, argtypes); every pointer is passed as c_void_p
@@ -36,6 +38,7 @@ SIGNATURES = {
     "moe_router_prepare": (I, [P, I, I, P, P]),
     "moe_router_topk": (I, [P, P, P, P, P, I, I, I, I, I, I, F, P, P, P, P, P, P, Z, P]),
     "moe_permute": (I, [P, I, I, I, P, I, P, P, P, P, P, P, Z, P]),
+    "moe_permute_static": (I, [P, I, I, I, P, I, P, P, P, P, P, P]),
     "moe_grouped_swiglu": (I, [P, P, I, I, I, I, P, P, P, P, P, P, P]),
     "moe_combine": (I, [P, P, P, P, I, I, I, P, P]),
     "moe_bias_update": (I, [P, P, I, I, I, F, P, P]),
@@ -118,6 +121,17 @@ def moe_permute(topk_idx, T, K, E, x, d, expert_offsets, row_of, tok_of, x_perm,
                           _ptr(row_of), _ptr(tok_of), _ptr(x_perm), _ptr(status_dev),
                           _ptr(ws), ws_bytes, _stream(stream))
     return _check("moe_permute", r) if check else r
+
+
+def moe_permute_static(topk_idx, T, K, E, x, d, expert_offsets, row_of, tok_of, x_perm,
+                       status_dev, stream=None, check=True):
+    """moe_permute without a workspace, for callers that cannot allocate
+    device memory at call time; its scratch is a fixed 256 KiB array inside
+    the library, shared by all calls (see include/moe.h)."""
+    r = lib().moe_permute_static(_ptr(topk_idx), T, K, E, _ptr(x), d, _ptr(expert_offsets),
+                                 _ptr(row_of), _ptr(tok_of), _ptr(x_perm), _ptr(status_dev),
+                                 _stream(stream))
+    return _check("moe_permute_static", r) if check else r
 
 
 def moe_grouped_swiglu(a, group_offsets, n_groups, R, d, I, w1, w3, w2, h, y, status_dev,

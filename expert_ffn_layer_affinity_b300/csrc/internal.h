@@ -28,6 +28,10 @@ cudaError_t launch_router_split(const float* w_r, int E, int d, uint16_t* w_spli
 // ---- permute (permute.cu)
 constexpr int kPermuteTile = 1024;   // (token, slot) entries per counting tile
 size_t permute_ws_bytes(int T, int K, int E);
+// Fixed device scratch for the allocation-free permute: (T*K/1024 rounded up)
+// x E counts of int32, at most this many.
+constexpr size_t kPermuteStaticScratchInts = 65536;  // 256 KiB
+cudaError_t permute_static_scratch(int32_t** ptr);
 cudaError_t launch_permute(const int32_t* idx, int T, int K, int E, const uint16_t* x, int d,
                            int32_t* offsets, int32_t* row_of, int32_t* tok_of, uint16_t* x_perm,
                            int32_t* status, int32_t* tile_counts, cudaStream_t s);

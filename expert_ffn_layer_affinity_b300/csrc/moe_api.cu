@@ -145,6 +145,31 @@ moe_status moe_permute(const int32_t* topk_idx, int T, int K, int E, const void*
                                     static_cast<cudaStream_t>(stream)));
 }
 
+moe_status moe_permute_static(const int32_t* topk_idx, int T, int K, int E, const void* x_bf16,
+                              int d, int32_t* expert_offsets, int32_t* row_of, int32_t* tok_of,
+                              void* x_perm_bf16, int32_t* status_dev, moe_stream_t stream) {
+  if (T < 0 || K < 1 || E < 1 || !expert_offsets) return MOE_ERR_INVALID_ARG;
+  if (T > 0 && (!topk_idx || !row_of || !tok_of)) return MOE_ERR_INVALID_ARG;
+  if (E > 512 || K > 32 || static_cast<long long>(T) * K >= (1ll << 31))
+    return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (x_bf16 != nullptr) {
+    if (!x_perm_bf16) return MOE_ERR_INVALID_ARG;
+    if (d < 8 || d % 8 || !aligned16(x_bf16) || !aligned16(x_perm_bf16))
+      return MOE_ERR_UNSUPPORTED_SHAPE;
+  }
+  if (permute_ws_bytes(T, K, E) > kPermuteStaticScratchInts * sizeof(int32_t))
+    return MOE_ERR_SCRATCH_LIMIT;
+  int32_t* scratch = nullptr;
+  if (T > 0) {
+    const cudaError_t e = permute_static_scratch(&scratch);
+    if (e != cudaSuccess) return cuda_status(e);
+  }
+  return cuda_status(launch_permute(topk_idx, T, K, E, static_cast<const uint16_t*>(x_bf16), d,
+                                    expert_offsets, row_of, tok_of,
+                                    static_cast<uint16_t*>(x_perm_bf16), status_dev, scratch,
+                                    static_cast<cudaStream_t>(stream)));
+}
+
 moe_status moe_grouped_swiglu(const void* a_bf16, const int32_t* group_offsets, int n_groups,
                               int R, int d, int I, const void* w1_bf16, const void* w3_bf16,
                               const void* w2_bf16, void* h_bf16, void* y_bf16,

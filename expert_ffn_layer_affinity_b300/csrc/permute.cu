@@ -156,6 +156,30 @@ __global__ void __launch_bounds__(256) gather_kernel(const uint4* __restrict__ x
 
 }  // namespace
 
+// Scratch of moe_permute_static: the per-tile expert counts of one call live
+// in this fixed device array instead of caller-provided workspace.  Every GPU
+// that loads the library holds it until the process exits.  All calls share
+// it, so calls whose kernels overlap on the GPU race on it.
+static __device__ __align__(256) int32_t g_permute_scratch[kPermuteStaticScratchInts];
+
+cudaError_t permute_static_scratch(int32_t** ptr) {
+  // In host code the symbol is only a host-side stand-in; the device address
+  // is looked up once per device, with that device current.
+  static int32_t* cached[64] = {nullptr};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (cached[dev] == nullptr) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_permute_scratch);
+    if (e != cudaSuccess) return e;
+    cached[dev] = static_cast<int32_t*>(p);
+  }
+  *ptr = cached[dev];
+  return cudaSuccess;
+}
+
 size_t permute_ws_bytes(int T, int K, int E) {
   const size_t R = static_cast<size_t>(T) * K;
   const size_t n_tiles = (R + kTile - 1) / kTile;

@@ -53,6 +53,7 @@ typedef void* moe_stream_t; /* a cudaStream_t */
 #define MOE_ERR_UNSUPPORTED_SHAPE (-2) /* outside the limits above */
 #define MOE_ERR_CUDA (-3)              /* a CUDA runtime/driver call failed */
 #define MOE_ERR_WORKSPACE (-4)         /* workspace smaller than required */
+#define MOE_ERR_SCRATCH_LIMIT (-5)     /* shape needs more than a fixed scratch array holds */
 
 /* Bits OR-ed into *status_dev by the kernels. */
 #define MOE_DEV_TIMEOUT 1u    /* a bounded mbarrier wait ran out (the kernel returned early) */
@@ -113,6 +114,33 @@ moe_status moe_permute(const int32_t* topk_idx, int T, int K, int E, const void*
                        int d, int32_t* expert_offsets, int32_t* row_of, int32_t* tok_of,
                        void* x_perm_bf16, int32_t* status_dev, void* ws, size_t ws_bytes,
                        moe_stream_t stream);
+
+/* Allocation-free variant of moe_permute.  (The method has no counterpart of
+ * this: it only changes where the call keeps its temporary data.)
+ *
+ * For callers that cannot allocate device memory at call time: for example a
+ * plugin running inside a host application that owns every device allocation
+ * through its own pool and hands out no workspace, or a latency-critical
+ * serving loop that must never call cudaMalloc once it has started (an
+ * allocation can synchronise the device and stall every stream).  Arguments,
+ * outputs and results are exactly those of moe_permute; only the workspace
+ * is gone.
+ *
+ * The per-tile expert counts go to a fixed array of 65536 int32 (256 KiB)
+ * compiled into this library, which every GPU that loads the library keeps
+ * until the process exits.  Limit: ceil(T*K / 1024) * E <= 65536 (for
+ * instance T*K <= 262144 with E = 256); larger shapes return
+ * MOE_ERR_SCRATCH_LIMIT before anything is launched.  Each call overwrites
+ * the counts it uses, so nothing has to be cleared between calls.
+ *
+ * The first call on each device looks up the array's device address (with
+ * that device current) and caches it; make that first call before any stream
+ * capture.  All calls share the one array: calls whose kernels can overlap on
+ * the GPU (other streams, other host threads) race on it, so the caller must
+ * serialise them.  No device memory is allocated or freed by this call. */
+moe_status moe_permute_static(const int32_t* topk_idx, int T, int K, int E, const void* x_bf16,
+                              int d, int32_t* expert_offsets, int32_t* row_of, int32_t* tok_of,
+                              void* x_perm_bf16, int32_t* status_dev, moe_stream_t stream);
 
 /* Step 4b, grouped SwiGLU experts: for each group g and each row r in
  * [group_offsets[g], group_offsets[g+1]):
