@@ -30,6 +30,11 @@ METRIC = "MoE-layer tokens/s (V3-shaped, bf16) and % of tensor-core / HBM roofli
 CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
                 "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
                 "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+# DRAM bytes (read + write) per routed expert of the two expert-GEMM launches,
+# from ncu dram__bytes on the 16-expert profiling case (profiles/gemm_pair_v3e16.md),
+# scaled by the experts a launch processes.  Must be re-measured when those
+# kernels change.
+GEMM_TRAFFIC_PER_EXPERT = (0.998950912e9 + 17.472512e6 + 486.599168e6 + 48.930048e6) / 16
 KERNELS_PER_STEP = 12  # router GEMM, selection, 4 permute, 2+2 grouped GEMM, combine, bias update
 
 
@@ -47,6 +52,8 @@ def parse():
                     help="tokens per step for --impl reference")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--feedback-steps", type=int, default=None,
+                    help="steps of the mid / drift feedback runs (default: the workload's)")
     ap.add_argument("--shared-stream", action="store_true",
                     help="run the shared expert on a second stream")
     return ap.parse_args()
@@ -216,8 +223,15 @@ def run_ours(args):
     cfg = load_config(args.config)
     p = synth.make_params(cfg, "cuda")            # identical replicas on every rank
     layer = MoELayer(cfg, p, device=f"cuda:{local}", shared_stream=args.shared_stream)
+    bias0 = layer.bias.clone()
     del p
-    n_batches = 2
+    feedback = cfg.steps > 1                     # mid / drift: a bias-feedback run
+    if feedback:
+        # one fresh batch per step, all resident in HBM before timing
+        args.steps = cfg.steps if args.feedback_steps is None else args.feedback_steps
+        n_batches = args.steps
+    else:
+        n_batches = 2
     xs = [synth.make_tokens(cfg, step=i, device="cuda", seed=cfg.seed + 7777 * rank)
           for i in range(n_batches)]
     stream = torch.cuda.current_stream()
@@ -231,6 +245,8 @@ def run_ours(args):
     torch.cuda.synchronize()
     if layer.device_status() != 0:
         raise RuntimeError(f"device status {layer.device_status()} during warm-up")
+    layer.bias.copy_(bias0)                      # the timed trajectory starts from the initial bias
+    stats_hist = torch.zeros(args.steps, 4, dtype=torch.float32, device="cuda")
     names = ["route", "permute", "routed", "shared", "combine"]
     marks = [{n: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
               for n in names} for _ in range(args.steps)]
@@ -242,7 +258,7 @@ def run_ours(args):
     clocks.mark_start()
     ev0.record(stream)
     for i in range(args.steps):
-        layer.step(xs[i % n_batches], group=group, marks=marks[i])
+        layer.step(xs[i % n_batches], group=group, marks=marks[i], stats_out=stats_hist[i])
     ev1.record(stream)
     torch.cuda.synchronize()
     clocks.mark_stop()
@@ -261,7 +277,7 @@ def run_ours(args):
     # end to end: host (pinned) -> device copy of the step's tokens, the pass
     # and bias update, device -> host copy of the output, every step
     e2e = None
-    if not args.no_e2e:
+    if not args.no_e2e and not feedback:
         x_host = [x.cpu().pin_memory() for x in xs]
         out_host = torch.empty(cfg.T, cfg.d, dtype=torch.bfloat16).pin_memory()
         x_dev = torch.empty_like(xs[0])
@@ -305,12 +321,22 @@ def run_ours(args):
         k["gbs"] = round(a["bytes"] / (per[n] * 1e-3) / 1e9, 1)
         kernels[n] = k
     routed_tf = alg["routed"]["flops"] / (per["routed"] * 1e-3) / 1e12
-    roofline = {"bound": "tensor", "achieved": round(routed_tf, 1), "peak": pk["bf16_sust"],
-                "unit": "TFLOP/s", "frac": round(routed_tf / pk["bf16_sust"], 4),
-                "traffic": None,
-                "kernel": "moe_grouped_swiglu (routed experts: GEMM1+SwiGLU and GEMM2 launches)",
-                "peak_kind": f"bf16 sustained, {pk['src']}",
-                "frac_of_burst": round(routed_tf / pk["bf16"], 4)}
+    if cfg.name == "v3_decode":
+        # decode: the expert GEMMs stream the weights of the touched experts
+        wbytes = 3.0 * (touched + cfg.n_shared) * cfg.I * cfg.d * 2
+        gbs = wbytes / ((per["routed"] + per["shared"]) * 1e-3) / 1e9
+        roofline = {"bound": "hbm", "achieved": round(gbs, 1), "peak": pk["hbm"], "unit": "GB/s",
+                    "frac": round(gbs / pk["hbm"], 4), "traffic": None,
+                    "kernel": "moe_grouped_swiglu routed + shared (expert-weight streaming)",
+                    "peak_kind": f"HBM copy, {pk['src']}",
+                    "weight_bytes_per_step": wbytes}
+    else:
+        roofline = {"bound": "tensor", "achieved": round(routed_tf, 1), "peak": pk["bf16_sust"],
+                    "unit": "TFLOP/s", "frac": round(routed_tf / pk["bf16_sust"], 4),
+                    "traffic": GEMM_TRAFFIC_PER_EXPERT * touched if cfg.d == 7168 else None,
+                    "kernel": "moe_grouped_swiglu (routed experts: GEMM1+SwiGLU and GEMM2 launches)",
+                    "peak_kind": f"bf16 sustained, {pk['src']}",
+                    "frac_of_burst": round(routed_tf / pk["bf16"], 4)}
     layer_tf = cfg.expert_flops() / (ms_step * 1e-3) / 1e12
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
@@ -330,11 +356,22 @@ def run_ours(args):
                               "frac_of_burst": round(layer_tf / pk["bf16"], 4)},
         "kernels": kernels,
         "experts_touched": touched,
+        "hbm_kernels": {n: {"gbs": kernels[n]["gbs"],
+                            "frac": round(kernels[n]["gbs"] / pk["hbm"], 4)}
+                        for n in ("permute", "combine")},
         "gpu_launches": KERNELS_PER_STEP * args.steps,
         "device_status": status,
         "clocks": clk,
         "e2e": e2e,
     }
+    if feedback:
+        h = stats_hist.cpu().numpy()
+        line["feedback"] = {"steps": args.steps, "gamma": cfg.gamma,
+                            "max_over_mean_per_step": [round(float(v), 4) for v in h[:, 2]],
+                            "cv_per_step": [round(float(v), 4) for v in h[:, 3]],
+                            "first": round(float(h[0, 2]), 4), "last": round(float(h[-1, 2]), 4),
+                            "min": round(float(h[:, 2].min()), 4),
+                            "max": round(float(h[:, 2].max()), 4)}
     if not args.no_cpu_baseline and world == 1:
         line["cpu_baseline"] = cpu_baseline(cfg, layer, xs[0], args.cpu_sample)
     print(json.dumps(line), flush=True)

@@ -67,27 +67,35 @@ struct Tr;
 template <>
 struct Tr<MODE_SWIGLU> {
   static constexpr bool kPair = true;
-  static constexpr int kTokTile = 256, kColTile = 128, kStages = 6, kBufs = 2, kBufCols = 256;
-  static constexpr int kA = 128 * BK * 2, kB = 128 * BK * 2;  // per CTA
+  static constexpr int kTokTile = 256, kColTile = 128, kStages = 6, kBoxes = 1, kBufs = 2,
+                       kBufCols = 256;
+  static constexpr int kA = 128 * BK * 2, kB = 128 * BK * 2;  // per CTA and 64-wide k-block
 };
 // Down-projection pair tile: 256 output columns x up to 256 tokens.
 template <>
 struct Tr<MODE_DOWN> {
   static constexpr bool kPair = true;
-  static constexpr int kTokTile = 256, kColTile = 256, kStages = 6, kBufs = 2, kBufCols = 256;
+  static constexpr int kTokTile = 256, kColTile = 256, kStages = 6, kBoxes = 1, kBufs = 2,
+                       kBufCols = 256;
   static constexpr int kA = 128 * BK * 2, kB = 128 * BK * 2;
 };
 template <>
 struct Tr<MODE_ROUTER> {
   static constexpr bool kPair = false;
-  static constexpr int kTokTile = 128, kColTile = 128, kStages = 6, kBufs = 4, kBufCols = 128;
+  static constexpr int kTokTile = 128, kColTile = 128, kStages = 6, kBoxes = 1, kBufs = 4,
+                       kBufCols = 128;
   static constexpr int kA = 128 * BK * 2, kB = 128 * BK * 2;      // token tile, w_split tile
 };
 
 template <int MODE>
 struct Cfg : Tr<MODE> {
   using T = Tr<MODE>;
-  static constexpr int kStageBytes = T::kA + T::kB;
+  // A stage holds kBoxes consecutive 64-wide k-blocks of both operands, laid
+  // out [A_0 .. A_{n-1}][B_0 .. B_{n-1}].  (Measured on the V3 shape: one box
+  // per stage with 6 stages beats two boxes with 3 stages; HBM itself streams
+  // these boxes at ~6.6 TB/s, and the shared-memory fill from L2 is bound by
+  // the bytes in flight per SM.)
+  static constexpr int kStageBytes = T::kBoxes * (T::kA + T::kB);
   static constexpr int kTmemCols = T::kBufs * T::kBufCols;
   static constexpr int kNumBars = 2 * T::kStages + 2 * T::kBufs + 1;
   static constexpr int kXposeBytes = (MODE == MODE_ROUTER) ? 0 : 4 * 32 * 80;  // per-warp staging
@@ -263,6 +271,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int NT = (p.N + C::kColTile - 1) / C::kColTile;
   const int total = mt_prefix[G] * NT;
   const int chunk_kb = (MODE == MODE_ROUTER) ? kRouterChunkKb : p.num_kb;
+  const int num_st = (p.num_kb + C::kBoxes - 1) / C::kBoxes;           // stages per tile
+  const int chunk_st = (MODE == MODE_ROUTER) ? kRouterChunkKb : num_st;  // stages per TMEM unit
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -281,30 +291,39 @@ __global__ void __launch_bounds__(kThreads, 1)
           tok_row += static_cast<int>(rank) * (tile_n(rows_g - m * C::kTokTile, C::kTokTile) / 2);
           w_row += static_cast<int>(rank) * (MODE == MODE_SWIGLU ? 64 : 128);
         }
-        for (int kb = 0; kb < p.num_kb; ++kb, ++it) {
+        for (int st = 0; st < num_st; ++st, ++it) {
           const int s = static_cast<int>(it % S);
           const uint32_t ph = (it / S) & 1u;
           if (!mbar_wait(empty_bar(s), ph ^ 1u, abort_flag, p.status)) {
             ok = false;
             break;
           }
+          const int kb0 = st * C::kBoxes;
+          const int nbox = (p.num_kb - kb0) < C::kBoxes ? p.num_kb - kb0 : C::kBoxes;
           const uint32_t sa = tiles + s * C::kStageBytes;
-          const uint32_t sb = sa + C::kA;
+          const uint32_t sb = sa + C::kBoxes * C::kA;
+          const uint32_t bytes = static_cast<uint32_t>(nbox * (C::kA + C::kB));
           if (MODE == MODE_ROUTER) {
-            mbar_arrive_expect_tx(full_bar(s), C::kStageBytes);
-            tma_load_2d(sa, &tmA, full_bar(s), (kb % p.a_k_wrap_kb) * BK, tok_row, pol_tok);
-            tma_load_2d(sb, &tmB, full_bar(s), kb * BK, w_row, pol_w);
+            mbar_arrive_expect_tx(full_bar(s), bytes);
+            tma_load_2d(sa, &tmA, full_bar(s), (kb0 % p.a_k_wrap_kb) * BK, tok_row, pol_tok);
+            tma_load_2d(sb, &tmB, full_bar(s), kb0 * BK, w_row, pol_w);
           } else {
             // both CTAs' copies complete on the even CTA's barrier
-            if (rank == 0) mbar_arrive_expect_tx(full_bar(s), 2 * C::kStageBytes);
+            if (rank == 0) mbar_arrive_expect_tx(full_bar(s), 2 * bytes);
             const uint32_t fb = mapa_shared(full_bar(s), 0);
-            if (MODE == MODE_SWIGLU) {
-              tma_load_2d_pair(sa, &tmA, fb, kb * BK, w_row, pol_w);
-              tma_load_2d_pair(sa + 64 * 128, &tmA2, fb, kb * BK, w_row, pol_w);
-            } else {
-              tma_load_2d_pair(sa, &tmA, fb, kb * BK, w_row, pol_w);
+            for (int j = 0; j < nbox; ++j) {
+              const uint32_t aj = sa + static_cast<uint32_t>(j * C::kA);
+              const int kx = (kb0 + j) * BK;
+              if (MODE == MODE_SWIGLU) {
+                tma_load_2d_pair(aj, &tmA, fb, kx, w_row, pol_w);
+                tma_load_2d_pair(aj + 64 * 128, &tmA2, fb, kx, w_row, pol_w);
+              } else {
+                tma_load_2d_pair(aj, &tmA, fb, kx, w_row, pol_w);
+              }
             }
-            tma_load_2d_pair(sb, &tmB, fb, kb * BK, tok_row, pol_tok);
+            for (int j = 0; j < nbox; ++j)
+              tma_load_2d_pair(sb + static_cast<uint32_t>(j * C::kB), &tmB, fb, (kb0 + j) * BK,
+                               tok_row, pol_tok);
           }
         }
       }
@@ -330,7 +349,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int rows_g = row_start[g + 1] - row_start[g];
           idesc = umma_idesc_bf16(256, tile_n(rows_g - m * C::kTokTile, C::kTokTile));
         }
-        for (int kb0 = 0; kb0 < p.num_kb && ok; kb0 += chunk_kb, ++unit) {
+        for (int st0 = 0; st0 < num_st && ok; st0 += chunk_st, ++unit) {
           const int b = static_cast<int>(unit % NB);
           const uint32_t bph = (unit / NB) & 1u;
           if (!mbar_wait(acce_bar(b), bph ^ 1u, abort_flag, p.status)) {
@@ -339,8 +358,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tc_fence_after();
           const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(b * C::kBufCols);
-          const int kb1 = (kb0 + chunk_kb < p.num_kb) ? kb0 + chunk_kb : p.num_kb;
-          for (int kb = kb0; kb < kb1; ++kb, ++it) {
+          const int st1 = (st0 + chunk_st < num_st) ? st0 + chunk_st : num_st;
+          for (int st = st0; st < st1; ++st, ++it) {
             const int s = static_cast<int>(it % S);
             const uint32_t ph = (it / S) & 1u;
             if (!mbar_wait(full_bar(s), ph, abort_flag, p.status)) {
@@ -348,14 +367,19 @@ __global__ void __launch_bounds__(kThreads, 1)
               break;
             }
             tc_fence_after();
+            const int kb0 = st * C::kBoxes;
+            const int nbox = (p.num_kb - kb0) < C::kBoxes ? p.num_kb - kb0 : C::kBoxes;
             const uint32_t sa = tiles + s * C::kStageBytes;
-            const uint64_t adesc = umma_sdesc_sw128(sa);
-            const uint64_t bdesc = umma_sdesc_sw128(sa + C::kA);
+            for (int j = 0; j < nbox; ++j) {
+              const uint64_t adesc = umma_sdesc_sw128(sa + static_cast<uint32_t>(j * C::kA));
+              const uint64_t bdesc =
+                  umma_sdesc_sw128(sa + static_cast<uint32_t>(C::kBoxes * C::kA + j * C::kB));
 #pragma unroll
-            for (int k = 0; k < BK / UMMA_K; ++k) {
-              const uint32_t acc = (kb > kb0 || k > 0) ? 1u : 0u;
-              if (PAIR) umma_bf16_pair(d_tmem, adesc + 2ull * k, bdesc + 2ull * k, idesc, acc);
-              else umma_bf16(d_tmem, adesc + 2ull * k, bdesc + 2ull * k, idesc, acc);
+              for (int k = 0; k < BK / UMMA_K; ++k) {
+                const uint32_t acc = (st > st0 || j > 0 || k > 0) ? 1u : 0u;
+                if (PAIR) umma_bf16_pair(d_tmem, adesc + 2ull * k, bdesc + 2ull * k, idesc, acc);
+                else umma_bf16(d_tmem, adesc + 2ull * k, bdesc + 2ull * k, idesc, acc);
+              }
             }
             issued = true;
             if (PAIR) umma_commit_pair_mc(empty_bar(s), 0x3);

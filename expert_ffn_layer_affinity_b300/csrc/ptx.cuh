@@ -259,3 +259,14 @@ __device__ __forceinline__ void umma_commit_pair_mc(uint32_t bar, uint16_t cta_m
 }
 
 }  // namespace moe
+
+namespace moe {
+// Ask L2 to fetch a box of a tiled tensor ahead of the load that will need
+// it (no shared memory is written and nothing is signalled).
+__device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap* map, int32_t x, int32_t y) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(x), "r"(y)
+               : "memory");
+}
+}  // namespace moe

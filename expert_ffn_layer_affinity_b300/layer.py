@@ -132,7 +132,7 @@ class MoELayer:
         mark("combine", 1)
         return self.out[:T]
 
-    def bias_update(self, T: int, stream=None, group=None):
+    def bias_update(self, T: int, stream=None, group=None, stats_out=None):
         """Sign-rule bias update from this pass's loads.  With a process
         group, the loads of all ranks are summed first (each rank routed its
         own T tokens), so every replica applies the same update for the
@@ -143,11 +143,13 @@ class MoELayer:
             from .dist import allreduce_loads
             T_total = allreduce_loads(self.load, group)
             T_total *= T
-        L.moe_bias_update(self.load, self.bias, T_total, c.K, c.E, c.gamma, self.stats, stream)
+        stats = self.stats if stats_out is None else stats_out
+        L.moe_bias_update(self.load, self.bias, T_total, c.K, c.E, c.gamma, stats, stream)
 
-    def step(self, x: torch.Tensor, stream=None, group=None, marks=None) -> torch.Tensor:
+    def step(self, x: torch.Tensor, stream=None, group=None, marks=None,
+             stats_out=None) -> torch.Tensor:
         out = self.forward(x, stream, marks)
-        self.bias_update(x.shape[0], stream, group)
+        self.bias_update(x.shape[0], stream, group, stats_out)
         return out
 
     def device_status(self) -> int:
