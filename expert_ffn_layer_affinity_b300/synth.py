@@ -81,6 +81,10 @@ CONFIGS = {
     # case (1.4 GB of weights, larger than L2, small enough for a full capture)
     "v3_e16": LayerConfig("v3_e16", T=512, d=7168, E=16, K=8, n_shared=1, I=2048,
                           n_groups=8, topk_groups=4, route_scale=2.5, bias_std=0.01),
+    # V3 token count and hidden size with 16 experts: the memory-bound calls see
+    # V3-sized activations (x_perm ~0.94 GB, larger than L2) with ~3.5 GB on the device
+    "v3_mem": LayerConfig("v3_mem", T=8192, d=7168, E=16, K=8, n_shared=1, I=2048,
+                          n_groups=8, topk_groups=4, route_scale=2.5, bias_std=0.01),
 }
 DECODE_T = (64, 256, 1024)
 
