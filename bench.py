@@ -54,6 +54,10 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--feedback-steps", type=int, default=None,
                     help="steps of the mid / drift feedback runs (default: the workload's)")
+    ap.add_argument("--shared-as-routed", action="store_true",
+                    help="serving layout: shared experts routed as experts E.. inside the grouped GEMM")
+    ap.add_argument("--redundant", type=int, default=0,
+                    help="serving layout: redundant expert copies, planned from warm-up loads")
     ap.add_argument("--shared-stream", action="store_true",
                     help="run the shared expert on a second stream")
     return ap.parse_args()
@@ -222,7 +226,8 @@ def run_ours(args):
         group = dist.group.WORLD
     cfg = load_config(args.config)
     p = synth.make_params(cfg, "cuda")            # identical replicas on every rank
-    layer = MoELayer(cfg, p, device=f"cuda:{local}", shared_stream=args.shared_stream)
+    layer = MoELayer(cfg, p, device=f"cuda:{local}", shared_stream=args.shared_stream,
+                     shared_as_routed=args.shared_as_routed, n_redundant=args.redundant)
     bias0 = layer.bias.clone()
     del p
     feedback = cfg.steps > 1                     # mid / drift: a bias-feedback run
@@ -245,9 +250,13 @@ def run_ours(args):
     torch.cuda.synchronize()
     if layer.device_status() != 0:
         raise RuntimeError(f"device status {layer.device_status()} during warm-up")
+    if args.redundant:
+        layer.plan_replicas(layer.load.cpu())    # copies placed from the warm-up loads
     layer.bias.copy_(bias0)                      # the timed trajectory starts from the initial bias
     stats_hist = torch.zeros(args.steps, 4, dtype=torch.float32, device="cuda")
-    names = ["route", "permute", "routed", "shared", "combine"]
+    names = ["route", "permute", "routed", "combine"]
+    if not args.shared_as_routed:
+        names.insert(3, "shared")
     marks = [{n: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
               for n in names} for _ in range(args.steps)]
     touched = int((layer.load > 0).sum().item())
@@ -313,6 +322,8 @@ def run_ours(args):
     pk = peaks()
     alg = algorithmic(cfg, touched)
     kernels = {}
+    if "shared" not in per:
+        per["shared"] = 0.0                       # inside the routed call in the serving layout
     for n in names:
         a = alg[n]
         k = {"ms": round(per[n], 4)}
@@ -349,7 +360,9 @@ def run_ours(args):
                    "tokens_per_rank": cfg.T, "parallelism": f"dp{world} (replicas, load all-reduce)",
                    "l2": "inputs larger than L2: 22.6 GB of expert weights streamed per step"
                    if cfg.d == 7168 else "two alternating token batches",
-                   "shared_stream": bool(args.shared_stream)},
+                   "shared_stream": bool(args.shared_stream),
+                   "shared_as_routed": bool(args.shared_as_routed),
+                   "redundant_experts": args.redundant},
         "roofline": roofline,
         "layer_tensor_frac": {"expert_tflops": round(layer_tf, 1),
                               "frac_of_sustained": round(layer_tf / pk["bf16_sust"], 4),
@@ -359,7 +372,8 @@ def run_ours(args):
         "hbm_kernels": {n: {"gbs": kernels[n]["gbs"],
                             "frac": round(kernels[n]["gbs"] / pk["hbm"], 4)}
                         for n in ("permute", "combine")},
-        "gpu_launches": KERNELS_PER_STEP * args.steps,
+        "gpu_launches": (KERNELS_PER_STEP - 2 * bool(args.shared_as_routed)
+                         + bool(args.redundant)) * args.steps,
         "device_status": status,
         "clocks": clk,
         "e2e": e2e,

@@ -36,11 +36,13 @@ SIGNATURES = {
     "moe_abi_version": (I, []),
     "moe_workspace_bytes": (Z, [I, I, I, I, I]),
     "moe_router_prepare": (I, [P, I, I, P, P]),
-    "moe_router_topk": (I, [P, P, P, P, P, I, I, I, I, I, I, F, P, P, P, P, P, P, Z, P]),
+    "moe_router_topk": (I, [P, P, P, P, P, I, I, I, I, I, I, F, I, P, P, P, P, P, P, Z, P]),
     "moe_permute": (I, [P, I, I, I, P, I, P, P, P, P, P, P, Z, P]),
     "moe_permute_static": (I, [P, I, I, I, P, I, P, P, P, P, P, P]),
     "moe_grouped_swiglu": (I, [P, P, I, I, I, I, P, P, P, P, P, P, P]),
     "moe_combine": (I, [P, P, P, P, I, I, I, P, P]),
+    "moe_replica_plan": (I, [P, I, I, P, P, P]),
+    "moe_replica_remap": (I, [P, I, I, I, I, P, P, P, P]),
     "moe_bias_update": (I, [P, P, I, I, I, F, P, P]),
 }
 
@@ -106,10 +108,11 @@ def moe_router_prepare(w_r, E, d, w_split, stream=None, check=True):
 
 def moe_router_topk(x, w_split, scores_in, logit_offset, bias, T, d, E, K, n_groups,
                     topk_groups, route_scale, topk_idx, topk_gate, expert_load,
-                    affinity_out, status_dev, ws, ws_bytes, stream=None, check=True):
+                    affinity_out, status_dev, ws, ws_bytes, stream=None, check=True,
+                    n_shared_routed=0):
     r = lib().moe_router_topk(_ptr(x), _ptr(w_split), _ptr(scores_in), _ptr(logit_offset),
                               _ptr(bias), T, d, E, K, n_groups, topk_groups,
-                              float(route_scale), _ptr(topk_idx), _ptr(topk_gate),
+                              float(route_scale), n_shared_routed, _ptr(topk_idx), _ptr(topk_gate),
                               _ptr(expert_load), _ptr(affinity_out), _ptr(status_dev),
                               _ptr(ws), ws_bytes, _stream(stream))
     return _check("moe_router_topk", r) if check else r
@@ -140,6 +143,28 @@ def moe_grouped_swiglu(a, group_offsets, n_groups, R, d, I, w1, w3, w2, h, y, st
                                  _ptr(w3), _ptr(w2), _ptr(h), _ptr(y), _ptr(status_dev),
                                  _stream(stream))
     return _check("moe_grouped_swiglu", r) if check else r
+
+
+def moe_replica_plan(load, E, n_redundant, check=True):
+    """Host call: returns (slot_start [E+1], slots [E+n], expert_of_slot [E+n])
+    as int32 CPU tensors for the given per-expert loads."""
+    load = torch.as_tensor(load, dtype=torch.int32).contiguous().cpu()
+    ss = torch.empty(E + 1, dtype=torch.int32)
+    sl = torch.empty(E + n_redundant, dtype=torch.int32)
+    eo = torch.empty(E + n_redundant, dtype=torch.int32)
+    r = lib().moe_replica_plan(load.data_ptr(), E, n_redundant, ss.data_ptr(), sl.data_ptr(),
+                               eo.data_ptr())
+    if check:
+        _check("moe_replica_plan", r)
+        return ss, sl, eo
+    return r
+
+
+def moe_replica_remap(topk_idx, T, K, E, n_redundant, slot_start, slots, phys_idx, stream=None,
+                      check=True):
+    r = lib().moe_replica_remap(_ptr(topk_idx), T, K, E, n_redundant, _ptr(slot_start),
+                                _ptr(slots), _ptr(phys_idx), _stream(stream))
+    return _check("moe_replica_remap", r) if check else r
 
 
 def moe_combine(y_perm, row_of, topk_gate, y_shared, T, K, d, out, stream=None, check=True):

@@ -15,8 +15,9 @@ struct TopkArgs {
   const float* bias;       // [E]
   int T, E, K, n_groups, topk_groups;
   float route_scale;
-  int32_t* idx;            // [T, K]
-  float* gate;             // [T, K]
+  int n_shared_routed;     // shared experts appended as ids E.. with gate 1 (0 = none)
+  int32_t* idx;            // [T, K + n_shared_routed]
+  float* gate;             // [T, K + n_shared_routed]
   int32_t* load;           // [E], zeroed before the launch
   int32_t* status;
 };
@@ -42,6 +43,13 @@ cudaError_t launch_combine(const uint16_t* y_perm, const int32_t* row_of, const 
                            cudaStream_t s);
 cudaError_t launch_bias_update(const int32_t* load, float* bias, int T, int K, int E, float gamma,
                                float* stats, cudaStream_t s);
+
+// ---- redundant expert copies (replicas.cu)
+bool replica_plan(const int32_t* load, int E, int n_redundant, int32_t* slot_start, int32_t* slots,
+                  int32_t* expert_of_slot);
+cudaError_t launch_replica_remap(const int32_t* idx, int T, int K, int E, int n_redundant,
+                                 const int32_t* slot_start, const int32_t* slots, int32_t* phys,
+                                 cudaStream_t s);
 
 // ---- tensor-core GEMMs (gemm_tc.cu)
 // Router logits + sigmoid: s[t, e] = sigmoid(sum_j x[t,j] w[e,j] + o[e]) with

@@ -80,12 +80,15 @@ moe_status moe_router_prepare(const float* w_r, int E, int d, void* w_split_bf16
 moe_status moe_router_topk(const void* x_bf16, const void* w_split_bf16, const float* scores_in,
                            const float* logit_offset, const float* bias, int T, int d, int E,
                            int K, int n_groups, int topk_groups, float route_scale,
-                           int32_t* topk_idx, float* topk_gate, int32_t* expert_load,
+                           int n_shared_routed, int32_t* topk_idx, float* topk_gate,
+                           int32_t* expert_load,
                            float* affinity_out, int32_t* status_dev, void* ws, size_t ws_bytes,
                            moe_stream_t stream) {
   if (!bias || !expert_load || T < 0) return MOE_ERR_INVALID_ARG;
   if (T > 0 && (!topk_idx || !topk_gate)) return MOE_ERR_INVALID_ARG;
   if (!routing_shape_ok(T, E, K, n_groups, topk_groups)) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (n_shared_routed < 0) return MOE_ERR_INVALID_ARG;
+  if (K + n_shared_routed > 32 || E + n_shared_routed > 512) return MOE_ERR_UNSUPPORTED_SHAPE;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const float* scores = scores_in;
   if (x_bf16 != nullptr) {
@@ -114,6 +117,7 @@ moe_status moe_router_topk(const void* x_bf16, const void* w_split_bf16, const f
   a.n_groups = n_groups;
   a.topk_groups = topk_groups;
   a.route_scale = route_scale;
+  a.n_shared_routed = n_shared_routed;
   a.idx = topk_idx;
   a.gate = topk_gate;
   a.load = expert_load;
@@ -187,6 +191,27 @@ moe_status moe_grouped_swiglu(const void* a_bf16, const int32_t* group_offsets, 
       static_cast<const uint16_t*>(w1_bf16), static_cast<const uint16_t*>(w3_bf16),
       static_cast<const uint16_t*>(w2_bf16), static_cast<uint16_t*>(h_bf16),
       static_cast<uint16_t*>(y_bf16), status_dev, static_cast<cudaStream_t>(stream)));
+}
+
+moe_status moe_replica_plan(const int32_t* load_host, int E, int n_redundant,
+                            int32_t* slot_start_host, int32_t* slots_host,
+                            int32_t* expert_of_slot_host) {
+  if (!load_host || !slot_start_host || !slots_host || !expert_of_slot_host || E < 1 ||
+      n_redundant < 0)
+    return MOE_ERR_INVALID_ARG;
+  if (E + n_redundant > 1024) return MOE_ERR_UNSUPPORTED_SHAPE;
+  return replica_plan(load_host, E, n_redundant, slot_start_host, slots_host, expert_of_slot_host)
+             ? MOE_OK
+             : MOE_ERR_INVALID_ARG;
+}
+
+moe_status moe_replica_remap(const int32_t* topk_idx, int T, int K, int E, int n_redundant,
+                             const int32_t* slot_start, const int32_t* slots, int32_t* phys_idx,
+                             moe_stream_t stream) {
+  if (T < 0 || K < 1 || E < 1 || n_redundant < 0) return MOE_ERR_INVALID_ARG;
+  if (T > 0 && (!topk_idx || !slot_start || !slots || !phys_idx)) return MOE_ERR_INVALID_ARG;
+  return cuda_status(launch_replica_remap(topk_idx, T, K, E, n_redundant, slot_start, slots,
+                                          phys_idx, static_cast<cudaStream_t>(stream)));
 }
 
 moe_status moe_combine(const void* y_perm_bf16, const int32_t* row_of, const float* topk_gate,

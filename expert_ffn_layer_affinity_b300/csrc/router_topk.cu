@@ -172,11 +172,17 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32) topk_kernel(TopkArgs a) {
       const float v = __shfl_sync(kFull, sk, r);
       denom = (r == 0) ? v : __fadd_rn(denom, v);
     }
+    const int ldk = K + a.n_shared_routed;
     if (lane < K) {
-      const size_t o = static_cast<size_t>(t) * K + lane;
+      const size_t o = static_cast<size_t>(t) * ldk + lane;
       a.idx[o] = my_idx;
       a.gate[o] = __fmul_rn(__fdiv_rn(sk, denom), scale);
       atomicAdd(&hist[my_idx], 1);
+    } else if (lane < ldk) {
+      // serving layout: shared expert j travels as routed expert E + j, gate 1
+      const size_t o = static_cast<size_t>(t) * ldk + lane;
+      a.idx[o] = E + (lane - K);
+      a.gate[o] = 1.0f;
     }
   }
   if (__any_sync(kFull, nonfinite) && lane == 0 && a.status)

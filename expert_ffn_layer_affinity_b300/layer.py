@@ -3,8 +3,17 @@ tensors, every step is one library call, nothing is computed in Python.
 
 Step order of one pass (the bias changes only between passes; qwbw.cn essay
 on the report, "训练的每一步结束之后统计整批样本各个专家的负载情况"):
-  moe_router_topk -> moe_permute -> moe_grouped_swiglu (routed)
-  -> moe_grouped_swiglu (shared) -> moe_combine ; then moe_bias_update.
+  moe_router_topk -> [moe_replica_remap] -> moe_permute -> moe_grouped_swiglu
+  (routed) -> moe_grouped_swiglu (shared) -> moe_combine ; then moe_bias_update.
+
+Serving layouts from the report's deployment (qwbw.cn essay, "9个专家",
+"32个冗余专家"):
+  shared_as_routed  the shared experts travel as routed experts E.. with gate 1,
+                    computed inside the routed grouped GEMM (no separate launch);
+  n_redundant       extra physical copies of the most loaded experts, planned by
+                    plan_replicas() from observed loads; tokens of a copied expert
+                    are spread over its copies.
+Physical expert weights are then laid out [E experts][copies][shared].
 """
 from __future__ import annotations
 
@@ -17,22 +26,49 @@ from .synth import LayerConfig
 class MoELayer:
     def __init__(self, cfg: LayerConfig, params: dict, max_T: int | None = None,
                  device: str = "cuda", keep_affinity: bool = False,
-                 shared_stream: bool = False):
+                 shared_stream: bool = False, shared_as_routed: bool = False,
+                 n_redundant: int = 0):
         self.cfg = cfg
         self.device = torch.device(device)
         dev = self.device
         p = params
+        E, d, I, ns = cfg.E, cfg.d, cfg.I, cfg.n_shared
         self.w_r = p["w_r"].to(dev).contiguous()
         self.bias = p["bias"].to(dev).clone().contiguous()
-        self.w1 = p["w1"].to(dev).contiguous()
-        self.w3 = p["w3"].to(dev).contiguous()
-        self.w2 = p["w2"].to(dev).contiguous()
         self.ws1 = p["ws1"].to(dev).contiguous()
         self.ws3 = p["ws3"].to(dev).contiguous()
         self.ws2 = p["ws2"].to(dev).contiguous()
         lo = p.get("logit_offset")
         self.logit_offset = lo.to(dev).contiguous() if lo is not None else None
-        E, d = cfg.E, cfg.d
+        self.shared_as_routed = shared_as_routed
+        self.n_redundant = n_redundant
+        self.ns_routed = ns if shared_as_routed else 0
+        self.E_phys = E + n_redundant + self.ns_routed
+        if self.E_phys == E:
+            self.w1 = p["w1"].to(dev).contiguous()
+            self.w3 = p["w3"].to(dev).contiguous()
+            self.w2 = p["w2"].to(dev).contiguous()
+        else:
+            bf = torch.bfloat16
+            self.w1 = torch.empty(self.E_phys, I, d, dtype=bf, device=dev)
+            self.w3 = torch.empty(self.E_phys, I, d, dtype=bf, device=dev)
+            self.w2 = torch.empty(self.E_phys, d, I, dtype=bf, device=dev)
+            self.w1[:E].copy_(p["w1"])
+            self.w3[:E].copy_(p["w3"])
+            self.w2[:E].copy_(p["w2"])
+            for r in range(n_redundant):           # until a plan exists: copies of expert 0
+                self.w1[E + r].copy_(self.w1[0])
+                self.w3[E + r].copy_(self.w3[0])
+                self.w2[E + r].copy_(self.w2[0])
+            for j in range(self.ns_routed):
+                sl = slice(j * I, (j + 1) * I)
+                self.w1[E + n_redundant + j].copy_(self.ws1[sl])
+                self.w3[E + n_redundant + j].copy_(self.ws3[sl])
+                self.w2[E + n_redundant + j].copy_(self.ws2[:, sl])
+        self.slot_start = self.slots = None
+        if n_redundant:                            # identity plan: no copy used yet
+            self.slot_start = torch.arange(E + 1, dtype=torch.int32, device=dev)
+            self.slots = torch.arange(E + n_redundant, dtype=torch.int32, device=dev)
         self.w_split = torch.empty(E, 3 * d, dtype=torch.bfloat16, device=dev)
         L.moe_router_prepare(self.w_r, E, d, self.w_split)
         self.keep_affinity = keep_affinity
@@ -43,26 +79,36 @@ class MoELayer:
         self._alloc(max_T or cfg.T)
 
     # ------------------------------------------------------------ buffers
+    @property
+    def K_slots(self) -> int:
+        """Entries per token after selection (K, plus shared experts in the
+        serving layout)."""
+        return self.cfg.K + self.ns_routed
+
     def _alloc(self, T: int):
         c, dev = self.cfg, self.device
-        K, E, d, I, ns = c.K, c.E, c.d, c.I, c.n_shared
+        K, E, d, I, ns = self.K_slots, c.E, c.d, c.I, c.n_shared
         R = T * K
         bf, i32 = torch.bfloat16, torch.int32
         self.idx = torch.empty(T, K, dtype=i32, device=dev)
+        self.phys_idx = torch.empty(T, K, dtype=i32, device=dev) if self.n_redundant else None
         self.gate = torch.empty(T, K, dtype=torch.float32, device=dev)
         self.load = torch.zeros(E, dtype=i32, device=dev)
-        self.offsets = torch.zeros(E + 1, dtype=i32, device=dev)
+        self.offsets = torch.zeros(self.E_phys + 1, dtype=i32, device=dev)
         self.row_of = torch.empty(T, K, dtype=i32, device=dev)
         self.tok_of = torch.empty(R, dtype=i32, device=dev)
         self.x_perm = torch.empty(R, d, dtype=bf, device=dev)
         self.h = torch.empty(R, I, dtype=bf, device=dev)
         self.y_perm = torch.empty(R, d, dtype=bf, device=dev)
-        self.h_sh = torch.empty(T, ns * I, dtype=bf, device=dev)
-        self.y_sh = torch.empty(T, d, dtype=bf, device=dev)
+        if not self.shared_as_routed:
+            self.h_sh = torch.empty(T, ns * I, dtype=bf, device=dev)
+            self.y_sh = torch.empty(T, d, dtype=bf, device=dev)
+        else:
+            self.h_sh = self.y_sh = None
         self.out = torch.empty(T, d, dtype=bf, device=dev)
         self.affinity = (torch.empty(T, E, dtype=torch.float32, device=dev)
                          if self.keep_affinity else None)
-        self.ws_bytes = L.moe_workspace_bytes(T, d, E, K, I)
+        self.ws_bytes = L.moe_workspace_bytes(T, d, self.E_phys, K, I)
         self.ws = torch.empty(max(self.ws_bytes, 256), dtype=torch.uint8, device=dev)
         self.shared_offsets = torch.tensor([0, T], dtype=i32, device=dev)
         self.T_cap = T
@@ -75,6 +121,22 @@ class MoELayer:
             self.shared_offsets.copy_(torch.tensor([0, T], dtype=torch.int32))
             self._shared_T = T
 
+    # ------------------------------------------------------------ replicas
+    def plan_replicas(self, load) -> torch.Tensor:
+        """Re-place the redundant copies from observed per-expert loads (a host
+        plan, then a copy of each planned expert's weights into its slot).
+        Returns the logical expert of every slot."""
+        E = self.cfg.E
+        ss, sl, eo = L.moe_replica_plan(load, E, self.n_redundant)
+        for r in range(self.n_redundant):
+            e = int(eo[E + r])
+            self.w1[E + r].copy_(self.w1[e])
+            self.w3[E + r].copy_(self.w3[e])
+            self.w2[E + r].copy_(self.w2[e])
+        self.slot_start = ss.to(self.device)
+        self.slots = sl.to(self.device)
+        return eo
+
     # ------------------------------------------------------------- steps
     def route(self, x: torch.Tensor, stream=None):
         c = self.cfg
@@ -82,8 +144,9 @@ class MoELayer:
         self._ensure(T)
         aff = self.affinity[:T] if self.affinity is not None else None
         L.moe_router_topk(x, self.w_split, None, self.logit_offset, self.bias, T, c.d, c.E,
-                          c.K, c.n_groups, c.topk_groups, c.route_scale, self.idx, self.gate,
-                          self.load, aff, self.status, self.ws, self.ws_bytes, stream)
+                          c.K, c.n_groups, c.topk_groups, c.route_scale, self.idx,
+                          self.gate, self.load, aff, self.status, self.ws, self.ws_bytes,
+                          stream, n_shared_routed=self.ns_routed)
 
     def forward(self, x: torch.Tensor, stream=None, marks: dict | None = None) -> torch.Tensor:
         """One layer pass over x bf16 [T, d]; returns the bf16 [T, d] output
@@ -94,7 +157,8 @@ class MoELayer:
         call on the stream it runs on."""
         c = self.cfg
         T = x.shape[0]
-        R = T * c.K
+        K = self.K_slots
+        R = T * K
         main = torch.cuda.current_stream() if stream is None else stream
 
         def mark(name, i, s=main):
@@ -103,12 +167,18 @@ class MoELayer:
 
         mark("route", 0)
         self.route(x, stream)
+        idx = self.idx
+        if self.n_redundant:
+            L.moe_replica_remap(self.idx, T, K, c.E, self.n_redundant, self.slot_start,
+                                self.slots, self.phys_idx, stream)
+            idx = self.phys_idx
         mark("route", 1)
         mark("permute", 0)
-        L.moe_permute(self.idx, T, c.K, c.E, x, c.d, self.offsets, self.row_of, self.tok_of,
+        L.moe_permute(idx, T, K, self.E_phys, x, c.d, self.offsets, self.row_of, self.tok_of,
                       self.x_perm, self.status, self.ws, self.ws_bytes, stream)
         mark("permute", 1)
-        if self.side is not None:
+        separate_shared = not self.shared_as_routed
+        if self.side is not None and separate_shared:
             self.side.wait_stream(main)
             mark("shared", 0, self.side)
             L.moe_grouped_swiglu(x, self.shared_offsets, 1, T, c.d, c.n_shared * c.I, self.ws1,
@@ -116,18 +186,18 @@ class MoELayer:
                                  self.side)
             mark("shared", 1, self.side)
         mark("routed", 0)
-        L.moe_grouped_swiglu(self.x_perm, self.offsets, c.E, R, c.d, c.I, self.w1, self.w3,
-                             self.w2, self.h, self.y_perm, self.status, stream)
+        L.moe_grouped_swiglu(self.x_perm, self.offsets, self.E_phys, R, c.d, c.I, self.w1,
+                             self.w3, self.w2, self.h, self.y_perm, self.status, stream)
         mark("routed", 1)
-        if self.side is not None:
+        if self.side is not None and separate_shared:
             main.wait_stream(self.side)
-        else:
+        elif separate_shared:
             mark("shared", 0)
             L.moe_grouped_swiglu(x, self.shared_offsets, 1, T, c.d, c.n_shared * c.I, self.ws1,
                                  self.ws3, self.ws2, self.h_sh, self.y_sh, self.status, stream)
             mark("shared", 1)
         mark("combine", 0)
-        L.moe_combine(self.y_perm, self.row_of, self.gate, self.y_sh, T, c.K, c.d,
+        L.moe_combine(self.y_perm, self.row_of, self.gate, self.y_sh, T, K, c.d,
                       self.out[:T], stream)
         mark("combine", 1)
         return self.out[:T]

@@ -87,9 +87,17 @@ moe_status moe_router_prepare(const float* w_r, int E, int d, void* w_split_bf16
  *  n_groups, topk_groups  G and M of the group limit (1, 1 = no limit).  A
  *                group's score is the sum of its ceil(K/M) largest z.
  *  route_scale   multiplies the normalised gates.
- * Outputs: topk_idx [T, K] int32 in rank order (z descending, lower expert
+ *  n_shared_routed  serving layout of the report's decode deployment, where
+ *                the shared expert travels as one more routed expert ("每个
+ *                token ... 9个专家", qwbw.cn essay on the report): 0 = off;
+ *                n > 0 appends ids E .. E+n-1 with gate 1.0 after the K routed
+ *                ones, so rows of topk_idx / topk_gate have K+n entries and
+ *                the shared experts run inside the routed grouped GEMM (their
+ *                weights stored as groups E .. E+n-1).  Loads count the K
+ *                routed experts only.  K + n <= 32.
+ * Outputs: topk_idx [T, K(+n)] int32 in rank order (z descending, lower expert
  *  index first on equal z, -0 == +0, NaN below every number); topk_gate
- *  [T, K] fp32; expert_load [E] int32 (overwritten: zeroed then counted);
+ *  [T, K(+n)] fp32; expert_load [E] int32 (overwritten: zeroed then counted);
  *  affinity_out [T, E] fp32 or NULL (the s used, when x is given).
  * Fp32 rule (bit-exact against a reference fed the same s): z = s + b; group
  *  score = top1 + top2 (+ ...); denom = s_1 + s_2 + ... in rank order;
@@ -99,7 +107,8 @@ moe_status moe_router_topk(const void* x_bf16, const void* w_split_bf16,
                            const float* scores_in, const float* logit_offset,
                            const float* bias, int T, int d, int E, int K,
                            int n_groups, int topk_groups, float route_scale,
-                           int32_t* topk_idx, float* topk_gate, int32_t* expert_load,
+                           int n_shared_routed, int32_t* topk_idx, float* topk_gate,
+                           int32_t* expert_load,
                            float* affinity_out, int32_t* status_dev, void* ws,
                            size_t ws_bytes, moe_stream_t stream);
 
@@ -164,6 +173,30 @@ moe_status moe_grouped_swiglu(const void* a_bf16, const int32_t* group_offsets, 
 moe_status moe_combine(const void* y_perm_bf16, const int32_t* row_of, const float* topk_gate,
                        const void* y_shared_bf16, int T, int K, int d, void* out_bf16,
                        moe_stream_t stream);
+
+/* Serving-side redundant experts (host call, no device work).  The report's
+ * prefill deployment keeps 32 redundant experts, re-placed from observed
+ * load ("32个冗余专家", qwbw.cn essay on the report).  Plans n_redundant extra
+ * copies from per-expert loads: slot e is expert e; slots E..E+n_redundant-1
+ * are copies, each given in turn to the expert with the largest load per copy
+ * (lower index on ties; this minimises the largest load per copy).
+ *  load_host [E] int32 (host): observed loads.
+ *  slot_start_host [E+1], slots_host [E+n_redundant] (host, out): CSR list of
+ *    each expert's slots (its own slot first).
+ *  expert_of_slot_host [E+n_redundant] (host, out): logical expert of each
+ *    slot (copy weights accordingly). */
+moe_status moe_replica_plan(const int32_t* load_host, int E, int n_redundant,
+                            int32_t* slot_start_host, int32_t* slots_host,
+                            int32_t* expert_of_slot_host);
+
+/* Device remap to physical slots: entry (t, k) of logical expert e in [0, E)
+ * becomes slots[slot_start[e] + t mod c_e] (c_e = copies of e); ids >= E
+ * (shared experts in the serving layout) become id + n_redundant, so the
+ * physical layout is [E experts][n_redundant copies][shared].  slot_start
+ * and slots are DEVICE copies of the plan.  phys_idx [T, K] int32. */
+moe_status moe_replica_remap(const int32_t* topk_idx, int T, int K, int E, int n_redundant,
+                             const int32_t* slot_start, const int32_t* slots, int32_t* phys_idx,
+                             moe_stream_t stream);
 
 /* Step 5, bias feedback after the step:
  *   bias[e] = bias[e] - gamma  if E*load[e] > T*K   (overloaded)

@@ -49,7 +49,7 @@ def check_pass(cfg, p, x, layer, out, sample=None, bias=None):
     idx64, gate64 = ref.select_experts(s64, b.astype(np.float64), cfg.K, cfg.n_groups,
                                        cfg.topk_groups, cfg.route_scale, precision="fp64")
     kth, grp = ref.near_tie_tokens(s64, b, cfg.K, cfg.n_groups, cfg.topk_groups)
-    gidx = layer.idx[:T].cpu().numpy()
+    gidx = layer.idx[:T, :cfg.K].cpu().numpy()
     mism = np.any(np.sort(gidx, 1) != np.sort(idx64, 1), axis=1)
     assert not np.any(mism & ~(kth | grp)), np.nonzero(mism & ~(kth | grp))[0][:10]
     tokens = np.arange(T) if sample is None else sample
