@@ -34,7 +34,7 @@ CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.a
 # from ncu dram__bytes on the 16-expert profiling case (profiles/gemm_pair_v3e16.md),
 # scaled by the experts a launch processes.  Must be re-measured when those
 # kernels change.
-GEMM_TRAFFIC_PER_EXPERT = (0.998950912e9 + 17.472512e6 + 486.599168e6 + 48.930048e6) / 16
+GEMM_TRAFFIC_PER_EXPERT = (1.042742e9 + 16.753152e6 + 0.497552e9 + 48.797696e6) / 16
 KERNELS_PER_STEP = 12  # router GEMM, selection, 4 permute, 2+2 grouped GEMM, combine, bias update
 
 

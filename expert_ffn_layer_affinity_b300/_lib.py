@@ -44,6 +44,7 @@ SIGNATURES = {
     "moe_replica_plan": (I, [P, I, I, P, P, P]),
     "moe_replica_remap": (I, [P, I, I, I, I, P, P, P, P]),
     "moe_bias_update": (I, [P, P, I, I, I, F, P, P]),
+    "moe_seq_balance_loss": (I, [P, P, I, P, I, I, I, F, P, P]),
 }
 
 _lib = None
@@ -171,6 +172,13 @@ def moe_combine(y_perm, row_of, topk_gate, y_shared, T, K, d, out, stream=None, 
     r = lib().moe_combine(_ptr(y_perm), _ptr(row_of), _ptr(topk_gate), _ptr(y_shared), T, K, d,
                           _ptr(out), _stream(stream))
     return _check("moe_combine", r) if check else r
+
+
+def moe_seq_balance_loss(scores, topk_idx, ldk, seq_offsets, S, E, K, alpha, loss_out,
+                         stream=None, check=True):
+    r = lib().moe_seq_balance_loss(_ptr(scores), _ptr(topk_idx), ldk, _ptr(seq_offsets), S, E, K,
+                                   float(alpha), _ptr(loss_out), _stream(stream))
+    return _check("moe_seq_balance_loss", r) if check else r
 
 
 def moe_bias_update(expert_load, bias, T, K, E, gamma, stats_out, stream=None, check=True):

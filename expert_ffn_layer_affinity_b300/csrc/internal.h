@@ -51,6 +51,11 @@ cudaError_t launch_replica_remap(const int32_t* idx, int T, int K, int E, int n_
                                  const int32_t* slot_start, const int32_t* slots, int32_t* phys,
                                  cudaStream_t s);
 
+// ---- sequence-wise balance loss (balance_loss.cu)
+cudaError_t launch_seq_balance(const float* scores, const int32_t* idx, int ldk,
+                               const int32_t* seq_offsets, int S, int E, int K, float alpha,
+                               float* loss, cudaStream_t s);
+
 // ---- tensor-core GEMMs (gemm_tc.cu)
 // Router logits + sigmoid: s[t, e] = sigmoid(sum_j x[t,j] w[e,j] + o[e]) with
 // w given as the exact bf16 split [E, 3d].

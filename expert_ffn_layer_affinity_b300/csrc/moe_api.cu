@@ -229,6 +229,16 @@ moe_status moe_combine(const void* y_perm_bf16, const int32_t* row_of, const flo
                                     static_cast<cudaStream_t>(stream)));
 }
 
+moe_status moe_seq_balance_loss(const float* scores, const int32_t* topk_idx, int ldk,
+                                const int32_t* seq_offsets, int S, int E, int K, float alpha,
+                                float* loss_out, moe_stream_t stream) {
+  if (S < 0 || E < 1 || K < 1 || ldk < K) return MOE_ERR_INVALID_ARG;
+  if (S > 0 && (!scores || !topk_idx || !seq_offsets || !loss_out)) return MOE_ERR_INVALID_ARG;
+  if (E > 512 || K > 32) return MOE_ERR_UNSUPPORTED_SHAPE;
+  return cuda_status(launch_seq_balance(scores, topk_idx, ldk, seq_offsets, S, E, K, alpha,
+                                        loss_out, static_cast<cudaStream_t>(stream)));
+}
+
 moe_status moe_bias_update(const int32_t* expert_load, float* bias, int T, int K, int E,
                            float gamma, float* stats_out, moe_stream_t stream) {
   if (!expert_load || !bias || T < 0 || K < 1 || E < 1) return MOE_ERR_INVALID_ARG;

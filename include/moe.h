@@ -198,6 +198,21 @@ moe_status moe_replica_remap(const int32_t* topk_idx, int T, int K, int E, int n
                              const int32_t* slot_start, const int32_t* slots, int32_t* phys_idx,
                              moe_stream_t stream);
 
+/* Forward value of the small sequence-wise balance loss kept next to the bias
+ * feedback ("同时保留一个极小的序列级平衡损失", chenshi221 DeepSeek-V3 notes,
+ * "Auxiliary-loss-free 负载均衡"; weigao.cc §3).  The pages print no formula;
+ * the reading taken, per sequence of T_s tokens:
+ *   f_i = E / (K T_s) * #{(t, k < K): topk_idx[t, k] = i}
+ *   P_i = (1 / T_s) * sum_t scores[t, i] / sum_j scores[t, j]
+ *   loss = alpha * sum_i f_i P_i
+ *  scores [T, E] fp32 affinities (e.g. affinity_out of moe_router_topk);
+ *  topk_idx [T, ldk] int32, first K columns used (ldk = K, or K + shared
+ *  experts in the serving layout); seq_offsets [S+1] DEVICE int32 token
+ *  ranges of the S sequences; loss_out [S] fp32.  Sums in a fixed order. */
+moe_status moe_seq_balance_loss(const float* scores, const int32_t* topk_idx, int ldk,
+                                const int32_t* seq_offsets, int S, int E, int K, float alpha,
+                                float* loss_out, moe_stream_t stream);
+
 /* Step 5, bias feedback after the step:
  *   bias[e] = bias[e] - gamma  if E*load[e] > T*K   (overloaded)
  *   bias[e] = bias[e] + gamma  if E*load[e] < T*K   (underloaded)

@@ -52,9 +52,20 @@ R6  Layer output y(t) = sum over shared experts FFN_j(x_t)
 R7  Dispatch order: the rows sent to expert e are the (token, slot) pairs with
     idx == e in ascending (token, slot) order; experts are laid out in
     ascending expert order.
+R8  Sequence-wise balance loss (the pages keep "a tiny-weight sequence-wise
+    balance loss" next to the bias feedback -- chenshi221 notes, same section;
+    weigao.cc §3 row "A small sequence-wise auxiliary loss is still used" --
+    but print no formula).  Reading: for a sequence of T_s tokens,
+      f_i = E / (K T_s) * #{(t, k): idx[t, k] = i},
+      P_i = (1 / T_s) * sum_t s[t, i] / sum_j s[t, j],
+      L   = alpha * sum_i f_i P_i.
+    Its formula is therefore not fixed by the pages (parity unpinned against
+    them); the pins fix the function against this reading.
 
 Function-level parity status: every function below is pinned by the CPU test
-suite (brute force, closed forms, invariants); none is "parity unpinned".
+suite (brute force, closed forms, invariants).  seq_balance_loss follows a
+reading (R8) whose formula the pages do not print: parity unpinned against
+the pages, pinned against the reading.
 """
 from __future__ import annotations
 
@@ -213,6 +224,27 @@ def bias_update(load, bias, T, K, E, gamma):
     out[over] = (b[over] - g).astype(F32)
     out[under] = (b[under] + g).astype(F32)
     return out
+
+
+def seq_balance_loss(s, idx, seq_offsets, K, alpha):
+    """Reading R8, one value per sequence (float64)."""
+    s = np.asarray(s, dtype=F64)
+    idx = np.asarray(idx)
+    T, E = s.shape
+    out = []
+    for a, b in zip(seq_offsets[:-1], seq_offsets[1:]):
+        Ts = b - a
+        if Ts == 0:
+            out.append(0.0)
+            continue
+        count = np.zeros(E)
+        for t in range(a, b):
+            for k in range(K):
+                count[idx[t, k]] += 1
+        f = E / (K * Ts) * count
+        P = (s[a:b] / s[a:b].sum(axis=1, keepdims=True)).sum(axis=0) / Ts
+        out.append(alpha * float((f * P).sum()))
+    return np.array(out, dtype=F64)
 
 
 def load_stats(load):

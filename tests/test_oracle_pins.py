@@ -312,3 +312,33 @@ def test_near_tie_detection():
     assert kth[0]          # 2nd vs 3rd: 0.5+1e-6 vs 0.5
     kth, _ = ref.near_tie_tokens(s, np.zeros(4), 1)
     assert not kth[0]
+
+
+def test_seq_balance_loss_closed_forms():
+    rng = np.random.default_rng(13)
+    E, K, alpha = 8, 2, 1e-4
+    # perfectly even routing: f_i = 1 for every expert, so L = alpha * sum_i P_i = alpha
+    T = 16
+    idx = np.array([[(2 * t) % E, (2 * t + 1) % E] for t in range(T)])
+    s = rng.random((T, E))
+    assert abs(ref.seq_balance_loss(s, idx, [0, T], K, alpha)[0] - alpha) < 1e-18
+    # everything on expert 0 with all affinity there: f_0 = E, P_0 = 1 -> L = alpha * E
+    idx1 = np.zeros((4, 1), dtype=int)
+    s1 = np.zeros((4, E))
+    s1[:, 0] = 1.0
+    assert abs(ref.seq_balance_loss(s1, idx1, [0, 4], 1, alpha)[0] - alpha * E) < 1e-18
+
+
+def test_seq_balance_loss_handworked_and_per_sequence():
+    # E=4, K=1, one sequence of 2 tokens: token 0 picks expert 0, token 1 picks 2.
+    # s rows (sums): [1,1,1,1] (4) and [2,0,1,1] (4)
+    # f = 4/(1*2) * [1,0,1,0] = [2,0,2,0];  P = ([.25,.25,.25,.25] + [.5,0,.25,.25]) / 2
+    #   = [.375, .125, .25, .25];  L = a * (2*.375 + 2*.25) = 1.25 a
+    s = np.array([[1.0, 1, 1, 1], [2, 0, 1, 1]])
+    idx = np.array([[0], [2]])
+    assert abs(ref.seq_balance_loss(s, idx, [0, 2], 1, 1.0)[0] - 1.25) < 1e-15
+    # two sequences are independent; an empty sequence gives 0
+    s2 = np.vstack([s, s])
+    idx2 = np.vstack([idx, idx])
+    got = ref.seq_balance_loss(s2, idx2, [0, 2, 2, 4], 1, 1.0)
+    assert np.allclose(got, [1.25, 0.0, 1.25], atol=1e-15)
