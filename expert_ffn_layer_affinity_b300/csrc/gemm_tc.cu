@@ -119,6 +119,7 @@ struct GemmParams {
   void* out;
   int ldo;               // output row stride in elements
   const float* col_offset;  // router: per-expert logit offset or nullptr
+  int w13_3d;               // SwiGLU: tmA is a 3-D map fetching w1 and w3 rows in one box
   int32_t* status;
 };
 
@@ -240,7 +241,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mt_prefix[G] = carry;
       row_start[G] = group_offset(p, G);
       tma_prefetch_desc(&tmA);
-      if (MODE == MODE_SWIGLU) tma_prefetch_desc(&tmA2);
+      if (MODE == MODE_SWIGLU && !p.w13_3d) tma_prefetch_desc(&tmA2);
       tma_prefetch_desc(&tmB);
     }
   } else if (warp == 1) {
@@ -320,7 +321,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int j = 0; j < nbox; ++j) {
               const uint32_t aj = sa + static_cast<uint32_t>(j * C::kA);
               const int kx = (kb0 + j) * BK;
-              if (MODE == MODE_SWIGLU) {
+              if (MODE == MODE_SWIGLU && p.w13_3d) {
+                tma_load_3d_pair(aj, &tmA, fb, kx, w_row, 0, pol_w);  // w1 rows, then w3 rows
+              } else if (MODE == MODE_SWIGLU) {
                 tma_load_2d_pair(aj, &tmA, fb, kx, w_row, pol_w);
                 tma_load_2d_pair(aj + 64 * 128, &tmA2, fb, kx, w_row, pol_w);
               } else {
@@ -553,6 +556,27 @@ bool make_map(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer, u
   return r == CUDA_SUCCESS;
 }
 
+// w1 and w3 of one allocation, w3 a fixed positive byte distance after w1:
+// a 3-D map [2][rows][inner] whose box {64, 64, 2} brings 64 rows of w1 and
+// the same 64 rows of w3 in one copy.
+bool make_map_w13(CUtensorMap* m, const void* w1, const void* w3, uint64_t inner, uint64_t rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  const uintptr_t a = reinterpret_cast<uintptr_t>(w1), b = reinterpret_cast<uintptr_t>(w3);
+  if (b <= a) return false;
+  const uint64_t dist = b - a;
+  if (dist % 16 || dist >= (1ull << 40) || dist < rows * inner * 2) return false;
+  cuuint64_t dims[3] = {inner, rows, 2};
+  cuuint64_t strides[2] = {inner * 2, dist};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(BK), 64, 2};
+  cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(w1), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 template <int MODE>
 cudaError_t launch_gemm(const CUtensorMap& a, const CUtensorMap& a2, const CUtensorMap& b,
                         const GemmParams& p, int max_units, cudaStream_t s) {
@@ -602,7 +626,10 @@ cudaError_t launch_grouped_swiglu(const uint16_t* a, const int32_t* offsets, int
       !make_map(&tw2, w2, I, static_cast<uint64_t>(G) * d, 128) ||
       !make_map(&th, h, I, R, 128))
     return cudaErrorInvalidValue;
+  CUtensorMap tw13;
+  const bool w13 = make_map_w13(&tw13, w1, w3, d, static_cast<uint64_t>(G) * I);
   GemmParams p1{};
+  p1.w13_3d = w13 ? 1 : 0;
   p1.group_offsets = offsets;
   p1.G = G;
   p1.N = I;
@@ -614,9 +641,10 @@ cudaError_t launch_grouped_swiglu(const uint16_t* a, const int32_t* offsets, int
   p1.ldo = I;
   p1.status = status;
   const int mt1 = (R + C1::kTokTile - 1) / C1::kTokTile + G;
-  cudaError_t e = launch_gemm<MODE_SWIGLU>(tw1, tw3, tx, p1, mt1 * ((I + 127) / 128), s);
+  cudaError_t e = launch_gemm<MODE_SWIGLU>(w13 ? tw13 : tw1, tw3, tx, p1, mt1 * ((I + 127) / 128), s);
   if (e != cudaSuccess) return e;
   GemmParams p2 = p1;
+  p2.w13_3d = 0;
   p2.N = d;
   p2.num_kb = I / BK;
   p2.a_k_wrap_kb = I / BK;

@@ -44,14 +44,24 @@ class MoELayer:
         self.n_redundant = n_redundant
         self.ns_routed = ns if shared_as_routed else 0
         self.E_phys = E + n_redundant + self.ns_routed
-        if self.E_phys == E:
-            self.w1 = p["w1"].to(dev).contiguous()
-            self.w3 = p["w3"].to(dev).contiguous()
+        # w1 and w3 live in one allocation [2, E, I, d] so the grouped GEMM
+        # fetches matching rows of both with a single copy
+        w13 = p.get("w13")
+        if (self.E_phys == E and w13 is not None and w13.device == dev
+                and w13.is_contiguous()):
+            self.w13 = w13
+            self.w1, self.w3 = w13[0], w13[1]
+            self.w2 = p["w2"].to(dev).contiguous()
+        elif self.E_phys == E:
+            self.w13 = torch.empty(2, E, I, d, dtype=torch.bfloat16, device=dev)
+            self.w1, self.w3 = self.w13[0], self.w13[1]
+            self.w1.copy_(p["w1"])
+            self.w3.copy_(p["w3"])
             self.w2 = p["w2"].to(dev).contiguous()
         else:
             bf = torch.bfloat16
-            self.w1 = torch.empty(self.E_phys, I, d, dtype=bf, device=dev)
-            self.w3 = torch.empty(self.E_phys, I, d, dtype=bf, device=dev)
+            self.w13 = torch.empty(2, self.E_phys, I, d, dtype=bf, device=dev)
+            self.w1, self.w3 = self.w13[0], self.w13[1]
             self.w2 = torch.empty(self.E_phys, d, I, dtype=bf, device=dev)
             self.w1[:E].copy_(p["w1"])
             self.w3[:E].copy_(p["w3"])

@@ -17,7 +17,7 @@ v3_drift   the v3 layer, 100 steps of T=16384 tokens from 4 Gaussian
 
 Layouts (all row-major, the reduction dimension contiguous):
   x      bf16 [T, d]          w_r   fp32 [E, d]       bias fp32 [E]
-  w1,w3  bf16 [E, I, d]       w2    bf16 [E, d, I]
+  w1,w3  bf16 [E, I, d]       w2    bf16 [E, d, I]   (w1, w3 = views of w13 [2, E, I, d])
   ws1,ws3 bf16 [n_s*I, d]     ws2   bf16 [d, n_s*I]   (shared experts side by side)
 """
 from __future__ import annotations
@@ -159,12 +159,14 @@ def make_params(cfg: LayerConfig, device="cpu", seed: int | None = None) -> dict
     p["w_r"], p["bias"], p["logit_offset"] = make_router(cfg, device, seed)
     bf = torch.bfloat16
     E, d, I = cfg.E, cfg.d, cfg.I
-    w1 = torch.empty(E, I, d, dtype=bf, device=device)
-    w3 = torch.empty(E, I, d, dtype=bf, device=device)
+    # w1 and w3 side by side in one allocation (the grouped GEMM then fetches
+    # matching rows of both with one copy); p["w13"] is that allocation
+    w13 = torch.empty(2, E, I, d, dtype=bf, device=device)
+    w1, w3 = w13[0], w13[1]
     w2 = torch.empty(E, d, I, dtype=bf, device=device)
     for e in range(E):
         w1[e], w3[e], w2[e] = make_expert(cfg, e, device, seed)
-    p["w1"], p["w3"], p["w2"] = w1, w3, w2
+    p["w1"], p["w3"], p["w2"], p["w13"] = w1, w3, w2, w13
     p["ws1"], p["ws3"], p["ws2"] = make_shared(cfg, device, seed)
     return p
 

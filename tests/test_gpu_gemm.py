@@ -120,3 +120,29 @@ def test_v3_expert_shape_sampled():
     H, Y = reference(a, offsets, w1, w3, w2)
     assert ref.rel_l2(bf16_to_np64(h), H) < 4e-3
     assert ref.rel_l2(bf16_to_np64(y), Y) < 1e-2
+
+
+@pytest.mark.parametrize("sizes,d,I", [
+    ([0, 129, 0, 127, 1, 256, 300], 256, 128),
+    ([200, 57, 0, 513], 512, 192),
+])
+def test_grouped_swiglu_w1_w3_in_one_allocation(sizes, d, I):
+    """w1 and w3 as the two halves of one [2, G, I, d] buffer (the layout the
+    layer uses): same result as separate tensors, bit for bit."""
+    G = len(sizes)
+    offsets = torch.tensor([0] + list(np.cumsum(sizes)), dtype=torch.int32)
+    R = int(offsets[-1])
+    a = synth.make_ffn_rows(R, d, seed=R + d)
+    w1, w3, w2 = weights(G, I, d, seed=G + I)
+    w13 = torch.stack([w1, w3]).contiguous()
+    h_sep, y_sep, st1 = run_grouped(a, offsets, w1, w3, w2)
+    dev = "cuda"
+    w13d = w13.to(dev)
+    h = torch.zeros(R, I, dtype=torch.bfloat16, device=dev)
+    y = torch.zeros(R, d, dtype=torch.bfloat16, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    moe.moe_grouped_swiglu(a.to(dev), offsets.to(dev), G, R, d, I, w13d[0], w13d[1], w2.to(dev),
+                           h, y, status)
+    assert sync_status(status) == 0 and st1 == 0
+    assert torch.equal(h.cpu().view(torch.int16), h_sep.view(torch.int16))
+    assert torch.equal(y.cpu().view(torch.int16), y_sep.view(torch.int16))
