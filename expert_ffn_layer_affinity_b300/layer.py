@@ -158,9 +158,11 @@ class MoELayer:
                           self.gate, self.load, aff, self.status, self.ws, self.ws_bytes,
                           stream, n_shared_routed=self.ns_routed)
 
-    def forward(self, x: torch.Tensor, stream=None, marks: dict | None = None) -> torch.Tensor:
-        """One layer pass over x bf16 [T, d]; returns the bf16 [T, d] output
-        (a view of an internal buffer, valid until the next call).
+    def forward(self, x: torch.Tensor, stream=None, marks: dict | None = None,
+                out: torch.Tensor | None = None) -> torch.Tensor:
+        """One layer pass over x bf16 [T, d]; returns the bf16 [T, d] output:
+        `out` when given, else a view of an internal buffer valid until the
+        next call.
 
         `marks`, if given, maps call names ("route", "permute", "routed",
         "shared", "combine") to a pair of CUDA events recorded around that
@@ -206,11 +208,11 @@ class MoELayer:
             L.moe_grouped_swiglu(x, self.shared_offsets, 1, T, c.d, c.n_shared * c.I, self.ws1,
                                  self.ws3, self.ws2, self.h_sh, self.y_sh, self.status, stream)
             mark("shared", 1)
+        dst = self.out[:T] if out is None else out
         mark("combine", 0)
-        L.moe_combine(self.y_perm, self.row_of, self.gate, self.y_sh, T, K, c.d,
-                      self.out[:T], stream)
+        L.moe_combine(self.y_perm, self.row_of, self.gate, self.y_sh, T, K, c.d, dst, stream)
         mark("combine", 1)
-        return self.out[:T]
+        return dst
 
     def bias_update(self, T: int, stream=None, group=None, stats_out=None):
         """Sign-rule bias update from this pass's loads.  With a process
@@ -227,10 +229,52 @@ class MoELayer:
         L.moe_bias_update(self.load, self.bias, T_total, c.K, c.E, c.gamma, stats, stream)
 
     def step(self, x: torch.Tensor, stream=None, group=None, marks=None,
-             stats_out=None) -> torch.Tensor:
-        out = self.forward(x, stream, marks)
+             stats_out=None, out: torch.Tensor | None = None) -> torch.Tensor:
+        y = self.forward(x, stream, marks, out)
         self.bias_update(x.shape[0], stream, group, stats_out)
-        return out
+        return y
 
     def device_status(self) -> int:
         return int(self.status.item())
+
+
+class HostPipeline:
+    """Layer steps on activations that live in (pinned) host memory, with the
+    copies overlapped: while step i computes, step i+1's input is copied in
+    on one stream and step i-1's output is copied out on another (PCIe runs
+    both directions at once).  Every step still moves its whole input to the
+    device and its whole output back; device buffers are double-buffered and
+    ordered with events.  Usage: pipe.step(i, x_host, out_host) for i = 0, 1,
+    ...; pipe.finish() orders the caller's stream after the last copy out."""
+
+    def __init__(self, layer: MoELayer, T: int):
+        self.layer = layer
+        dev = layer.device
+        d = layer.cfg.d
+        self.h2d = torch.cuda.Stream(device=dev)
+        self.d2h = torch.cuda.Stream(device=dev)
+        self.x_dev = [torch.empty(T, d, dtype=torch.bfloat16, device=dev) for _ in range(2)]
+        self.out_dev = [torch.empty(T, d, dtype=torch.bfloat16, device=dev) for _ in range(2)]
+        self.ev_in = [torch.cuda.Event() for _ in range(2)]
+        self.ev_done = [torch.cuda.Event() for _ in range(2)]
+        self.ev_out = [torch.cuda.Event() for _ in range(2)]
+
+    def step(self, i: int, x_host: torch.Tensor, out_host: torch.Tensor, group=None,
+             stats_out=None) -> None:
+        b = i % 2
+        comp = torch.cuda.current_stream()
+        self.h2d.wait_event(self.ev_done[b])         # step i-2 no longer reads x_dev[b]
+        with torch.cuda.stream(self.h2d):
+            self.x_dev[b].copy_(x_host, non_blocking=True)
+        self.ev_in[b].record(self.h2d)
+        comp.wait_event(self.ev_in[b])
+        comp.wait_event(self.ev_out[b])              # step i-2's output has left out_dev[b]
+        self.layer.step(self.x_dev[b], group=group, stats_out=stats_out, out=self.out_dev[b])
+        self.ev_done[b].record(comp)
+        self.d2h.wait_event(self.ev_done[b])
+        with torch.cuda.stream(self.d2h):
+            out_host.copy_(self.out_dev[b], non_blocking=True)
+        self.ev_out[b].record(self.d2h)
+
+    def finish(self) -> None:
+        torch.cuda.current_stream().wait_stream(self.d2h)
