@@ -45,6 +45,10 @@ SIGNATURES = {
     "moe_replica_remap": (I, [P, I, I, I, I, P, P, P, P]),
     "moe_bias_update": (I, [P, P, I, I, I, F, P, P]),
     "moe_seq_balance_loss": (I, [P, P, I, P, I, I, I, F, P, P]),
+    "moe_quantize_fp8": (I, [P, I, I, P, P, I, P]),
+    "moe_quantize_weights_fp8": (I, [P, P, I, I, I, P, P, P]),
+    "moe_permute_fp8": (I, [P, P, I, I, I, I, P, P, P, I, P]),
+    "moe_grouped_swiglu_fp8": (I, [P, P, I, P, I, I, I, I, P, P, P, P, P, P, P, P, P, P]),
 }
 
 _lib = None
@@ -185,3 +189,33 @@ def moe_bias_update(expert_load, bias, T, K, E, gamma, stats_out, stream=None, c
     r = lib().moe_bias_update(_ptr(expert_load), _ptr(bias), T, K, E, float(gamma),
                               _ptr(stats_out), _stream(stream))
     return _check("moe_bias_update", r) if check else r
+
+
+# ------------------------------------------------------------------ FP8 path
+def moe_quantize_fp8(x, rows, cols, q_out, s_out, ld_s, stream=None, check=True):
+    r = lib().moe_quantize_fp8(_ptr(x), rows, cols, _ptr(q_out), _ptr(s_out), ld_s,
+                               _stream(stream))
+    return _check("moe_quantize_fp8", r) if check else r
+
+
+def moe_quantize_weights_fp8(w, w_pair, groups, rows, cols, q_out, s_out, stream=None,
+                             check=True):
+    r = lib().moe_quantize_weights_fp8(_ptr(w), _ptr(w_pair), groups, rows, cols, _ptr(q_out),
+                                       _ptr(s_out), _stream(stream))
+    return _check("moe_quantize_weights_fp8", r) if check else r
+
+
+def moe_permute_fp8(q_in, s_in, ld_in, T, K, d, row_of, q_perm, s_perm, ld_out, stream=None,
+                    check=True):
+    r = lib().moe_permute_fp8(_ptr(q_in), _ptr(s_in), ld_in, T, K, d, _ptr(row_of), _ptr(q_perm),
+                              _ptr(s_perm), ld_out, _stream(stream))
+    return _check("moe_permute_fp8", r) if check else r
+
+
+def moe_grouped_swiglu_fp8(a_q, a_s, ld_as, group_offsets, n_groups, R, d, I, w13_q, w13_s,
+                           w2_q, w2_s, h, h_q, h_s, y, status_dev, stream=None, check=True):
+    r = lib().moe_grouped_swiglu_fp8(_ptr(a_q), _ptr(a_s), ld_as, _ptr(group_offsets), n_groups,
+                                     R, d, I, _ptr(w13_q), _ptr(w13_s), _ptr(w2_q), _ptr(w2_s),
+                                     _ptr(h), _ptr(h_q), _ptr(h_s), _ptr(y), _ptr(status_dev),
+                                     _stream(stream))
+    return _check("moe_grouped_swiglu_fp8", r) if check else r

@@ -43,6 +43,7 @@
 #include <cstdint>
 
 #include "internal.h"
+#include "gemm_common.cuh"
 #include "ptx.cuh"
 
 namespace moe {
@@ -51,7 +52,11 @@ namespace {
 constexpr int BK = 64;
 constexpr int UMMA_K = 16;
 constexpr int kThreads = 192;
-constexpr int kMaxGroups = 512;
+using gemm::kMaxGroups;
+using gemm::decode_work;
+using gemm::wait_plain;
+using gemm::tile_n;
+using gemm::store_block_transposed;
 constexpr int kRouterChunkKb = 4;
 
 enum Mode : int { MODE_SWIGLU = 0, MODE_DOWN = 1, MODE_ROUTER = 2 };
@@ -127,62 +132,6 @@ __device__ __forceinline__ int group_offset(const GemmParams& p, int g) {
   return p.group_offsets ? p.group_offsets[g] : (g == 0 ? 0 : p.dense_rows);
 }
 
-__device__ __forceinline__ void decode_work(int w, int NT, const int* mt_prefix, int G, int& g,
-                                            int& n, int& m) {
-  int lo = 0, hi = G - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (mt_prefix[mid] * NT <= w) lo = mid;
-    else hi = mid - 1;
-  }
-  g = lo;
-  // token tile major, weight tile fastest: the pairs that run side by side
-  // cover every weight tile of a token tile, and the other token tiles of the
-  // same group follow NT positions later (still running, sharing weights
-  // through L2).  Full and ragged token tiles thus spread over all pairs
-  // instead of repeating on the same ones (with 74 pairs and token-tile-
-  // fastest order, some pairs drew only full tiles and others only ragged
-  // ones: 3.53 -> 3.42 ms for GEMM1 at the V3 shape).  Claiming items from an
-  // atomic counter instead of this fixed stride measured no better.
-  const int local = w - mt_prefix[g] * NT;
-  m = local / NT;
-  n = local - m * NT;
-}
-
-__device__ __forceinline__ bool wait_plain(uint32_t bar, uint32_t parity, unsigned long long ns) {
-  const unsigned long long t0 = globaltimer_ns();
-  while (!mbar_try_wait(bar, parity))
-    if (globaltimer_ns() - t0 > ns) return false;
-  return true;
-}
-
-// Tokens of this tile the MMA must cover, rounded up to 32 (16 rows staged
-// in each CTA of the pair).
-__device__ __forceinline__ int tile_n(int rows_left, int tok_tile) {
-  const int n = rows_left < tok_tile ? rows_left : tok_tile;
-  return (n + 31) & ~31;
-}
-
-// Writes a 32 (weight row = output column) x 32 (token) block, held one
-// output column per lane as 16 packed bf16 pairs along tokens, as 32 token
-// rows of 64 bytes.  `xp` is this warp's 32 x 80-byte staging area.
-__device__ __forceinline__ void store_block_transposed(const uint32_t (&v)[32], uint8_t* xp,
-                                                       int lane, __nv_bfloat16* out, long long row0,
-                                                       int rows_valid, int ldo, int col) {
-  // v[j] holds the value for token j of column `lane`, as fp32 bits
-  __nv_bfloat16* x = reinterpret_cast<__nv_bfloat16*>(xp);
-#pragma unroll
-  for (int j = 0; j < 32; ++j) x[j * 40 + lane] = __float2bfloat16_rn(__uint_as_float(v[j]));
-  __syncwarp();
-  if (lane < rows_valid) {
-    const uint4* src = reinterpret_cast<const uint4*>(xp + lane * 80);
-    uint4* dst = reinterpret_cast<uint4*>(out + (row0 + lane) * ldo + col);
-#pragma unroll
-    for (int k = 0; k < 4; ++k) dst[k] = src[k];
-  }
-  __syncwarp();
-}
-
 template <int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA2,
@@ -218,28 +167,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int n_units = PAIR ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
 
   if (warp == 0) {
-    int carry = 0;
-    for (int g0 = 0; g0 < G; g0 += 32) {
-      const int g = g0 + lane;
-      int mt = 0;
-      if (g < G) {
-        const int a = group_offset(p, g), b = group_offset(p, g + 1);
-        const int rows = b > a ? b - a : 0;
-        mt = (rows + C::kTokTile - 1) / C::kTokTile;
-        row_start[g] = a;
-      }
-      int incl = mt;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-        if (lane >= o) incl += y;
-      }
-      if (g < G) mt_prefix[g] = carry + incl - mt;
-      carry += __shfl_sync(0xFFFFFFFFu, incl, 31);
-    }
+    gemm::build_tile_prefix(G, C::kTokTile, lane, [&](int g) { return group_offset(p, g); },
+                            mt_prefix, row_start);
     if (lane == 0) {
-      mt_prefix[G] = carry;
-      row_start[G] = group_offset(p, G);
       tma_prefetch_desc(&tmA);
       if (MODE == MODE_SWIGLU && !p.w13_3d) tma_prefetch_desc(&tmA2);
       tma_prefetch_desc(&tmB);
@@ -527,33 +457,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ------------------------------------------------------------------ host side
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  if (!fn) {
-    void* ptr = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
-  }
-  return fn;
-}
+using gemm::encode_fn;
 
 // 2-D bf16 tensor [outer, inner] (inner contiguous), box = 64 x box_rows,
 // 128-byte swizzle, zero fill outside the tensor.
 bool make_map(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer, uint32_t box_rows) {
-  auto fn = encode_fn();
-  if (!fn) return false;
-  cuuint64_t dims[2] = {inner, outer};
-  cuuint64_t strides[1] = {inner * 2};
-  cuuint32_t box[2] = {static_cast<cuuint32_t>(BK), box_rows};
-  cuuint32_t estr[2] = {1, 1};
-  const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims,
-                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
+  return gemm::make_map_sw128(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, ptr, inner, outer, box_rows);
 }
 
 // w1 and w3 of one allocation, w3 a fixed positive byte distance after w1:

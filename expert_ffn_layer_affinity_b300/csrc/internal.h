@@ -68,4 +68,19 @@ cudaError_t launch_grouped_swiglu(const uint16_t* a, const int32_t* offsets, int
                                   const uint16_t* w2, uint16_t* h, uint16_t* y, int32_t* status,
                                   cudaStream_t s);
 
+// ---- FP8 path (quant_fp8.cu, gemm_fp8.cu)
+cudaError_t launch_quantize_rows(const uint16_t* in, int rows, int cols, uint8_t* q, float* s,
+                                 int ld_s, cudaStream_t st);
+cudaError_t launch_quantize_blocks(const uint16_t* w, const uint16_t* w_pair, int groups, int rows,
+                                   int cols, uint8_t* q, float* s, cudaStream_t st);
+cudaError_t launch_permute_fp8(const uint8_t* q, const float* s, int ld_in, int T, int K, int d,
+                               const int32_t* row_of, uint8_t* q_perm, float* s_perm, int ld_out,
+                               cudaStream_t st);
+cudaError_t launch_grouped_swiglu_fp8(const uint8_t* a_q, const float* a_s, int ld_as,
+                                      const int32_t* offsets, int G, int R, int d, int I,
+                                      const uint8_t* w13_q, const float* w13_s,
+                                      const uint8_t* w2_q, const float* w2_s, uint16_t* h,
+                                      uint8_t* h_q, float* h_s, uint16_t* y, int32_t* status,
+                                      cudaStream_t s);
+
 }  // namespace moe

@@ -193,6 +193,69 @@ moe_status moe_grouped_swiglu(const void* a_bf16, const int32_t* group_offsets, 
       static_cast<uint16_t*>(y_bf16), status_dev, static_cast<cudaStream_t>(stream)));
 }
 
+// ------------------------------------------------------------------ FP8 path
+moe_status moe_quantize_fp8(const void* x_bf16, int rows, int cols, void* q_out, float* s_out,
+                            int ld_s, moe_stream_t stream) {
+  if (rows < 0 || cols < 1 || ld_s < rows) return MOE_ERR_INVALID_ARG;
+  if (rows > 0 && (!x_bf16 || !q_out || !s_out)) return MOE_ERR_INVALID_ARG;
+  if (cols % 128) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (rows > 0 && (!aligned16(x_bf16) || !aligned16(q_out) ||
+                   (reinterpret_cast<uintptr_t>(s_out) & 3u)))
+    return MOE_ERR_UNSUPPORTED_SHAPE;
+  return cuda_status(launch_quantize_rows(static_cast<const uint16_t*>(x_bf16), rows, cols,
+                                          static_cast<uint8_t*>(q_out), s_out, ld_s,
+                                          static_cast<cudaStream_t>(stream)));
+}
+
+moe_status moe_quantize_weights_fp8(const void* w_bf16, const void* w_pair_bf16, int groups,
+                                    int rows, int cols, void* q_out, float* s_out,
+                                    moe_stream_t stream) {
+  if (groups < 0 || rows < 1 || cols < 1) return MOE_ERR_INVALID_ARG;
+  if (groups > 0 && (!w_bf16 || !q_out || !s_out)) return MOE_ERR_INVALID_ARG;
+  if (rows % 128 || cols % 128) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (groups > 0 && (!aligned16(w_bf16) || !aligned16(q_out) ||
+                     (w_pair_bf16 && !aligned16(w_pair_bf16)) ||
+                     (reinterpret_cast<uintptr_t>(s_out) & 3u)))
+    return MOE_ERR_UNSUPPORTED_SHAPE;
+  return cuda_status(launch_quantize_blocks(
+      static_cast<const uint16_t*>(w_bf16), static_cast<const uint16_t*>(w_pair_bf16), groups,
+      rows, cols, static_cast<uint8_t*>(q_out), s_out, static_cast<cudaStream_t>(stream)));
+}
+
+moe_status moe_permute_fp8(const void* q_in, const float* s_in, int ld_in, int T, int K, int d,
+                           const int32_t* row_of, void* q_perm, float* s_perm, int ld_out,
+                           moe_stream_t stream) {
+  if (T < 0 || K < 1 || d < 1 || ld_in < T) return MOE_ERR_INVALID_ARG;
+  if (static_cast<long long>(T) * K >= (1ll << 31) || static_cast<long long>(ld_out) < 1ll * T * K)
+    return MOE_ERR_INVALID_ARG;
+  if (T > 0 && (!q_in || !s_in || !row_of || !q_perm || !s_perm)) return MOE_ERR_INVALID_ARG;
+  if (d % 128) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (T > 0 && (!aligned16(q_in) || !aligned16(q_perm))) return MOE_ERR_UNSUPPORTED_SHAPE;
+  return cuda_status(launch_permute_fp8(static_cast<const uint8_t*>(q_in), s_in, ld_in, T, K, d,
+                                        row_of, static_cast<uint8_t*>(q_perm), s_perm, ld_out,
+                                        static_cast<cudaStream_t>(stream)));
+}
+
+moe_status moe_grouped_swiglu_fp8(const void* a_q, const float* a_s, int ld_as,
+                                  const int32_t* group_offsets, int n_groups, int R, int d, int I,
+                                  const void* w13_q, const float* w13_s, const void* w2_q,
+                                  const float* w2_s, void* h_bf16, void* h_q, float* h_s,
+                                  void* y_bf16, int32_t* status_dev, moe_stream_t stream) {
+  if (R < 0 || n_groups < 1 || d < 1 || I < 1 || ld_as < R) return MOE_ERR_INVALID_ARG;
+  if (R > 0 && (!a_q || !a_s || !group_offsets || !w13_q || !w13_s || !w2_q || !w2_s ||
+                !h_bf16 || !h_q || !h_s || !y_bf16))
+    return MOE_ERR_INVALID_ARG;
+  if (d % 128 || I % 128 || n_groups > 512) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (R > 0 && (!aligned16(a_q) || !aligned16(w13_q) || !aligned16(w2_q) || !aligned16(h_bf16) ||
+                !aligned16(h_q) || !aligned16(y_bf16) || !aligned16(w13_s)))
+    return MOE_ERR_UNSUPPORTED_SHAPE;
+  return cuda_status(launch_grouped_swiglu_fp8(
+      static_cast<const uint8_t*>(a_q), a_s, ld_as, group_offsets, n_groups, R, d, I,
+      static_cast<const uint8_t*>(w13_q), w13_s, static_cast<const uint8_t*>(w2_q), w2_s,
+      static_cast<uint16_t*>(h_bf16), static_cast<uint8_t*>(h_q), h_s,
+      static_cast<uint16_t*>(y_bf16), status_dev, static_cast<cudaStream_t>(stream)));
+}
+
 moe_status moe_replica_plan(const int32_t* load_host, int E, int n_redundant,
                             int32_t* slot_start_host, int32_t* slots_host,
                             int32_t* expert_of_slot_host) {

@@ -149,7 +149,9 @@ __global__ void __launch_bounds__(256) gather_kernel(const uint4* __restrict__ x
     const int32_t* rows = row_of + t * K;
     for (int k = 0; k < K; ++k) {
       const int32_t r = __ldg(rows + k);
-      __stcs(x_perm + static_cast<size_t>(r) * chunks + c, v);
+      // entries with an out-of-range expert id (MOE_DEV_BAD_INDEX) have no row
+      if (r >= 0 && static_cast<size_t>(r) < static_cast<size_t>(T) * K)
+        __stcs(x_perm + static_cast<size_t>(r) * chunks + c, v);
     }
   }
 }

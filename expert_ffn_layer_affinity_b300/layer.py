@@ -14,6 +14,15 @@ Serving layouts from the report's deployment (qwbw.cn essay, "9个专家",
                     plan_replicas() from observed loads; tokens of a copied expert
                     are spread over its copies.
 Physical expert weights are then laid out [E experts][copies][shared].
+
+precision="fp8" runs the expert GEMMs in E4M3 with fine-grained scaling
+(qwbw.cn essay on the report, the FP8 training passage; weigao.cc section
+"6. FP8 Training"): weights are quantized once per 128 x 128 block when the
+layer is built (and again when replicas are re-placed), activations per
+1 x 128 tile inside every pass:
+  moe_router_topk -> moe_permute (maps only) -> moe_quantize_fp8 (x) ->
+  moe_permute_fp8 -> moe_grouped_swiglu_fp8 (routed, shared) -> moe_combine.
+Routing, gates and the combine are those of the bf16 path.
 """
 from __future__ import annotations
 
@@ -27,8 +36,11 @@ class MoELayer:
     def __init__(self, cfg: LayerConfig, params: dict, max_T: int | None = None,
                  device: str = "cuda", keep_affinity: bool = False,
                  shared_stream: bool = False, shared_as_routed: bool = False,
-                 n_redundant: int = 0):
+                 n_redundant: int = 0, precision: str = "bf16"):
+        if precision not in ("bf16", "fp8"):
+            raise ValueError(f"precision must be 'bf16' or 'fp8', not {precision!r}")
         self.cfg = cfg
+        self.fp8 = precision == "fp8"
         self.device = torch.device(device)
         dev = self.device
         p = params
@@ -81,12 +93,34 @@ class MoELayer:
             self.slots = torch.arange(E + n_redundant, dtype=torch.int32, device=dev)
         self.w_split = torch.empty(E, 3 * d, dtype=torch.bfloat16, device=dev)
         L.moe_router_prepare(self.w_r, E, d, self.w_split)
+        if self.fp8:
+            self._quantize_weights()
         self.keep_affinity = keep_affinity
         self.side = torch.cuda.Stream(device=dev) if shared_stream else None
         self.status = torch.zeros(1, dtype=torch.int32, device=dev)
         self.stats = torch.zeros(4, dtype=torch.float32, device=dev)
         self.T_cap = 0
         self._alloc(max_T or cfg.T)
+
+    def _quantize_weights(self):
+        """E4M3 copies of the expert weights: w1/w3 row-interleaved per
+        expert with 128 x 128 block scales, w2 likewise; the shared block as
+        one group."""
+        c, dev = self.cfg, self.device
+        E, d, I, nI = self.E_phys, c.d, c.I, c.n_shared * c.I
+        u8, f32 = torch.uint8, torch.float32
+        self.w13_q = torch.empty(E, 2 * I, d, dtype=u8, device=dev)
+        self.w13_s = torch.empty(E, I // 128, d // 128, 2, dtype=f32, device=dev)
+        self.w2_q = torch.empty(E, d, I, dtype=u8, device=dev)
+        self.w2_s = torch.empty(E, d // 128, I // 128, dtype=f32, device=dev)
+        L.moe_quantize_weights_fp8(self.w1, self.w3, E, I, d, self.w13_q, self.w13_s)
+        L.moe_quantize_weights_fp8(self.w2, None, E, d, I, self.w2_q, self.w2_s)
+        self.ws13_q = torch.empty(1, 2 * nI, d, dtype=u8, device=dev)
+        self.ws13_s = torch.empty(1, nI // 128, d // 128, 2, dtype=f32, device=dev)
+        self.ws2_q = torch.empty(1, d, nI, dtype=u8, device=dev)
+        self.ws2_s = torch.empty(1, d // 128, nI // 128, dtype=f32, device=dev)
+        L.moe_quantize_weights_fp8(self.ws1, self.ws3, 1, nI, d, self.ws13_q, self.ws13_s)
+        L.moe_quantize_weights_fp8(self.ws2, None, 1, d, nI, self.ws2_q, self.ws2_s)
 
     # ------------------------------------------------------------ buffers
     @property
@@ -121,6 +155,18 @@ class MoELayer:
         self.ws_bytes = L.moe_workspace_bytes(T, d, self.E_phys, K, I)
         self.ws = torch.empty(max(self.ws_bytes, 256), dtype=torch.uint8, device=dev)
         self.shared_offsets = torch.tensor([0, T], dtype=i32, device=dev)
+        if self.fp8:
+            u8, f32 = torch.uint8, torch.float32
+            self.x_perm = None
+            self.xq = torch.empty(T, d, dtype=u8, device=dev)
+            self.xs = torch.empty(d // 128, T, dtype=f32, device=dev)
+            self.xq_perm = torch.empty(R, d, dtype=u8, device=dev)
+            self.xs_perm = torch.empty(d // 128, R, dtype=f32, device=dev)
+            self.hq = torch.empty(R, I, dtype=u8, device=dev)
+            self.hs = torch.empty(I // 128, R, dtype=f32, device=dev)
+            if not self.shared_as_routed:
+                self.hq_sh = torch.empty(T, ns * I, dtype=u8, device=dev)
+                self.hs_sh = torch.empty(ns * I // 128, T, dtype=f32, device=dev)
         self.T_cap = T
         self._shared_T = T
 
@@ -143,6 +189,9 @@ class MoELayer:
             self.w1[E + r].copy_(self.w1[e])
             self.w3[E + r].copy_(self.w3[e])
             self.w2[E + r].copy_(self.w2[e])
+            if self.fp8:
+                for t in (self.w13_q, self.w13_s, self.w2_q, self.w2_s):
+                    t[E + r].copy_(t[e])
         self.slot_start = ss.to(self.device)
         self.slots = sl.to(self.device)
         return eo
@@ -185,6 +234,8 @@ class MoELayer:
                                 self.slots, self.phys_idx, stream)
             idx = self.phys_idx
         mark("route", 1)
+        if self.fp8:
+            return self._forward_fp8(x, idx, stream, mark, out)
         mark("permute", 0)
         L.moe_permute(idx, T, K, self.E_phys, x, c.d, self.offsets, self.row_of, self.tok_of,
                       self.x_perm, self.status, self.ws, self.ws_bytes, stream)
@@ -207,6 +258,50 @@ class MoELayer:
             mark("shared", 0)
             L.moe_grouped_swiglu(x, self.shared_offsets, 1, T, c.d, c.n_shared * c.I, self.ws1,
                                  self.ws3, self.ws2, self.h_sh, self.y_sh, self.status, stream)
+            mark("shared", 1)
+        dst = self.out[:T] if out is None else out
+        mark("combine", 0)
+        L.moe_combine(self.y_perm, self.row_of, self.gate, self.y_sh, T, K, c.d, dst, stream)
+        mark("combine", 1)
+        return dst
+
+    def _forward_fp8(self, x, idx, stream, mark, out):
+        c = self.cfg
+        T = x.shape[0]
+        K = self.K_slots
+        R = T * K
+        Tc, Rc = self.T_cap, self.T_cap * K
+        main = torch.cuda.current_stream() if stream is None else stream
+        mark("permute", 0)
+        L.moe_permute(idx, T, K, self.E_phys, None, c.d, self.offsets, self.row_of, self.tok_of,
+                      None, self.status, self.ws, self.ws_bytes, stream)
+        L.moe_quantize_fp8(x, T, c.d, self.xq, self.xs, Tc, stream)
+        L.moe_permute_fp8(self.xq, self.xs, Tc, T, K, c.d, self.row_of, self.xq_perm,
+                          self.xs_perm, Rc, stream)
+        mark("permute", 1)
+        separate_shared = not self.shared_as_routed
+        nI = c.n_shared * c.I
+
+        def shared(s):
+            L.moe_grouped_swiglu_fp8(self.xq, self.xs, Tc, self.shared_offsets, 1, T, c.d, nI,
+                                     self.ws13_q, self.ws13_s, self.ws2_q, self.ws2_s,
+                                     self.h_sh, self.hq_sh, self.hs_sh, self.y_sh, self.status, s)
+
+        if self.side is not None and separate_shared:
+            self.side.wait_stream(main)
+            mark("shared", 0, self.side)
+            shared(self.side)
+            mark("shared", 1, self.side)
+        mark("routed", 0)
+        L.moe_grouped_swiglu_fp8(self.xq_perm, self.xs_perm, Rc, self.offsets, self.E_phys, R,
+                                 c.d, c.I, self.w13_q, self.w13_s, self.w2_q, self.w2_s, self.h,
+                                 self.hq, self.hs, self.y_perm, self.status, stream)
+        mark("routed", 1)
+        if self.side is not None and separate_shared:
+            main.wait_stream(self.side)
+        elif separate_shared:
+            mark("shared", 0)
+            shared(stream)
             mark("shared", 1)
         dst = self.out[:T] if out is None else out
         mark("combine", 0)

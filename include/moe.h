@@ -213,6 +213,68 @@ moe_status moe_seq_balance_loss(const float* scores, const int32_t* topk_idx, in
                                 const int32_t* seq_offsets, int S, int E, int K, float alpha,
                                 float* loss_out, moe_stream_t stream);
 
+/* ---------------------------------------------------------------- FP8 path
+ * E4M3 expert GEMMs with fine-grained scaling: activations scaled per 1 x 128
+ * tile, weights per 128 x 128 block, tensor-core partial sums promoted to
+ * fp32 every 128 reduction elements (qwbw.cn essay on the report, the FP8
+ * training passage; "DeepSeek-V3 Technical Report：中英对照解读", weigao.cc,
+ * section "6. FP8 Training").  Gating, dispatch maps and the combine stay
+ * those of the bf16 calls above.
+ *
+ * Quantization rule of every block: scale = fp32(amax / 448) with amax the
+ * largest |value| of the block (NaN ignored), scale = 1 for an all-zero
+ * block; code = E4M3 rounding (nearest, ties to even, saturating at +-448)
+ * of fp32(value / scale).  Codes are E4M3 bytes (uint8).
+ *
+ * Activation scales are stored BLOCK-MAJOR: s[j * ld_s + row] is the scale
+ * of columns j*128 .. j*128+127 of `row` (ld_s >= rows).
+ * Shape limits: cols, d and I multiples of 128. */
+
+/* Quantize bf16 rows [rows, cols] per 1 x 128 tile: q_out uint8 [rows, cols],
+ * s_out fp32 [cols/128][ld_s]. */
+moe_status moe_quantize_fp8(const void* x_bf16, int rows, int cols, void* q_out, float* s_out,
+                            int ld_s, moe_stream_t stream);
+
+/* Quantize weights bf16 [groups, rows, cols] per 128 x 128 block (rows and
+ * cols multiples of 128).
+ *  w_pair_bf16 == NULL: q_out uint8 [groups, rows, cols], s_out fp32
+ *    [groups, rows/128, cols/128] (the down projection w2, rows = d).
+ *  w_pair_bf16 != NULL (a second matrix of the same shape): the two are
+ *    written ROW-INTERLEAVED for the SwiGLU GEMM, q_out uint8
+ *    [groups, 2*rows, cols] with row 2i = w_bf16 row i and row 2i+1 =
+ *    w_pair_bf16 row i, s_out fp32 [groups, rows/128, cols/128, 2] (the two
+ *    matrices' block scales side by side).  Pass w1 and w3.
+ * The quantized layout is what moe_grouped_swiglu_fp8 reads. */
+moe_status moe_quantize_weights_fp8(const void* w_bf16, const void* w_pair_bf16, int groups,
+                                    int rows, int cols, void* q_out, float* s_out,
+                                    moe_stream_t stream);
+
+/* Dispatch of quantized activations: q_perm[row_of[t,k]] = q_in[t] (d bytes
+ * per row) and s_perm[j * ld_out + row_of[t,k]] = s_in[j * ld_in + t] for
+ * every block j.  row_of [T, K] from moe_permute (x may be NULL there).
+ * ld_in >= T, ld_out >= T*K. */
+moe_status moe_permute_fp8(const void* q_in, const float* s_in, int ld_in, int T, int K, int d,
+                           const int32_t* row_of, void* q_perm, float* s_perm, int ld_out,
+                           moe_stream_t stream);
+
+/* FP8 grouped SwiGLU experts: for group g (rows group_offsets[g] ..
+ * group_offsets[g+1] of a):
+ *   h = bf16(silu(a . w1[g]^T) * (a . w3[g]^T)),  h quantized per 1 x 128,
+ *   y = bf16(h . w2[g]^T)
+ * with every product an E4M3 GEMM promoted to fp32 per 128-deep block.
+ *  a_q uint8 [R, d], a_s fp32 [d/128][ld_as] (ld_as >= R);
+ *  group_offsets [n_groups+1] DEVICE int32, 1 <= n_groups <= 512;
+ *  w13_q / w13_s and w2_q / w2_s as written by moe_quantize_weights_fp8
+ *  (w1 paired with w3; w2 alone, rows = d);
+ *  h_bf16 [R, I] and h_q uint8 [R, I], h_s fp32 [I/128][R]: scratch that
+ *  holds h (bf16 and quantized) on return; y_bf16 [R, d].
+ * Shared experts: n_groups = 1, offsets {0, T}, I = n_shared * expert width. */
+moe_status moe_grouped_swiglu_fp8(const void* a_q, const float* a_s, int ld_as,
+                                  const int32_t* group_offsets, int n_groups, int R, int d, int I,
+                                  const void* w13_q, const float* w13_s, const void* w2_q,
+                                  const float* w2_s, void* h_bf16, void* h_q, float* h_s,
+                                  void* y_bf16, int32_t* status_dev, moe_stream_t stream);
+
 /* Step 5, bias feedback after the step:
  *   bias[e] = bias[e] - gamma  if E*load[e] > T*K   (overloaded)
  *   bias[e] = bias[e] + gamma  if E*load[e] < T*K   (underloaded)

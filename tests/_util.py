@@ -3,6 +3,7 @@ arithmetic comes from the oracle only)."""
 import numpy as np
 import torch
 
+from oracle import fp8_ref as f8ref
 from oracle import moe_ref as ref
 
 
@@ -38,9 +39,17 @@ class HostExperts:
         return (bf16_to_np64(self.p["ws1"]), bf16_to_np64(self.p["ws3"]),
                 bf16_to_np64(self.p["ws2"]))
 
+    def quantized(self, e):
+        """The oracle's own E4M3 quantization of routed expert e."""
+        return f8ref.quantize_expert(*self(e))
 
-def check_pass(cfg, p, x, layer, out, sample=None, bias=None):
-    """Compare one pass: routing on every token, output on `sample` tokens."""
+    def shared_quantized(self):
+        return f8ref.quantize_expert(*self.shared())
+
+
+def check_pass(cfg, p, x, layer, out, sample=None, bias=None, fp8=False):
+    """Compare one pass: routing on every token, output on `sample` tokens
+    (against the FP8 reading of the experts when fp8=True)."""
     T = x.shape[0]
     x64 = bf16_to_np64(x)
     off = p["logit_offset"].cpu().numpy() if p["logit_offset"] is not None else None
@@ -55,7 +64,11 @@ def check_pass(cfg, p, x, layer, out, sample=None, bias=None):
     tokens = np.arange(T) if sample is None else sample
     tokens = tokens[~mism[tokens]]
     host = HostExperts(p)
-    want = ref.moe_output64(x64, idx64, gate64, host, host.shared(), cfg.n_shared, tokens)
+    if fp8:
+        want = f8ref.moe_output64_fp8(x64, idx64, gate64, host.quantized,
+                                      host.shared_quantized(), cfg.n_shared, tokens)
+    else:
+        want = ref.moe_output64(x64, idx64, gate64, host, host.shared(), cfg.n_shared, tokens)
     got = bf16_to_np64(out[torch.from_numpy(tokens).to(out.device)])
     err = ref.rel_l2(got, want)
     assert err < 1e-2, err

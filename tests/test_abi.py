@@ -87,3 +87,34 @@ def test_other_calls_reject_bad_arguments():
 def test_binding_raises_on_error():
     with pytest.raises(moe.MoEError):
         moe.moe_combine(None, FAKE, FAKE, None, 4, 2, 16, FAKE, stream=0)
+
+
+def test_fp8_calls_reject_bad_arguments():
+    E_SHAPE, E_ARG = moe.MOE_ERR_UNSUPPORTED_SHAPE, moe.MOE_ERR_INVALID_ARG
+    # quantize: cols not a multiple of 128, ld_s < rows, null input
+    assert moe.moe_quantize_fp8(FAKE, 4, 192, FAKE, FAKE, 4, stream=0, check=False) == E_SHAPE
+    assert moe.moe_quantize_fp8(FAKE, 4, 256, FAKE, FAKE, 3, stream=0, check=False) == E_ARG
+    assert moe.moe_quantize_fp8(None, 4, 256, FAKE, FAKE, 4, stream=0, check=False) == E_ARG
+    assert moe.moe_quantize_fp8(FAKE + 8, 4, 256, FAKE, FAKE, 4, stream=0, check=False) == E_SHAPE
+    # weights: rows / cols multiples of 128
+    assert moe.moe_quantize_weights_fp8(FAKE, None, 2, 192, 256, FAKE, FAKE, stream=0,
+                                        check=False) == E_SHAPE
+    assert moe.moe_quantize_weights_fp8(FAKE, FAKE + 8, 2, 128, 256, FAKE, FAKE, stream=0,
+                                        check=False) == E_SHAPE
+    # permute: d multiple of 128, ld_out >= T*K
+    assert moe.moe_permute_fp8(FAKE, FAKE, 4, 4, 2, 192, FAKE, FAKE, FAKE, 8, stream=0,
+                               check=False) == E_SHAPE
+    assert moe.moe_permute_fp8(FAKE, FAKE, 4, 4, 2, 256, FAKE, FAKE, FAKE, 7, stream=0,
+                               check=False) == E_ARG
+    # grouped experts: d, I multiples of 128; ld_as >= R; groups <= 512
+    args = dict(stream=0, check=False)
+    assert moe.moe_grouped_swiglu_fp8(FAKE, FAKE, 64, FAKE, 4, 64, 192, 128, FAKE, FAKE, FAKE,
+                                      FAKE, FAKE, FAKE, FAKE, FAKE, None, **args) == E_SHAPE
+    assert moe.moe_grouped_swiglu_fp8(FAKE, FAKE, 64, FAKE, 4, 64, 256, 64, FAKE, FAKE, FAKE,
+                                      FAKE, FAKE, FAKE, FAKE, FAKE, None, **args) == E_SHAPE
+    assert moe.moe_grouped_swiglu_fp8(FAKE, FAKE, 63, FAKE, 4, 64, 256, 128, FAKE, FAKE, FAKE,
+                                      FAKE, FAKE, FAKE, FAKE, FAKE, None, **args) == E_ARG
+    assert moe.moe_grouped_swiglu_fp8(FAKE, FAKE, 64, FAKE, 513, 64, 256, 128, FAKE, FAKE, FAKE,
+                                      FAKE, FAKE, FAKE, FAKE, FAKE, None, **args) == E_SHAPE
+    assert moe.moe_grouped_swiglu_fp8(FAKE, FAKE, 64, None, 4, 64, 256, 128, FAKE, FAKE, FAKE,
+                                      FAKE, FAKE, FAKE, FAKE, FAKE, None, **args) == E_ARG
