@@ -60,6 +60,8 @@ def parse():
                     help="serving layout: redundant expert copies, planned from warm-up loads")
     ap.add_argument("--shared-stream", action="store_true",
                     help="run the shared expert on a second stream")
+    ap.add_argument("--precision", choices=["bf16", "fp8"], default="bf16",
+                    help="expert GEMM inputs: bf16, or E4M3 with 1x128 / 128x128 scales")
     return ap.parse_args()
 
 
@@ -154,10 +156,24 @@ class ClockSampler:
 
 
 # --------------------------------------------------------------------------
-def algorithmic(cfg, touched):
-    """Per-call algorithmic work (bytes moved at least once, dense FLOPs)."""
+def algorithmic(cfg, touched, fp8=False):
+    """Per-call algorithmic work (bytes moved at least once, dense FLOPs).
+    With fp8 the expert GEMMs read 1-byte weights and activations (scales
+    are 1/128 or less of that and not counted) and the dispatch quantizes x
+    (bf16 in, E4M3 out) before gathering 1-byte rows."""
     T, d, E, K, I, ns = cfg.T, cfg.d, cfg.E, cfg.K, cfg.I, cfg.n_shared
     R = T * K
+    if fp8:
+        return {
+            "route": dict(flops=2.0 * T * d * E * 3,
+                          bytes=T * d * 2 + 3 * E * d * 2 + 2 * T * E * 4 + T * K * 8),
+            "permute": dict(flops=0.0, bytes=4 * R * 4 + T * d * 3 + T * d + R * d),
+            "routed": dict(flops=6.0 * d * I * R,
+                           bytes=3.0 * touched * I * d + R * d + R * I * (2 + 2 + 1 + 1) + R * d * 2),
+            "shared": dict(flops=6.0 * d * I * ns * T,
+                           bytes=3.0 * ns * I * d + T * d + T * ns * I * 6 + T * d * 2),
+            "combine": dict(flops=0.0, bytes=(R + 2 * T) * d * 2 + T * K * 8),
+        }
     return {
         "route": dict(flops=2.0 * T * d * E * 3,
                       bytes=T * d * 2 + 3 * E * d * 2 + 2 * T * E * 4 + T * K * 8),
@@ -170,11 +186,13 @@ def algorithmic(cfg, touched):
     }
 
 
-def cpu_baseline(cfg, layer, x, n_tokens):
+def cpu_baseline(cfg, layer, x, n_tokens, fp8=False):
     """The oracle as it stands, timed on the host on `n_tokens` tokens of the
-    first batch (expert weights are fetched to host memory before timing)."""
+    first batch (expert weights are fetched to host memory, and for fp8
+    quantized by the oracle, before timing)."""
     import numpy as np
     import torch
+    from oracle import fp8_ref as f8
     from oracle import moe_ref as ref
 
     def f64(t):
@@ -193,6 +211,9 @@ def cpu_baseline(cfg, layer, x, n_tokens):
     host = {int(e): (layer.w1[e].cpu(), layer.w3[e].cpu(), layer.w2[e].cpu())
             for e in np.unique(idx)}
     shared_h = (layer.ws1.cpu(), layer.ws3.cpu(), layer.ws2.cpu())
+    if fp8:
+        hq = {e: f8.quantize_expert(*(f64(w) for w in ws)) for e, ws in host.items()}
+        shq = f8.quantize_expert(*(f64(w) for w in shared_h))
     t0 = time.perf_counter()
     x64 = f64(x_h)
     s = ref.router_affinity64(x64, w_r, off)
@@ -200,12 +221,16 @@ def cpu_baseline(cfg, layer, x, n_tokens):
                                    cfg.topk_groups, cfg.route_scale, precision="fp64")
     load = ref.expert_load(idx, cfg.E)
     ref.bias_update(load, bias, n_tokens, cfg.K, cfg.E, cfg.gamma)
-    ref.moe_output64(x64, idx, gate, lambda e: tuple(f64(w) for w in host[e]),
-                     tuple(f64(w) for w in shared_h), cfg.n_shared)
+    if fp8:
+        f8.moe_output64_fp8(x64, idx, gate, lambda e: hq[e], shq, cfg.n_shared)
+    else:
+        ref.moe_output64(x64, idx, gate, lambda e: tuple(f64(w) for w in host[e]),
+                         tuple(f64(w) for w in shared_h), cfg.n_shared)
     dt = time.perf_counter() - t0
     return {"value": n_tokens / dt, "unit": "tokens/s", "cores": blas_threads(), "kind": "oracle",
             "sample": f"{n_tokens} random tokens of the first {cfg.T}-token batch, full layer "
-                      f"(routing, {cfg.K} routed + {cfg.n_shared} shared SwiGLU experts in fp64, "
+                      f"(routing, {cfg.K} routed + {cfg.n_shared} shared SwiGLU experts in fp64"
+                      f"{' on E4M3-quantized operands' if fp8 else ''}, "
                       f"load count, bias update); {dt:.1f} s"}
 
 
@@ -226,8 +251,10 @@ def run_ours(args):
         group = dist.group.WORLD
     cfg = load_config(args.config)
     p = synth.make_params(cfg, "cuda")            # identical replicas on every rank
+    fp8 = args.precision == "fp8"
     layer = MoELayer(cfg, p, device=f"cuda:{local}", shared_stream=args.shared_stream,
-                     shared_as_routed=args.shared_as_routed, n_redundant=args.redundant)
+                     shared_as_routed=args.shared_as_routed, n_redundant=args.redundant,
+                     precision=args.precision)
     bias0 = layer.bias.clone()
     del p
     feedback = cfg.steps > 1                     # mid / drift: a bias-feedback run
@@ -322,7 +349,12 @@ def run_ours(args):
             dist.destroy_process_group()
         return
     pk = peaks()
-    alg = algorithmic(cfg, touched)
+    alg = algorithmic(cfg, touched, fp8)
+    # E4M3 dense peak: the measured bf16 figures times the nominal dense ratio
+    # (4.5 / 2.25 PFLOP/s)
+    tc_sust, tc_burst = (2 * pk["bf16_sust"], 2 * pk["bf16"]) if fp8 else (pk["bf16_sust"], pk["bf16"])
+    tc_kind = (f"E4M3 = 2 x bf16 sustained, {pk['src']} (nominal dense ratio)" if fp8
+               else f"bf16 sustained, {pk['src']}")
     kernels = {}
     if "shared" not in per:
         per["shared"] = 0.0                       # inside the routed call in the serving layout
@@ -336,7 +368,7 @@ def run_ours(args):
     routed_tf = alg["routed"]["flops"] / (per["routed"] * 1e-3) / 1e12
     if cfg.name == "v3_decode":
         # decode: the expert GEMMs stream the weights of the touched experts
-        wbytes = 3.0 * (touched + cfg.n_shared) * cfg.I * cfg.d * 2
+        wbytes = 3.0 * (touched + cfg.n_shared) * cfg.I * cfg.d * (1 if fp8 else 2)
         gbs = wbytes / ((per["routed"] + per["shared"]) * 1e-3) / 1e9
         roofline = {"bound": "hbm", "achieved": round(gbs, 1), "peak": pk["hbm"], "unit": "GB/s",
                     "frac": round(gbs / pk["hbm"], 4), "traffic": None,
@@ -344,17 +376,21 @@ def run_ours(args):
                     "peak_kind": f"HBM copy, {pk['src']}",
                     "weight_bytes_per_step": wbytes}
     else:
-        roofline = {"bound": "tensor", "achieved": round(routed_tf, 1), "peak": pk["bf16_sust"],
-                    "unit": "TFLOP/s", "frac": round(routed_tf / pk["bf16_sust"], 4),
-                    "traffic": GEMM_TRAFFIC_PER_EXPERT * touched if cfg.d == 7168 else None,
-                    "kernel": "moe_grouped_swiglu (routed experts: GEMM1+SwiGLU and GEMM2 launches)",
-                    "peak_kind": f"bf16 sustained, {pk['src']}",
-                    "frac_of_burst": round(routed_tf / pk["bf16"], 4)}
+        roofline = {"bound": "tensor", "achieved": round(routed_tf, 1), "peak": tc_sust,
+                    "unit": "TFLOP/s", "frac": round(routed_tf / tc_sust, 4),
+                    "traffic": (GEMM_TRAFFIC_PER_EXPERT * touched
+                                if cfg.d == 7168 and not fp8 else None),
+                    "kernel": ("moe_grouped_swiglu_fp8 (routed experts: GEMM1+SwiGLU, h "
+                               "quantization, GEMM2 launches)" if fp8 else
+                               "moe_grouped_swiglu (routed experts: GEMM1+SwiGLU and GEMM2 launches)"),
+                    "peak_kind": tc_kind,
+                    "frac_of_burst": round(routed_tf / tc_burst, 4)}
     layer_tf = cfg.expert_flops() / (ms_step * 1e-3) / 1e12
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "e4m3 expert GEMMs (fp32 promotion), bf16 activations" if fp8 else "bf16",
         "data": "synthetic (seeded N(0,1) tokens, N(0,0.02) weights, random-init)",
         "config": {"workload": f"{cfg.name}: T={cfg.T} d={cfg.d} E={cfg.E} K={cfg.K} "
                                f"shared={cfg.n_shared} I={cfg.I} groups={cfg.n_groups}/"
@@ -364,17 +400,19 @@ def run_ours(args):
                    if cfg.d == 7168 else "two alternating token batches",
                    "shared_stream": bool(args.shared_stream),
                    "shared_as_routed": bool(args.shared_as_routed),
-                   "redundant_experts": args.redundant},
+                   "redundant_experts": args.redundant,
+                   "precision": args.precision},
         "roofline": roofline,
         "layer_tensor_frac": {"expert_tflops": round(layer_tf, 1),
-                              "frac_of_sustained": round(layer_tf / pk["bf16_sust"], 4),
-                              "frac_of_burst": round(layer_tf / pk["bf16"], 4)},
+                              "frac_of_sustained": round(layer_tf / tc_sust, 4),
+                              "frac_of_burst": round(layer_tf / tc_burst, 4)},
         "kernels": kernels,
         "experts_touched": touched,
         "hbm_kernels": {n: {"gbs": kernels[n]["gbs"],
                             "frac": round(kernels[n]["gbs"] / pk["hbm"], 4)}
                         for n in ("permute", "combine")},
-        "gpu_launches": (KERNELS_PER_STEP - 2 * bool(args.shared_as_routed)
+        "gpu_launches": (KERNELS_PER_STEP + 3 * fp8
+                         - (3 if fp8 else 2) * bool(args.shared_as_routed)
                          + bool(args.redundant)) * args.steps,
         "device_status": status,
         "clocks": clk,
@@ -389,7 +427,7 @@ def run_ours(args):
                             "min": round(float(h[:, 2].min()), 4),
                             "max": round(float(h[:, 2].max()), 4)}
     if not args.no_cpu_baseline and world == 1:
-        line["cpu_baseline"] = cpu_baseline(cfg, layer, xs[0], args.cpu_sample)
+        line["cpu_baseline"] = cpu_baseline(cfg, layer, xs[0], args.cpu_sample, fp8)
     print(json.dumps(line), flush=True)
     if group is not None:
         dist.destroy_process_group()

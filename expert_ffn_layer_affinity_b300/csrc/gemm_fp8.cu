@@ -24,13 +24,23 @@
 // and meet with one shuffle.  TMEM holds two 256-column partial buffers: the
 // MMA fills one while the epilogue promotes the other.
 //
+// Scales travel by TMA as well: for every 128-deep k-block the producer
+// also fetches the tile's 256 activation scales and this CTA's weight
+// scale(s) into a ring of scale slots.  One k-block ahead, the epilogue turns
+// them into per-token-column products (activation scale x weight scale) in a
+// 4-deep buffer, so the promotion never waits for a global load.
+//
 // CTA layout (384 threads, one CTA per SM, persistent):
-//   warp 0       TMA producer (one 128-deep k-block of both operands per stage)
+//   warp 0       TMA producer (operands and scales of one k-block per stage)
 //   warp 1       TMEM allocator; lane 0 of the even CTA issues the MMAs
 //   warps 2, 3   idle
 //   warps 4..11  epilogue: two warps per TMEM lane quarter, each owning 128 of
-//                the 256 token columns (128 fp32 accumulators per thread); all
-//                eight stage the per-column scale products of the next k-block
+//                the 256 token columns (128 fp32 accumulators per thread).
+//                TMEM is read in the 16x256b shape, so a thread holds 4 rows x
+//                32 token columns and one 8-byte scale load serves 8
+//                accumulators (a row-per-thread read would need a broadcast
+//                shared-memory load per accumulator, which the shared-memory
+//                pipe cannot sustain at the tensor core's rate).
 // Registers: the first warpgroup gives its registers up (setmaxnreg.dec to
 // kCtrlRegs) and the two epilogue warpgroups take them (setmaxnreg.inc to
 // kEpiRegs).  The host checks, before every launch, that the split fits the
@@ -50,7 +60,6 @@ namespace {
 
 using gemm::decode_work;
 using gemm::kMaxGroups;
-using gemm::store_block_transposed;
 using gemm::tile_n;
 using gemm::wait_plain;
 
@@ -68,13 +77,26 @@ constexpr int kA = 128 * BK, kB = 128 * BK;  // per CTA: 128 weight rows, up to 
 constexpr int kStageBytes = kA + kB;
 constexpr int kBufCols = 256;
 constexpr int kTmemCols = 2 * kBufCols;
-constexpr int kXposeBytes = kEpiWarps * 32 * 80;
-constexpr int kScaleFloats = 2 * 2 * 256;  // [buffer][w1 / w3 variant][token column]
-// full[S], empty[S], accf[2], acce[2], drain, sfull[2]
-constexpr int kNumBars = 2 * kStages + 7;
-constexpr int kSmem = 1024 + kStages * kStageBytes + kXposeBytes + kScaleFloats * 4 +
-                      kNumBars * 8 + 16 + 2 * (kMaxGroups + 1) * 4;
+// scale slot: activation scales of tokens x0 .. x0+263 (x0 = first token
+// rounded down to a multiple of 4, two boxes of 128 and 136), then a box of
+// 4 weight scales; each box starts on a 128-byte boundary
+constexpr int kSaBox1 = 128, kSaBox2 = 136, kSwBox = 4;
+constexpr int kSlotW = 1152;       // byte offset of the weight-scale box
+constexpr int kSlotBytes = 1280;
+constexpr int kScaleTx = 4 * (kSaBox1 + kSaBox2 + kSwBox);
+constexpr int kSlots = 8;          // producer runs at most 8 k-blocks ahead of the epilogue
+constexpr int kProdBufs = 4;       // scale-product buffers (see the epilogue)
+// [w1 variant: 256 token columns][8 floats pad][w3 variant: 256 columns]: the
+// pad puts the two variants' same columns in different banks
+constexpr int kVar1 = 264;
+constexpr int kProdFloats = kVar1 + 256;
+// full[S], empty[S], accf[2], acce[2], drain, sfull[4], safull[8], saempty[8]
+constexpr int kNumBars = 2 * kStages + 5 + kProdBufs + 2 * kSlots;
+constexpr int kSmem = 1024 + kStages * kStageBytes + kSlots * kSlotBytes +
+                      kProdBufs * kProdFloats * 4 + kNumBars * 8 + 16 + 2 * (kMaxGroups + 1) * 4;
 static_assert(kStageBytes % 1024 == 0, "stages must keep 1024-byte alignment");
+static_assert(kSlotBytes % 128 == 0 && kSlotW % 128 == 0 && 4 * (kSaBox1 + kSaBox2) <= kSlotW,
+              "scale boxes start on 128-byte boundaries");
 static_assert(kSmem <= 227 * 1024, "shared memory");
 
 enum Fp8Mode : int { F8_SWIGLU = 0, F8_DOWN = 1 };
@@ -86,9 +108,6 @@ struct Fp8Params {
   int R;                 // token rows
   int num_kb;            // reduction length / 128
   int w_rows_per_group;  // weight operand rows per group (2I interleaved, or d)
-  const float* a_scale;  // [num_kb][ld_as]
-  int ld_as;
-  const float* w_scale;  // SwiGLU [G][I/128][num_kb][2]; down [G][d/128][num_kb]
   void* out;             // bf16 [R, ldo]
   int ldo;
   int32_t* status;
@@ -116,15 +135,19 @@ __device__ __forceinline__ Item item_of(int w, int NT, const int* mt_prefix, con
 template <int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
     fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
-                    const Fp8Params p) {
+                    const __grid_constant__ CUtensorMap tmSa1,
+                    const __grid_constant__ CUtensorMap tmSa2,
+                    const __grid_constant__ CUtensorMap tmSw, const Fp8Params p) {
   constexpr int kColTile = (MODE == F8_SWIGLU) ? 128 : 256;  // output columns per pair
+  constexpr int kNm = (MODE == F8_SWIGLU) ? 2 : 1;             // weight scales per k-block
   constexpr int S = kStages;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   const uint32_t tiles = (raw_addr + 1023u) & ~1023u;
-  uint8_t* xpose = smem_raw + (tiles - raw_addr) + S * kStageBytes;
-  float* sc = reinterpret_cast<float*>(xpose + kXposeBytes);
-  uint8_t* meta = reinterpret_cast<uint8_t*>(sc + kScaleFloats);
+  uint8_t* ring = smem_raw + (tiles - raw_addr) + S * kStageBytes;
+  const uint32_t ring_addr = tiles + S * kStageBytes;
+  float* prod = reinterpret_cast<float*>(ring + kSlots * kSlotBytes);
+  uint8_t* meta = reinterpret_cast<uint8_t*>(prod + kProdBufs * kProdFloats);
   const uint32_t bars = smem_u32(meta);
   auto full_bar = [&](int s) { return bars + 8u * s; };
   auto empty_bar = [&](int s) { return bars + 8u * (S + s); };
@@ -132,6 +155,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto acce_bar = [&](int b) { return bars + 8u * (2 * S + 2 + b); };
   const uint32_t drain_bar = bars + 8u * (2 * S + 4);
   auto sfull_bar = [&](int b) { return bars + 8u * (2 * S + 5 + b); };
+  auto safull_bar = [&](int k) { return bars + 8u * (2 * S + 5 + kProdBufs + k); };
+  auto saempty_bar = [&](int k) { return bars + 8u * (2 * S + 5 + kProdBufs + kSlots + k); };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(meta + 8 * kNumBars);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   int* mt_prefix = reinterpret_cast<int*>(meta + 8 * kNumBars + 16);
@@ -149,6 +174,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       tma_prefetch_desc(&tmW);
       tma_prefetch_desc(&tmX);
+      tma_prefetch_desc(&tmSa1);
+      tma_prefetch_desc(&tmSa2);
+      tma_prefetch_desc(&tmSw);
     }
   } else if (warp == 1) {
     if (lane == 0) {
@@ -159,7 +187,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int b = 0; b < 2; ++b) {
         mbar_init(accf_bar(b), 1);
         mbar_init(acce_bar(b), 2 * kEpiWarps);  // every epilogue warp of both CTAs
-        mbar_init(sfull_bar(b), kEpiWarps);     // every epilogue warp of this CTA
+      }
+      for (int b = 0; b < kProdBufs; ++b) mbar_init(sfull_bar(b), kEpiWarps);
+      for (int k = 0; k < kSlots; ++k) {
+        mbar_init(safull_bar(k), 1);
+        mbar_init(saempty_bar(k), kEpiWarps);
       }
       mbar_init(drain_bar, 1);
       *abort_flag = 0;
@@ -182,218 +214,247 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp < kEpiWarp0) {
     setmaxnreg_dec<kCtrlRegs>();
-  if (warp == 0) {
-    // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      const uint64_t pol_tok = l2_policy_evict_last();
-      const uint64_t pol_w = l2_policy_evict_normal();
-      uint32_t it = 0;
-      bool ok = true;
-      for (int w = unit_id; w < total && ok; w += n_units) {
-        const Item t = item_of(w, NT, mt_prefix, row_start, G);
-        const int tok_row = static_cast<int>(t.row0) + static_cast<int>(rank) * (t.n_eff / 2);
-        const int w_row = t.g * p.w_rows_per_group + t.n * 256 + static_cast<int>(rank) * 128;
-        for (int j = 0; j < nkb; ++j, ++it) {
-          const int s = static_cast<int>(it % S);
-          const uint32_t ph = (it / S) & 1u;
-          if (!mbar_wait(empty_bar(s), ph ^ 1u, abort_flag, p.status)) {
-            ok = false;
-            break;
+    if (warp == 0) {
+      // ---------------------------------------------------------- producer
+      if (lane == 0) {
+        const uint64_t pol_tok = l2_policy_evict_last();
+        const uint64_t pol_w = l2_policy_evict_normal();
+        uint32_t it = 0;
+        bool ok = true;
+        for (int w = unit_id; w < total && ok; w += n_units) {
+          const Item t = item_of(w, NT, mt_prefix, row_start, G);
+          const int tok_row = static_cast<int>(t.row0) + static_cast<int>(rank) * (t.n_eff / 2);
+          const int w_row = t.g * p.w_rows_per_group + t.n * 256 + static_cast<int>(rank) * 128;
+          const int sa_x = static_cast<int>(t.row0) & ~3;
+          const int sw_row = (MODE == F8_SWIGLU) ? t.g * (p.N / 128) + t.n
+                                                 : t.g * (p.N / 128) + t.n * 2 + static_cast<int>(rank);
+          for (int j = 0; j < nkb; ++j, ++it) {
+            const int s = static_cast<int>(it % S);
+            const int k = static_cast<int>(it % kSlots);
+            if (!mbar_wait(empty_bar(s), ((it / S) & 1u) ^ 1u, abort_flag, p.status) ||
+                !mbar_wait(saempty_bar(k), ((it / kSlots) & 1u) ^ 1u, abort_flag, p.status)) {
+              ok = false;
+              break;
+            }
+            // this CTA's scales of the k-block, into its own slot
+            const uint32_t slot = ring_addr + static_cast<uint32_t>(k * kSlotBytes);
+            mbar_arrive_expect_tx(safull_bar(k), kScaleTx);
+            tma_load_2d(slot, &tmSa1, safull_bar(k), sa_x, j, pol_tok);
+            tma_load_2d(slot + 4 * kSaBox1, &tmSa2, safull_bar(k), sa_x + kSaBox1, j, pol_tok);
+            tma_load_2d(slot + kSlotW, &tmSw, safull_bar(k), (j * kNm) & ~3, sw_row, pol_w);
+            // operands: both CTAs' copies complete on the even CTA's barrier
+            const uint32_t sa = tiles + s * kStageBytes;
+            if (rank == 0) mbar_arrive_expect_tx(full_bar(s), 2u * kStageBytes);
+            const uint32_t fb = mapa_shared(full_bar(s), 0);
+            tma_load_2d_pair(sa, &tmW, fb, j * BK, w_row, pol_w);
+            tma_load_2d_pair(sa + kA, &tmX, fb, j * BK, tok_row, pol_tok);
           }
-          const uint32_t sa = tiles + s * kStageBytes;
-          // both CTAs' copies complete on the even CTA's barrier
-          if (rank == 0) mbar_arrive_expect_tx(full_bar(s), 2u * kStageBytes);
-          const uint32_t fb = mapa_shared(full_bar(s), 0);
-          tma_load_2d_pair(sa, &tmW, fb, j * BK, w_row, pol_w);
-          tma_load_2d_pair(sa + kA, &tmX, fb, j * BK, tok_row, pol_tok);
+        }
+        if (!ok) {
+          // let this CTA's own copies land before the CTA can exit
+          const uint32_t first = it > kSlots ? it - kSlots : 0u;
+          for (uint32_t j = first; j < it; ++j)
+            wait_plain(safull_bar(static_cast<int>(j % kSlots)), (j / kSlots) & 1u, 200000000ull);
+          if (rank == 0) {
+            const uint32_t f2 = it > S ? it - S : 0u;
+            for (uint32_t j = f2; j < it; ++j)
+              wait_plain(full_bar(static_cast<int>(j % S)), (j / S) & 1u, 200000000ull);
+          }
         }
       }
-      if (!ok && rank == 0) {
-        const uint32_t first = it > S ? it - S : 0u;
-        for (uint32_t j = first; j < it; ++j)
-          wait_plain(full_bar(static_cast<int>(j % S)), (j / S) & 1u, 200000000ull);
-      }
-    }
-    __syncwarp();
-  } else if (warp == 1) {
-    // ---------------------------------------------------------- MMA issuer
-    if (lane == 0 && rank == 0) {
-      uint32_t it = 0, unit = 0;
-      bool ok = true, issued = false;
-      for (int w = unit_id; w < total && ok; w += n_units) {
-        const Item t = item_of(w, NT, mt_prefix, row_start, G);
-        const uint32_t idesc = umma_idesc_e4m3(256, t.n_eff);
-        for (int j = 0; j < nkb; ++j, ++it, ++unit) {
-          const int b = static_cast<int>(unit & 1u);
-          if (!mbar_wait(acce_bar(b), ((unit >> 1) & 1u) ^ 1u, abort_flag, p.status)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const int s = static_cast<int>(it % S);
-          if (!mbar_wait(full_bar(s), (it / S) & 1u, abort_flag, p.status)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t sa = tiles + s * kStageBytes;
-          const uint64_t adesc = umma_sdesc_sw128(sa);
-          const uint64_t bdesc = umma_sdesc_sw128(sa + kA);
-          const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(b * kBufCols);
+      __syncwarp();
+    } else if (warp == 1) {
+      // -------------------------------------------------------- MMA issuer
+      if (lane == 0 && rank == 0) {
+        uint32_t it = 0;
+        bool ok = true, issued = false;
+        for (int w = unit_id; w < total && ok; w += n_units) {
+          const Item t = item_of(w, NT, mt_prefix, row_start, G);
+          const uint32_t idesc = umma_idesc_e4m3(256, t.n_eff);
+          for (int j = 0; j < nkb; ++j, ++it) {
+            const int b = static_cast<int>(it & 1u);
+            if (!mbar_wait(acce_bar(b), ((it >> 1) & 1u) ^ 1u, abort_flag, p.status)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const int s = static_cast<int>(it % S);
+            if (!mbar_wait(full_bar(s), (it / S) & 1u, abort_flag, p.status)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t sa = tiles + s * kStageBytes;
+            const uint64_t adesc = umma_sdesc_sw128(sa);
+            const uint64_t bdesc = umma_sdesc_sw128(sa + kA);
+            const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(b * kBufCols);
 #pragma unroll
-          for (int k = 0; k < BK / UMMA_K; ++k)
-            umma_f8_pair(d_tmem, adesc + 2ull * k, bdesc + 2ull * k, idesc, k > 0 ? 1u : 0u);
-          issued = true;
-          umma_commit_pair_mc(empty_bar(s), 0x3);
-          umma_commit_pair_mc(accf_bar(b), 0x3);
+            for (int k = 0; k < BK / UMMA_K; ++k)
+              umma_f8_pair(d_tmem, adesc + 2ull * k, bdesc + 2ull * k, idesc, k > 0 ? 1u : 0u);
+            issued = true;
+            umma_commit_pair_mc(empty_bar(s), 0x3);
+            umma_commit_pair_mc(accf_bar(b), 0x3);
+          }
+        }
+        if (!ok && issued) {
+          umma_commit_pair_mc(drain_bar, 0x1);
+          wait_plain(drain_bar, 0u, 200000000ull);
         }
       }
-      if (!ok && issued) {
-        umma_commit_pair_mc(drain_bar, 0x1);
-        wait_plain(drain_bar, 0u, 200000000ull);
-      }
+      __syncwarp();
     }
-    __syncwarp();
-  }
   } else {
     setmaxnreg_inc<kEpiRegs>();
     // ------------------------------------------------------------ epilogue
-    const int ew = warp - kEpiWarp0;  // 0..7
-    const int q = warp & 3;         // this warp may read TMEM lanes 32q .. 32q+31
-    const int half = ew >> 2;       // token columns half*128 .. half*128+127
-    const int col_thr = ew * 32 + lane;  // the token column whose scales this thread stages
-    uint8_t* xp = xpose + ew * 32 * 80;
-    const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
+    const int ew = warp - kEpiWarp0;      // 0..7
+    const int q = warp & 3;               // this warp may read TMEM lanes 32q .. 32q+31
+    const int half = ew >> 2;             // token columns half*128 .. half*128+127
+    const int col_thr = ew * 32 + lane;   // the token column whose scale products this thread makes
+    const int tq = lane & 3, tr = lane >> 2;
+    const uint32_t taddr_lo = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
+    const uint32_t taddr_hi = tmem_base + (static_cast<uint32_t>(q * 32 + 16) << 16);
     __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out);
 
-    // scale of (item, k-block j) for column col_thr: activation scale and the
-    // weight scale(s) of this CTA's rows
-    auto fetch = [&](const Item& t, int j, float& sa, float& s0, float& s1) {
-      sa = 0.0f;
-      if (col_thr < t.rows_tile && t.row0 + col_thr < p.R)
-        sa = __ldg(p.a_scale + static_cast<long long>(j) * p.ld_as + t.row0 + col_thr);
-      if (MODE == F8_SWIGLU) {
-        const float2 wv = __ldg(reinterpret_cast<const float2*>(p.w_scale) +
-                                static_cast<long long>(t.g * (p.N / 128) + t.n) * p.num_kb + j);
-        s0 = wv.x;
-        s1 = wv.y;
-      } else {
-        const int blk = t.n * 2 + static_cast<int>(rank);
-        s0 = (blk * 128 < p.N)
-                 ? __ldg(p.w_scale + static_cast<long long>(t.g * (p.N / 128) + blk) * p.num_kb + j)
-                 : 0.0f;
-        s1 = 0.0f;
+    // Scale products of k-block `u` (item t, block j): the slot's activation
+    // scale of column col_thr times this CTA's weight scale(s), into product
+    // buffer u % 4.  Four buffers suffice: a warp writing u+1 has seen every
+    // warp stage u-1, so no warp still reads u-3.
+    auto stage = [&](uint32_t u, const Item& t, int j) -> bool {
+      const int k = static_cast<int>(u % kSlots);
+      if (!__all_sync(0xFFFFFFFFu,
+                      mbar_wait(safull_bar(k), (u / kSlots) & 1u, abort_flag, p.status)))
+        return false;
+      const float* sl = reinterpret_cast<const float*>(ring + k * kSlotBytes);
+      const float a = col_thr < t.rows_tile ? sl[(static_cast<int>(t.row0) & 3) + col_thr] : 0.0f;
+      const float* sw = sl + kSlotW / 4 + ((j * kNm) & 3);
+      float* pb = prod + (u % kProdBufs) * kProdFloats;
+      pb[col_thr] = a * sw[0];
+      if (MODE == F8_SWIGLU) pb[kVar1 + col_thr] = a * sw[1];
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(sfull_bar(static_cast<int>(u % kProdBufs)));
+        mbar_arrive(saempty_bar(k));
       }
+      return true;
     };
 
-    uint32_t unit = 0;
+    uint32_t u = 0;
     bool ok = true;
-    float nsa = 0.0f, ns0 = 0.0f, ns1 = 0.0f;
-    if (unit_id < total) fetch(item_of(unit_id, NT, mt_prefix, row_start, G), 0, nsa, ns0, ns1);
+    if (unit_id < total) ok = stage(0, item_of(unit_id, NT, mt_prefix, row_start, G), 0);
     for (int w = unit_id; w < total && ok; w += n_units) {
       const Item t = item_of(w, NT, mt_prefix, row_start, G);
       const bool has_next = w + n_units < total;
       const Item nx = has_next ? item_of(w + n_units, NT, mt_prefix, row_start, G) : t;
       int nc = t.n_eff - half * 128;
       nc = nc < 0 ? 0 : (nc > 128 ? 128 : nc);
-      float acc[128];
+      // acc[c][m][k]: chunk c (32 columns), repeat m (8 columns), row slot k
+      // (rows tr, tr+8, tr+16, tr+24 of this warp's lane quarter); .x/.y =
+      // columns half*128 + 32c + 8m + 2tq + {0, 1}
+      float2 acc[4][4][4];
 #pragma unroll
-      for (int i = 0; i < 128; ++i) acc[i] = 0.0f;
+      for (int c = 0; c < 4; ++c)
+#pragma unroll
+        for (int m = 0; m < 4; ++m)
+#pragma unroll
+          for (int k = 0; k < 4; ++k) acc[c][m][k] = make_float2(0.0f, 0.0f);
 
-      for (int j = 0; j < nkb; ++j, ++unit) {
-        const int bsel = static_cast<int>(unit & 1u);
-        const uint32_t par = (unit >> 1) & 1u;
-        float* scb = sc + bsel * 512;
-        scb[col_thr] = nsa * ns0;
-        if (MODE == F8_SWIGLU) scb[256 + col_thr] = nsa * ns1;
-        __syncwarp();
-        if (lane == 0) mbar_arrive(sfull_bar(bsel));
-        if (j + 1 < nkb) fetch(t, j + 1, nsa, ns0, ns1);
-        else if (has_next) fetch(nx, 0, nsa, ns0, ns1);
-        ok = __all_sync(0xFFFFFFFFu, mbar_wait(sfull_bar(bsel), par, abort_flag, p.status));
+      for (int j = 0; j < nkb; ++j, ++u) {
+        if (j + 1 < nkb) ok = stage(u + 1, t, j + 1);
+        else if (has_next) ok = stage(u + 1, nx, 0);
         if (!ok) break;
-        ok = __all_sync(0xFFFFFFFFu, mbar_wait(accf_bar(bsel), par, abort_flag, p.status));
+        const int pbi = static_cast<int>(u % kProdBufs);
+        const int bsel = static_cast<int>(u & 1u);
+        ok = __all_sync(0xFFFFFFFFu,
+                        mbar_wait(sfull_bar(pbi), (u / kProdBufs) & 1u, abort_flag, p.status));
+        if (!ok) break;
+        ok = __all_sync(0xFFFFFFFFu,
+                        mbar_wait(accf_bar(bsel), (u >> 1) & 1u, abort_flag, p.status));
         if (!ok) break;
         tc_fence_after();
-        const float* srow = scb + ((MODE == F8_SWIGLU && (lane & 1)) ? 256 : 0) + half * 128;
-        const uint32_t taddr =
-            tmem_base + lane_base + static_cast<uint32_t>(bsel * kBufCols + half * 128);
+        const float* srow = prod + pbi * kProdFloats + ((MODE == F8_SWIGLU && (tr & 1)) ? kVar1 : 0) +
+                            half * 128 + 2 * tq;
+        const uint32_t col0 = static_cast<uint32_t>(bsel * kBufCols + half * 128);
 #pragma unroll
-        for (int c = 0; c < 128; c += 32) {
-          if (c < nc) {
-            uint32_t v[32];
-            tmem_ld32(taddr + c, v);
+        for (int c = 0; c < 4; ++c) {
+          if (32 * c < nc) {
+            uint32_t lo[16], hi[16];
+            tmem_ld16x256b_x4(taddr_lo + col0 + 32 * c, lo);
+            tmem_ld16x256b_x4(taddr_hi + col0 + 32 * c, hi);
             tmem_ld_wait();
 #pragma unroll
-            for (int i = 0; i < 32; i += 4) {
-              const float4 s4 = *reinterpret_cast<const float4*>(srow + c + i);
-              acc[c + i] = fmaf(__uint_as_float(v[i]), s4.x, acc[c + i]);
-              acc[c + i + 1] = fmaf(__uint_as_float(v[i + 1]), s4.y, acc[c + i + 1]);
-              acc[c + i + 2] = fmaf(__uint_as_float(v[i + 2]), s4.z, acc[c + i + 2]);
-              acc[c + i + 3] = fmaf(__uint_as_float(v[i + 3]), s4.w, acc[c + i + 3]);
+            for (int m = 0; m < 4; ++m) {
+              const float2 sc2 = *reinterpret_cast<const float2*>(srow + 32 * c + 8 * m);
+              acc[c][m][0] = __ffma2_rn(make_float2(__uint_as_float(lo[4 * m]),
+                                                    __uint_as_float(lo[4 * m + 1])), sc2, acc[c][m][0]);
+              acc[c][m][1] = __ffma2_rn(make_float2(__uint_as_float(lo[4 * m + 2]),
+                                                    __uint_as_float(lo[4 * m + 3])), sc2, acc[c][m][1]);
+              acc[c][m][2] = __ffma2_rn(make_float2(__uint_as_float(hi[4 * m]),
+                                                    __uint_as_float(hi[4 * m + 1])), sc2, acc[c][m][2]);
+              acc[c][m][3] = __ffma2_rn(make_float2(__uint_as_float(hi[4 * m + 2]),
+                                                    __uint_as_float(hi[4 * m + 3])), sc2, acc[c][m][3]);
             }
           }
         }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive_cluster(mapa_shared(acce_bar(bsel), 0));
+        if (lane == 0) mbar_arrive_remote(mapa_shared(acce_bar(bsel), 0));
       }
       if (!ok) break;
 
-      // ---- store this thread's 128 token columns
+      // ---- store (tokens half*128 + 32c + 8m + 2tq + e, e = 0, 1)
+      const int t0 = half * 128;
+      int nvalid = t.rows_tile - t0;
+      if (nvalid > nc) nvalid = nc;
+      const long long over = t.row0 + t0 + nvalid - p.R;
+      if (over > 0) nvalid -= static_cast<int>(over);
+      __nv_bfloat16* obase = out + (t.row0 + t0) * p.ldo;
       if (MODE == F8_SWIGLU) {
-        const int ibase = t.n * 128 + static_cast<int>(rank) * 64 + q * 16;  // first h column
-        const bool odd = (lane & 1) != 0;
-        const int pcol = lane >> 1;
-        __nv_bfloat16* x = reinterpret_cast<__nv_bfloat16*>(xp);
+        // rows tr + 8k are gate (tr even) or up (tr odd) of h column
+        // tr/2 + 4k; the partner row sits in lane ^ 4.  The gate lane makes
+        // and stores h for the even token of each pair, the up lane for the
+        // odd one.
+        const bool up = (tr & 1) != 0;
+        const int colb = t.n * 128 + static_cast<int>(rank) * 64 + q * 16 + (tr >> 1);
 #pragma unroll
-        for (int c = 0; c < 128; c += 32) {
-          if (c < nc) {
-            float h[32];
+        for (int c = 0; c < 4; ++c) {
+          if (32 * c < nc) {
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              const float o = __shfl_xor_sync(0xFFFFFFFFu, acc[c + i], 1);
-              const float a = odd ? o : acc[c + i];
-              const float u = odd ? acc[c + i] : o;
-              h[i] = a * __frcp_rn(1.0f + __expf(-a)) * u;
-            }
-            // stage [32 tokens][16 h columns]: even lanes tokens 0..15, odd
-            // lanes tokens 16..31 (rows an odd distance apart: no bank clash)
+            for (int m = 0; m < 4; ++m) {
+              const int tok = 32 * c + 8 * m + 2 * tq + (up ? 1 : 0);
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              const int row = odd ? 16 + (i ^ 1) : i;
-              x[row * 16 + pcol] = __float2bfloat16_rn(odd ? h[16 + (i ^ 1)] : h[i]);
+              for (int k = 0; k < 4; ++k) {
+                const float2 mine = acc[c][m][k];
+                const float ox = __shfl_xor_sync(0xFFFFFFFFu, mine.x, 4);
+                const float oy = __shfl_xor_sync(0xFFFFFFFFu, mine.y, 4);
+                const float g = up ? oy : mine.x;
+                const float v = up ? mine.y : ox;
+                const float h = g * __frcp_rn(1.0f + __expf(-g)) * v;
+                if (tok < nvalid)
+                  obase[static_cast<long long>(tok) * p.ldo + colb + 4 * k] = __float2bfloat16_rn(h);
+              }
             }
-            __syncwarp();
-            const int t0 = half * 128 + c;
-            int valid = t.rows_tile - t0;
-            valid = valid > 32 ? 32 : valid;
-            const long long last = t.row0 + t0 + valid;
-            if (last > p.R) valid -= static_cast<int>(last - p.R);
-            if (lane < valid && ibase < p.N) {
-              const uint4* src = reinterpret_cast<const uint4*>(xp + lane * 32);
-              uint4* dst = reinterpret_cast<uint4*>(out + (t.row0 + t0 + lane) * p.ldo + ibase);
-              dst[0] = src[0];
-              dst[1] = src[1];
-            }
-            __syncwarp();
           }
         }
       } else {
-        const int colbase = t.n * 256 + static_cast<int>(rank) * 128 + q * 32;
-        if (colbase < p.N) {
+        const int colb = t.n * 256 + static_cast<int>(rank) * 128 + q * 32 + tr;
 #pragma unroll
-          for (int c = 0; c < 128; c += 32) {
-            if (c < nc) {
-              uint32_t v[32];
+        for (int c = 0; c < 4; ++c) {
+          if (32 * c < nc) {
 #pragma unroll
-              for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(acc[c + i]);
-              const int t0 = half * 128 + c;
-              int valid = t.rows_tile - t0;
-              valid = valid > 32 ? 32 : valid;
-              const long long last = t.row0 + t0 + valid;
-              if (last > p.R) valid -= static_cast<int>(last - p.R);
-              store_block_transposed(v, xp, lane, out, t.row0 + t0, valid, p.ldo, colbase);
+            for (int m = 0; m < 4; ++m) {
+              const int tok = 32 * c + 8 * m + 2 * tq;
+#pragma unroll
+              for (int k = 0; k < 4; ++k) {
+                const int col = colb + 8 * k;
+                if (col < p.N) {
+                  if (tok < nvalid)
+                    obase[static_cast<long long>(tok) * p.ldo + col] =
+                        __float2bfloat16_rn(acc[c][m][k].x);
+                  if (tok + 1 < nvalid)
+                    obase[static_cast<long long>(tok + 1) * p.ldo + col] =
+                        __float2bfloat16_rn(acc[c][m][k].y);
+                }
+              }
             }
           }
         }
@@ -413,8 +474,25 @@ bool make_map_u8(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer
   return gemm::make_map_sw128(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, ptr, inner, outer, 128);
 }
 
+// fp32 rows [outer, inner] (inner % 4 == 0), box = box_inner x 1, no swizzle.
+bool make_map_f32_rows(CUtensorMap* m, const float* ptr, uint64_t inner, uint64_t outer,
+                       uint32_t box_inner) {
+  auto fn = gemm::encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {inner * 4};
+  cuuint32_t box[2] = {box_inner, 1};
+  cuuint32_t estr[2] = {1, 1};
+  const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(ptr), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 template <int MODE>
-cudaError_t launch_fp8(const CUtensorMap& w, const CUtensorMap& x, const Fp8Params& p,
+cudaError_t launch_fp8(const CUtensorMap& w, const CUtensorMap& x, const CUtensorMap& sa1,
+                       const CUtensorMap& sa2, const CUtensorMap& sw, const Fp8Params& p,
                        int max_units, cudaStream_t s) {
   static bool attr_done[64] = {false};
   int dev = 0;
@@ -446,10 +524,12 @@ cudaError_t launch_fp8(const CUtensorMap& w, const CUtensorMap& x, const Fp8Para
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, fp8_gemm_kernel<MODE>, w, x, p);
+  return cudaLaunchKernelEx(&cfg, fp8_gemm_kernel<MODE>, w, x, sa1, sa2, sw, p);
 }
 
 }  // namespace
+
+int fp8_scale_pitch(int pairs, int cols) { return (pairs * (cols / 128) + 3) & ~3; }
 
 cudaError_t launch_grouped_swiglu_fp8(const uint8_t* a_q, const float* a_s, int ld_as,
                                       const int32_t* offsets, int G, int R, int d, int I,
@@ -458,41 +538,45 @@ cudaError_t launch_grouped_swiglu_fp8(const uint8_t* a_q, const float* a_s, int 
                                       uint8_t* h_q, float* h_s, uint16_t* y, int32_t* status,
                                       cudaStream_t s) {
   if (R == 0 || G == 0) return cudaSuccess;
-  if (G > kMaxGroups) return cudaErrorInvalidValue;
-  CUtensorMap tw13, tx, tw2, th;
+  if (G > kMaxGroups || ld_as % 4) return cudaErrorInvalidValue;
+  const int ld_h = (R + 3) & ~3;
+  const int kb1 = d / BK, kb2 = I / BK;
+  CUtensorMap tw13, tx, tw2, th, ta1, ta2, tsw13, th1, th2, tsw2;
   if (!make_map_u8(&tw13, w13_q, d, static_cast<uint64_t>(G) * 2 * I) ||
       !make_map_u8(&tx, a_q, d, R) ||
       !make_map_u8(&tw2, w2_q, I, static_cast<uint64_t>(G) * d) ||
-      !make_map_u8(&th, h_q, I, R))
+      !make_map_u8(&th, h_q, I, R) ||
+      !make_map_f32_rows(&ta1, a_s, ld_as, kb1, kSaBox1) ||
+      !make_map_f32_rows(&ta2, a_s, ld_as, kb1, kSaBox2) ||
+      !make_map_f32_rows(&tsw13, w13_s, fp8_scale_pitch(2, d), static_cast<uint64_t>(G) * (I / 128),
+                         kSwBox) ||
+      !make_map_f32_rows(&th1, h_s, ld_h, kb2, kSaBox1) ||
+      !make_map_f32_rows(&th2, h_s, ld_h, kb2, kSaBox2) ||
+      !make_map_f32_rows(&tsw2, w2_s, fp8_scale_pitch(1, I), static_cast<uint64_t>(G) * (d / 128),
+                         kSwBox))
     return cudaErrorInvalidValue;
   Fp8Params p1{};
   p1.group_offsets = offsets;
   p1.G = G;
   p1.N = I;
   p1.R = R;
-  p1.num_kb = d / BK;
+  p1.num_kb = kb1;
   p1.w_rows_per_group = 2 * I;
-  p1.a_scale = a_s;
-  p1.ld_as = ld_as;
-  p1.w_scale = w13_s;
   p1.out = h;
   p1.ldo = I;
   p1.status = status;
   const int mt = (R + kTokTile - 1) / kTokTile + G;
-  cudaError_t e = launch_fp8<F8_SWIGLU>(tw13, tx, p1, mt * (I / 128), s);
+  cudaError_t e = launch_fp8<F8_SWIGLU>(tw13, tx, ta1, ta2, tsw13, p1, mt * (I / 128), s);
   if (e != cudaSuccess) return e;
-  e = launch_quantize_rows(h, R, I, h_q, h_s, R, s);
+  e = launch_quantize_rows(h, R, I, h_q, h_s, ld_h, s);
   if (e != cudaSuccess) return e;
   Fp8Params p2 = p1;
   p2.N = d;
-  p2.num_kb = I / BK;
+  p2.num_kb = kb2;
   p2.w_rows_per_group = d;
-  p2.a_scale = h_s;
-  p2.ld_as = R;
-  p2.w_scale = w2_s;
   p2.out = y;
   p2.ldo = d;
-  return launch_fp8<F8_DOWN>(tw2, th, p2, mt * ((d + 255) / 256), s);
+  return launch_fp8<F8_DOWN>(tw2, th, th1, th2, tsw2, p2, mt * ((d + 255) / 256), s);
 }
 
 }  // namespace moe

@@ -245,9 +245,11 @@ moe_status moe_grouped_swiglu_fp8(const void* a_q, const float* a_s, int ld_as,
   if (R > 0 && (!a_q || !a_s || !group_offsets || !w13_q || !w13_s || !w2_q || !w2_s ||
                 !h_bf16 || !h_q || !h_s || !y_bf16))
     return MOE_ERR_INVALID_ARG;
-  if (d % 128 || I % 128 || n_groups > 512) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (d % 128 || I % 128 || n_groups > 512 || ld_as % 4)
+    return MOE_ERR_UNSUPPORTED_SHAPE;
   if (R > 0 && (!aligned16(a_q) || !aligned16(w13_q) || !aligned16(w2_q) || !aligned16(h_bf16) ||
-                !aligned16(h_q) || !aligned16(y_bf16) || !aligned16(w13_s)))
+                !aligned16(h_q) || !aligned16(y_bf16) || !aligned16(w13_s) ||
+                !aligned16(w2_s) || !aligned16(a_s) || !aligned16(h_s)))
     return MOE_ERR_UNSUPPORTED_SHAPE;
   return cuda_status(launch_grouped_swiglu_fp8(
       static_cast<const uint8_t*>(a_q), a_s, ld_as, group_offsets, n_groups, R, d, I,

@@ -326,3 +326,29 @@ __device__ __forceinline__ void setmaxnreg_dec() {
   asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
 }
 }  // namespace moe
+
+namespace moe {
+// Arrive on an mbarrier of either CTA of the cluster with the default
+// (CTA-scope release) semantics: no cluster-wide memory fence.  For handing
+// a TMEM buffer back to the MMA issuer, whose ordering the tcgen05 fences
+// around the arrive and the wait already provide.
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+}  // namespace moe
+
+namespace moe {
+// 16 TMEM lanes x 4 repeats of 8 consecutive 32-bit columns.  For repeat m,
+// thread i gets r[4m], r[4m+1] from lane (base + i/4), columns
+// 8m + 2(i%4) and 8m + 2(i%4) + 1, and r[4m+2], r[4m+3] from lane
+// (base + 8 + i/4), the same two columns.
+__device__ __forceinline__ void tmem_ld16x256b_x4(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.16x256b.x4.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+}
+}  // namespace moe

@@ -58,7 +58,9 @@ __global__ void __launch_bounds__(256) quant_rows_kernel(const uint16_t* __restr
 // One CTA (256 threads) per 128 x 128 block.  Thread t holds row t/2,
 // columns (t%2)*64 .. +63 of the block.  With a second matrix (w_pair), the
 // two are written row-interleaved: output row 2i is w's row i, 2i+1 is
-// w_pair's row i, and the two block scales sit side by side.
+// w_pair's row i, and the two block scales sit side by side.  Each row of
+// block scales is padded to a multiple of 4 floats, so the GEMM can fetch
+// them with 16-byte TMA boxes.
 __global__ void __launch_bounds__(256) quant_blocks_kernel(const uint16_t* __restrict__ w,
                                                            const uint16_t* __restrict__ w_pair,
                                                            int rows, int cols,
@@ -111,8 +113,9 @@ __global__ void __launch_bounds__(256) quant_blocks_kernel(const uint16_t* __res
     dst[k] = make_uint4(o[0], o[1], o[2], o[3]);
   }
   if (t == 0) {
-    const size_t si = (static_cast<size_t>(g) * nbr + br) * nbc + bc;
-    s[nm == 2 ? si * 2 + which : si] = sc;
+    // rows of block scales padded to a multiple of 4 floats (16 bytes)
+    const int pitch = (nm * nbc + 3) & ~3;
+    s[(static_cast<size_t>(g) * nbr + br) * pitch + bc * nm + which] = sc;
   }
 }
 

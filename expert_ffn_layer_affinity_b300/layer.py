@@ -32,6 +32,10 @@ from . import _lib as L
 from .synth import LayerConfig
 
 
+def _round4(v: int) -> int:
+    return (v + 3) // 4 * 4
+
+
 class MoELayer:
     def __init__(self, cfg: LayerConfig, params: dict, max_T: int | None = None,
                  device: str = "cuda", keep_affinity: bool = False,
@@ -109,16 +113,17 @@ class MoELayer:
         c, dev = self.cfg, self.device
         E, d, I, nI = self.E_phys, c.d, c.I, c.n_shared * c.I
         u8, f32 = torch.uint8, torch.float32
+        r4 = _round4
         self.w13_q = torch.empty(E, 2 * I, d, dtype=u8, device=dev)
-        self.w13_s = torch.empty(E, I // 128, d // 128, 2, dtype=f32, device=dev)
+        self.w13_s = torch.empty(E, I // 128, r4(2 * d // 128), dtype=f32, device=dev)
         self.w2_q = torch.empty(E, d, I, dtype=u8, device=dev)
-        self.w2_s = torch.empty(E, d // 128, I // 128, dtype=f32, device=dev)
+        self.w2_s = torch.empty(E, d // 128, r4(I // 128), dtype=f32, device=dev)
         L.moe_quantize_weights_fp8(self.w1, self.w3, E, I, d, self.w13_q, self.w13_s)
         L.moe_quantize_weights_fp8(self.w2, None, E, d, I, self.w2_q, self.w2_s)
         self.ws13_q = torch.empty(1, 2 * nI, d, dtype=u8, device=dev)
-        self.ws13_s = torch.empty(1, nI // 128, d // 128, 2, dtype=f32, device=dev)
+        self.ws13_s = torch.empty(1, nI // 128, r4(2 * d // 128), dtype=f32, device=dev)
         self.ws2_q = torch.empty(1, d, nI, dtype=u8, device=dev)
-        self.ws2_s = torch.empty(1, d // 128, nI // 128, dtype=f32, device=dev)
+        self.ws2_s = torch.empty(1, d // 128, r4(nI // 128), dtype=f32, device=dev)
         L.moe_quantize_weights_fp8(self.ws1, self.ws3, 1, nI, d, self.ws13_q, self.ws13_s)
         L.moe_quantize_weights_fp8(self.ws2, None, 1, d, nI, self.ws2_q, self.ws2_s)
 
@@ -158,15 +163,17 @@ class MoELayer:
         if self.fp8:
             u8, f32 = torch.uint8, torch.float32
             self.x_perm = None
+            # rows of activation scales: leading dimensions rounded to 4 floats
+            self.ld_xs, self.ld_xsp = _round4(T), _round4(R)
             self.xq = torch.empty(T, d, dtype=u8, device=dev)
-            self.xs = torch.empty(d // 128, T, dtype=f32, device=dev)
+            self.xs = torch.empty(d // 128, self.ld_xs, dtype=f32, device=dev)
             self.xq_perm = torch.empty(R, d, dtype=u8, device=dev)
-            self.xs_perm = torch.empty(d // 128, R, dtype=f32, device=dev)
+            self.xs_perm = torch.empty(d // 128, self.ld_xsp, dtype=f32, device=dev)
             self.hq = torch.empty(R, I, dtype=u8, device=dev)
-            self.hs = torch.empty(I // 128, R, dtype=f32, device=dev)
+            self.hs = torch.empty(I // 128, _round4(R), dtype=f32, device=dev)
             if not self.shared_as_routed:
                 self.hq_sh = torch.empty(T, ns * I, dtype=u8, device=dev)
-                self.hs_sh = torch.empty(ns * I // 128, T, dtype=f32, device=dev)
+                self.hs_sh = torch.empty(ns * I // 128, _round4(T), dtype=f32, device=dev)
         self.T_cap = T
         self._shared_T = T
 
@@ -270,7 +277,7 @@ class MoELayer:
         T = x.shape[0]
         K = self.K_slots
         R = T * K
-        Tc, Rc = self.T_cap, self.T_cap * K
+        Tc, Rc = self.ld_xs, self.ld_xsp
         main = torch.cuda.current_stream() if stream is None else stream
         mark("permute", 0)
         L.moe_permute(idx, T, K, self.E_phys, None, c.d, self.offsets, self.row_of, self.tok_of,

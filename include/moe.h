@@ -238,13 +238,17 @@ moe_status moe_quantize_fp8(const void* x_bf16, int rows, int cols, void* q_out,
 /* Quantize weights bf16 [groups, rows, cols] per 128 x 128 block (rows and
  * cols multiples of 128).
  *  w_pair_bf16 == NULL: q_out uint8 [groups, rows, cols], s_out fp32
- *    [groups, rows/128, cols/128] (the down projection w2, rows = d).
+ *    [groups, rows/128, pitch] with pitch = round_up(cols/128, 4): scale of
+ *    block (r, c) at [g, r, c] (the down projection w2, rows = d).
  *  w_pair_bf16 != NULL (a second matrix of the same shape): the two are
  *    written ROW-INTERLEAVED for the SwiGLU GEMM, q_out uint8
  *    [groups, 2*rows, cols] with row 2i = w_bf16 row i and row 2i+1 =
- *    w_pair_bf16 row i, s_out fp32 [groups, rows/128, cols/128, 2] (the two
- *    matrices' block scales side by side).  Pass w1 and w3.
- * The quantized layout is what moe_grouped_swiglu_fp8 reads. */
+ *    w_pair_bf16 row i; s_out fp32 [groups, rows/128, pitch] with pitch =
+ *    round_up(2*cols/128, 4): the two matrices' block scales side by side,
+ *    block (r, c) of w_bf16 at [g, r, 2c], of w_pair_bf16 at [g, r, 2c+1].
+ *    Pass w1 and w3.
+ * Padding floats at the end of each scale row are not written.  The
+ * quantized layout is what moe_grouped_swiglu_fp8 reads. */
 moe_status moe_quantize_weights_fp8(const void* w_bf16, const void* w_pair_bf16, int groups,
                                     int rows, int cols, void* q_out, float* s_out,
                                     moe_stream_t stream);
@@ -262,12 +266,13 @@ moe_status moe_permute_fp8(const void* q_in, const float* s_in, int ld_in, int T
  *   h = bf16(silu(a . w1[g]^T) * (a . w3[g]^T)),  h quantized per 1 x 128,
  *   y = bf16(h . w2[g]^T)
  * with every product an E4M3 GEMM promoted to fp32 per 128-deep block.
- *  a_q uint8 [R, d], a_s fp32 [d/128][ld_as] (ld_as >= R);
+ *  a_q uint8 [R, d], a_s fp32 [d/128][ld_as] (ld_as >= R, ld_as % 4 == 0,
+ *  so that rows of scales can be fetched by TMA);
  *  group_offsets [n_groups+1] DEVICE int32, 1 <= n_groups <= 512;
  *  w13_q / w13_s and w2_q / w2_s as written by moe_quantize_weights_fp8
  *  (w1 paired with w3; w2 alone, rows = d);
- *  h_bf16 [R, I] and h_q uint8 [R, I], h_s fp32 [I/128][R]: scratch that
- *  holds h (bf16 and quantized) on return; y_bf16 [R, d].
+ *  h_bf16 [R, I] and h_q uint8 [R, I], h_s fp32 [I/128][round_up(R, 4)]:
+ *  scratch that holds h (bf16 and quantized) on return; y_bf16 [R, d].
  * Shared experts: n_groups = 1, offsets {0, T}, I = n_shared * expert width. */
 moe_status moe_grouped_swiglu_fp8(const void* a_q, const float* a_s, int ld_as,
                                   const int32_t* group_offsets, int n_groups, int R, int d, int I,

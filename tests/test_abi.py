@@ -118,3 +118,6 @@ def test_fp8_calls_reject_bad_arguments():
                                       FAKE, FAKE, FAKE, FAKE, FAKE, None, **args) == E_SHAPE
     assert moe.moe_grouped_swiglu_fp8(FAKE, FAKE, 64, None, 4, 64, 256, 128, FAKE, FAKE, FAKE,
                                       FAKE, FAKE, FAKE, FAKE, FAKE, None, **args) == E_ARG
+    # rows of activation scales must be whole 16-byte units (ld_as % 4 == 0)
+    assert moe.moe_grouped_swiglu_fp8(FAKE, FAKE, 66, FAKE, 4, 64, 256, 128, FAKE, FAKE, FAKE,
+                                      FAKE, FAKE, FAKE, FAKE, FAKE, None, **args) == E_SHAPE

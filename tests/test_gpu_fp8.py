@@ -63,8 +63,9 @@ def test_quantize_weights_bit_exact(pair):
     w[1, :128, 128:256] *= 1000
     w2 = (torch.randn(G, rows, cols, generator=g) * 0.02).to(torch.bfloat16) if pair else None
     nm = 2 if pair else 1
+    pitch = (nm * (cols // 128) + 3) // 4 * 4
     q = torch.zeros(G, nm * rows, cols, dtype=torch.uint8, device=DEV)
-    s = torch.zeros(G, rows // 128, cols // 128, nm, device=DEV)
+    s = torch.full((G, rows // 128, pitch), -1.0, device=DEV)
     moe.moe_quantize_weights_fp8(w.to(DEV), w2.to(DEV) if pair else None, G, rows, cols, q, s)
     torch.cuda.synchronize()
     qv = e4m3_values(q)
@@ -75,7 +76,9 @@ def test_quantize_weights_bit_exact(pair):
             wq, ws = F8.quantize_w_128x128(bf16_to_np64(m))
             got = qv[gi, which::nm] if pair else qv[gi]
             assert same_values(got, wq)
-            assert np.array_equal(sv[gi, :, :, which].view(np.uint32), ws.view(np.uint32))
+            got_s = sv[gi, :, which:nm * (cols // 128):nm]
+            assert np.array_equal(got_s.view(np.uint32), ws.view(np.uint32))
+    assert np.all(sv[:, :, nm * (cols // 128):] == -1.0)       # row padding untouched
 
 
 def test_permute_fp8_exact():
@@ -107,21 +110,23 @@ def run_fp8_experts(a, offsets, w1, w3, w2):
     """Quantize with the library and run the FP8 grouped experts."""
     R, d = a.shape
     G, I, _ = w1.shape
+    r4 = lambda v: (v + 3) // 4 * 4  # noqa: E731
+    ld_as = r4(R + 1)
     aq = torch.zeros(R, d, dtype=torch.uint8, device=DEV)
-    as_ = torch.zeros(d // 128, R + 1, device=DEV)
+    as_ = torch.zeros(d // 128, ld_as, device=DEV)
     w13q = torch.zeros(G, 2 * I, d, dtype=torch.uint8, device=DEV)
-    w13s = torch.zeros(G, I // 128, d // 128, 2, device=DEV)
+    w13s = torch.zeros(G, I // 128, r4(2 * d // 128), device=DEV)
     w2q = torch.zeros(G, d, I, dtype=torch.uint8, device=DEV)
-    w2s = torch.zeros(G, d // 128, I // 128, device=DEV)
+    w2s = torch.zeros(G, d // 128, r4(I // 128), device=DEV)
     h = torch.full((R, I), 7.0, dtype=torch.bfloat16, device=DEV)
     hq = torch.zeros(R, I, dtype=torch.uint8, device=DEV)
-    hs = torch.zeros(I // 128, R, device=DEV)
+    hs = torch.zeros(I // 128, r4(R), device=DEV)
     y = torch.full((R, d), -3.0, dtype=torch.bfloat16, device=DEV)
     status = torch.zeros(1, dtype=torch.int32, device=DEV)
-    moe.moe_quantize_fp8(a.to(DEV), R, d, aq, as_, R + 1)
+    moe.moe_quantize_fp8(a.to(DEV), R, d, aq, as_, ld_as)
     moe.moe_quantize_weights_fp8(w1.to(DEV), w3.to(DEV), G, I, d, w13q, w13s)
     moe.moe_quantize_weights_fp8(w2.to(DEV), None, G, d, I, w2q, w2s)
-    moe.moe_grouped_swiglu_fp8(aq, as_, R + 1, offsets.to(DEV), G, R, d, I, w13q, w13s, w2q, w2s,
+    moe.moe_grouped_swiglu_fp8(aq, as_, ld_as, offsets.to(DEV), G, R, d, I, w13q, w13s, w2q, w2s,
                                h, hq, hs, y, status)
     st = sync_status(status)
     return h.cpu(), y.cpu(), st
