@@ -26,14 +26,18 @@
 //
 // Scales travel by TMA as well: for every 128-deep k-block the producer
 // also fetches the tile's 256 activation scales and this CTA's weight
-// scale(s) into a ring of scale slots.  One k-block ahead, the epilogue turns
-// them into per-token-column products (activation scale x weight scale) in a
-// 4-deep buffer, so the promotion never waits for a global load.
+// scale(s) into a ring of scale slots.  A stager warp turns them into
+// per-token-column products (activation scale x weight scale) in a 4-deep
+// buffer ahead of the epilogue, so the promotion never waits for a global
+// load and the epilogue warps only load TMEM, multiply-add and hand buffers
+// back (each TMEM buffer as soon as its last chunk is in registers).
 //
 // CTA layout (384 threads, one CTA per SM, persistent):
 //   warp 0       TMA producer (operands and scales of one k-block per stage)
 //   warp 1       TMEM allocator; lane 0 of the even CTA issues the MMAs
-//   warps 2, 3   idle
+//   warp 2       scale stager: per k-block, the activation x weight scale
+//                products of the tile's 256 token columns (one k-block ahead)
+//   warp 3       idle
 //   warps 4..11  epilogue: two warps per TMEM lane quarter, each owning 128 of
 //                the 256 token columns (128 fp32 accumulators per thread).
 //                TMEM is read in the 16x256b shape, so a thread holds 4 rows x
@@ -90,8 +94,8 @@ constexpr int kProdBufs = 4;       // scale-product buffers (see the epilogue)
 // pad puts the two variants' same columns in different banks
 constexpr int kVar1 = 264;
 constexpr int kProdFloats = kVar1 + 256;
-// full[S], empty[S], accf[2], acce[2], drain, sfull[4], safull[8], saempty[8]
-constexpr int kNumBars = 2 * kStages + 5 + kProdBufs + 2 * kSlots;
+// full[S], empty[S], accf[2], acce[2], drain, sfull[4], safull[8], saempty[8], pempty[4]
+constexpr int kNumBars = 2 * kStages + 5 + 2 * kProdBufs + 2 * kSlots;
 constexpr int kSmem = 1024 + kStages * kStageBytes + kSlots * kSlotBytes +
                       kProdBufs * kProdFloats * 4 + kNumBars * 8 + 16 + 2 * (kMaxGroups + 1) * 4;
 static_assert(kStageBytes % 1024 == 0, "stages must keep 1024-byte alignment");
@@ -157,6 +161,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto sfull_bar = [&](int b) { return bars + 8u * (2 * S + 5 + b); };
   auto safull_bar = [&](int k) { return bars + 8u * (2 * S + 5 + kProdBufs + k); };
   auto saempty_bar = [&](int k) { return bars + 8u * (2 * S + 5 + kProdBufs + kSlots + k); };
+  auto pempty_bar = [&](int b) { return bars + 8u * (2 * S + 5 + kProdBufs + 2 * kSlots + b); };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(meta + 8 * kNumBars);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   int* mt_prefix = reinterpret_cast<int*>(meta + 8 * kNumBars + 16);
@@ -188,10 +193,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(accf_bar(b), 1);
         mbar_init(acce_bar(b), 2 * kEpiWarps);  // every epilogue warp of both CTAs
       }
-      for (int b = 0; b < kProdBufs; ++b) mbar_init(sfull_bar(b), kEpiWarps);
+      for (int b = 0; b < kProdBufs; ++b) {
+        mbar_init(sfull_bar(b), 1);            // the scale stager
+        mbar_init(pempty_bar(b), kEpiWarps);   // every epilogue warp of this CTA
+      }
       for (int k = 0; k < kSlots; ++k) {
         mbar_init(safull_bar(k), 1);
-        mbar_init(saempty_bar(k), kEpiWarps);
+        mbar_init(saempty_bar(k), 1);          // the scale stager
       }
       mbar_init(drain_bar, 1);
       *abort_flag = 0;
@@ -302,6 +310,42 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       __syncwarp();
+    } else if (warp == 2) {
+      // ------------------------------------------------------ scale stager
+      // Per k-block: the activation scale of each token column times this
+      // CTA's weight scale(s), into product buffer v % 4 (8 columns per lane).
+      uint32_t v = 0;
+      bool ok = true;
+      for (int w = unit_id; w < total && ok; w += n_units) {
+        const Item t = item_of(w, NT, mt_prefix, row_start, G);
+        const int x0 = static_cast<int>(t.row0) & 3;
+        for (int j = 0; j < nkb; ++j, ++v) {
+          const int k = static_cast<int>(v % kSlots);
+          const int b = static_cast<int>(v % kProdBufs);
+          ok = __all_sync(0xFFFFFFFFu,
+                          mbar_wait(safull_bar(k), (v / kSlots) & 1u, abort_flag, p.status) &&
+                              mbar_wait(pempty_bar(b), ((v / kProdBufs) & 1u) ^ 1u, abort_flag,
+                                        p.status));
+          if (!ok) break;
+          const float* sl = reinterpret_cast<const float*>(ring + k * kSlotBytes);
+          const float* sw = sl + kSlotW / 4 + ((j * kNm) & 3);
+          const float w0 = sw[0], w1 = (MODE == F8_SWIGLU) ? sw[1] : 0.0f;
+          float* pb = prod + b * kProdFloats;
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const int col = lane + 32 * i;
+            const float a = col < t.rows_tile ? sl[x0 + col] : 0.0f;
+            pb[col] = a * w0;
+            if (MODE == F8_SWIGLU) pb[kVar1 + col] = a * w1;
+          }
+          __syncwarp();
+          if (lane == 0) {
+            mbar_arrive(sfull_bar(b));
+            mbar_arrive(saempty_bar(k));
+          }
+        }
+      }
+      __syncwarp();
     }
   } else {
     setmaxnreg_inc<kEpiRegs>();
@@ -309,44 +353,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int ew = warp - kEpiWarp0;      // 0..7
     const int q = warp & 3;               // this warp may read TMEM lanes 32q .. 32q+31
     const int half = ew >> 2;             // token columns half*128 .. half*128+127
-    const int col_thr = ew * 32 + lane;   // the token column whose scale products this thread makes
     const int tq = lane & 3, tr = lane >> 2;
     const uint32_t taddr_lo = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
     const uint32_t taddr_hi = tmem_base + (static_cast<uint32_t>(q * 32 + 16) << 16);
     __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out);
 
-    // Scale products of k-block `u` (item t, block j): the slot's activation
-    // scale of column col_thr times this CTA's weight scale(s), into product
-    // buffer u % 4.  Four buffers suffice: a warp writing u+1 has seen every
-    // warp stage u-1, so no warp still reads u-3.
-    auto stage = [&](uint32_t u, const Item& t, int j) -> bool {
-      const int k = static_cast<int>(u % kSlots);
-      if (!__all_sync(0xFFFFFFFFu,
-                      mbar_wait(safull_bar(k), (u / kSlots) & 1u, abort_flag, p.status)))
-        return false;
-      const float* sl = reinterpret_cast<const float*>(ring + k * kSlotBytes);
-      const float a = col_thr < t.rows_tile ? sl[(static_cast<int>(t.row0) & 3) + col_thr] : 0.0f;
-      const float* sw = sl + kSlotW / 4 + ((j * kNm) & 3);
-      float* pb = prod + (u % kProdBufs) * kProdFloats;
-      pb[col_thr] = a * sw[0];
-      if (MODE == F8_SWIGLU) pb[kVar1 + col_thr] = a * sw[1];
-      __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(sfull_bar(static_cast<int>(u % kProdBufs)));
-        mbar_arrive(saempty_bar(k));
-      }
-      return true;
+    // TMEM reads of chunk c (32 token columns) of the buffer at column col0
+    auto tld = [&](uint32_t col0, int c, uint32_t (&lo)[16], uint32_t (&hi)[16]) {
+      tmem_ld16x256b_x4(taddr_lo + col0 + 32 * c, lo);
+      tmem_ld16x256b_x4(taddr_hi + col0 + 32 * c, hi);
     };
 
     uint32_t u = 0;
     bool ok = true;
-    if (unit_id < total) ok = stage(0, item_of(unit_id, NT, mt_prefix, row_start, G), 0);
     for (int w = unit_id; w < total && ok; w += n_units) {
       const Item t = item_of(w, NT, mt_prefix, row_start, G);
-      const bool has_next = w + n_units < total;
-      const Item nx = has_next ? item_of(w + n_units, NT, mt_prefix, row_start, G) : t;
       int nc = t.n_eff - half * 128;
       nc = nc < 0 ? 0 : (nc > 128 ? 128 : nc);
+      const int nch = nc / 32;
       // acc[c][m][k]: chunk c (32 columns), repeat m (8 columns), row slot k
       // (rows tr, tr+8, tr+16, tr+24 of this warp's lane quarter); .x/.y =
       // columns half*128 + 32c + 8m + 2tq + {0, 1}
@@ -359,45 +383,73 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int k = 0; k < 4; ++k) acc[c][m][k] = make_float2(0.0f, 0.0f);
 
       for (int j = 0; j < nkb; ++j, ++u) {
-        if (j + 1 < nkb) ok = stage(u + 1, t, j + 1);
-        else if (has_next) ok = stage(u + 1, nx, 0);
-        if (!ok) break;
         const int pbi = static_cast<int>(u % kProdBufs);
         const int bsel = static_cast<int>(u & 1u);
         ok = __all_sync(0xFFFFFFFFu,
-                        mbar_wait(sfull_bar(pbi), (u / kProdBufs) & 1u, abort_flag, p.status));
-        if (!ok) break;
-        ok = __all_sync(0xFFFFFFFFu,
-                        mbar_wait(accf_bar(bsel), (u >> 1) & 1u, abort_flag, p.status));
+                        mbar_wait(sfull_bar(pbi), (u / kProdBufs) & 1u, abort_flag, p.status) &&
+                            mbar_wait(accf_bar(bsel), (u >> 1) & 1u, abort_flag, p.status));
         if (!ok) break;
         tc_fence_after();
         const float* srow = prod + pbi * kProdFloats + ((MODE == F8_SWIGLU && (tr & 1)) ? kVar1 : 0) +
                             half * 128 + 2 * tq;
         const uint32_t col0 = static_cast<uint32_t>(bsel * kBufCols + half * 128);
+        // hand the TMEM buffer back as soon as its last chunk is in registers
+        auto release = [&]() {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive_remote(mapa_shared(acce_bar(bsel), 0));
+        };
+        // acc += P * (activation scale x weight scale), one chunk
+        auto promote = [&](float2 (&a)[4][4], const uint32_t (&lo)[16], const uint32_t (&hi)[16],
+                           int c) {
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          if (32 * c < nc) {
-            uint32_t lo[16], hi[16];
-            tmem_ld16x256b_x4(taddr_lo + col0 + 32 * c, lo);
-            tmem_ld16x256b_x4(taddr_hi + col0 + 32 * c, hi);
-            tmem_ld_wait();
-#pragma unroll
-            for (int m = 0; m < 4; ++m) {
-              const float2 sc2 = *reinterpret_cast<const float2*>(srow + 32 * c + 8 * m);
-              acc[c][m][0] = __ffma2_rn(make_float2(__uint_as_float(lo[4 * m]),
-                                                    __uint_as_float(lo[4 * m + 1])), sc2, acc[c][m][0]);
-              acc[c][m][1] = __ffma2_rn(make_float2(__uint_as_float(lo[4 * m + 2]),
-                                                    __uint_as_float(lo[4 * m + 3])), sc2, acc[c][m][1]);
-              acc[c][m][2] = __ffma2_rn(make_float2(__uint_as_float(hi[4 * m]),
-                                                    __uint_as_float(hi[4 * m + 1])), sc2, acc[c][m][2]);
-              acc[c][m][3] = __ffma2_rn(make_float2(__uint_as_float(hi[4 * m + 2]),
-                                                    __uint_as_float(hi[4 * m + 3])), sc2, acc[c][m][3]);
-            }
+          for (int m = 0; m < 4; ++m) {
+            const float2 sc2 = *reinterpret_cast<const float2*>(srow + 32 * c + 8 * m);
+            a[m][0] = __ffma2_rn(make_float2(__uint_as_float(lo[4 * m]), __uint_as_float(lo[4 * m + 1])),
+                                 sc2, a[m][0]);
+            a[m][1] = __ffma2_rn(make_float2(__uint_as_float(lo[4 * m + 2]),
+                                             __uint_as_float(lo[4 * m + 3])), sc2, a[m][1]);
+            a[m][2] = __ffma2_rn(make_float2(__uint_as_float(hi[4 * m]), __uint_as_float(hi[4 * m + 1])),
+                                 sc2, a[m][2]);
+            a[m][3] = __ffma2_rn(make_float2(__uint_as_float(hi[4 * m + 2]),
+                                             __uint_as_float(hi[4 * m + 3])), sc2, a[m][3]);
           }
+        };
+        // two register buffers: chunk c+1 loads while chunk c is promoted
+        uint32_t lo0[16], hi0[16], lo1[16], hi1[16];
+        if (nch > 0) tld(col0, 0, lo0, hi0);
+        tmem_ld_wait();
+        reg_fence16(lo0);
+        reg_fence16(hi0);
+        if (nch > 1) tld(col0, 1, lo1, hi1);
+        else release();
+        if (nch > 0) promote(acc[0], lo0, hi0, 0);
+        if (nch > 1) {
+          tmem_ld_wait();
+          reg_fence16(lo1);
+          reg_fence16(hi1);
+          if (nch > 2) tld(col0, 2, lo0, hi0);
+          else release();
+          promote(acc[1], lo1, hi1, 1);
         }
-        tc_fence_before();
+        if (nch > 2) {
+          tmem_ld_wait();
+          reg_fence16(lo0);
+          reg_fence16(hi0);
+          if (nch > 3) tld(col0, 3, lo1, hi1);
+          else release();
+          promote(acc[2], lo0, hi0, 2);
+        }
+        if (nch > 3) {
+          tmem_ld_wait();
+          reg_fence16(lo1);
+          reg_fence16(hi1);
+          release();
+          promote(acc[3], lo1, hi1, 3);
+        }
+        // the products of this k-block are no longer read
         __syncwarp();
-        if (lane == 0) mbar_arrive_remote(mapa_shared(acce_bar(bsel), 0));
+        if (lane == 0) mbar_arrive(pempty_bar(pbi));
       }
       if (!ok) break;
 

@@ -352,3 +352,14 @@ __device__ __forceinline__ void tmem_ld16x256b_x4(uint32_t taddr, uint32_t (&r)[
       : "r"(taddr));
 }
 }  // namespace moe
+
+namespace moe {
+// Marks 16 registers as rewritten here, so no use of a tcgen05.ld result can
+// be scheduled before the tcgen05.wait::ld that precedes this call.
+__device__ __forceinline__ void reg_fence16(uint32_t (&r)[16]) {
+  asm volatile(""
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),
+                 "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]),
+                 "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]));
+}
+}  // namespace moe
