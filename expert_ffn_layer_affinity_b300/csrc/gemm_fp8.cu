@@ -10,41 +10,39 @@
 // reduction elements.  Here a 128-deep k-block is exactly one promotion
 // interval and one scale block:
 //
-//   P_j      = sum over the 128 k of k-block j of qw[row, k] * qa[tok, k]
+//   P_j      = sum over the 128 k of k-block j of qa[tok, k] * qw[row, k]
 //              (tensor core, into its own TMEM buffer)
-//   acc     += P_j * (sw[row block, j] * sa[j, tok])   (fp32 FFMA, registers)
+//   acc     += P_j * (sa[j, tok] * sw[row block, j])   (fp32 FFMA, registers)
 //
 //   F8_SWIGLU  h[tok, i] = bf16(silu(acc_w1) * acc_w3)
 //   F8_DOWN    y[tok, c] = bf16(acc)
 //
-// Layout: CTA pairs (cta_group::2) with 256 weight rows on M (128 per CTA)
-// and up to 256 tokens on N, as in the bf16 kernel.  For SwiGLU the weights
-// are stored row-interleaved (row 2i = w1 row i, row 2i+1 = w3 row i), so
-// the gate and up values of one output column sit in neighbouring TMEM lanes
-// and meet with one shuffle.  TMEM holds two 256-column partial buffers: the
-// MMA fills one while the epilogue promotes the other.
+// Layout: CTA pairs (cta_group::2).  TOKENS are on the MMA's M side (256 per
+// pair tile, 128 in each CTA's TMEM lanes) and 256 WEIGHT rows on N (128
+// staged in each CTA).  Each epilogue thread thus owns one token and 128
+// weight columns: its activation scale is one number per k-block and the
+// weight scales are at most two, so the promotion is a plain fused
+// multiply-add per accumulator with no per-column scale traffic, and TMEM
+// is read in the fast 32x32b shape.  (The other orientation, weights on M as
+// in the bf16 kernel, needs a per-token-column scale for every accumulator;
+// measured on B300, its shared-memory scale reads and the slower 16x256b
+// TMEM shape cost about twice as much per k-block.)  Reading each k-block's
+// fp32 partial out of TMEM is what bounds this kernel; ragged token tiles
+// only waste tensor-core work, which is not the limit.
 //
-// Scales travel by TMA as well: for every 128-deep k-block the producer
-// also fetches the tile's 256 activation scales and this CTA's weight
-// scale(s) into a ring of scale slots.  A stager warp turns them into
-// per-token-column products (activation scale x weight scale) in a 4-deep
-// buffer ahead of the epilogue, so the promotion never waits for a global
-// load and the epilogue warps only load TMEM, multiply-add and hand buffers
-// back (each TMEM buffer as soon as its last chunk is in registers).
+// For SwiGLU the weights are stored row-interleaved (row 2i = w1 row i, row
+// 2i+1 = w3 row i), so the gate and up values of one output column are
+// neighbouring accumulators of the same thread.  TMEM holds two 256-column
+// partial buffers: the MMA fills one while the epilogue promotes the other,
+// and each buffer goes back as soon as its last chunk is in registers.
+// Scales arrive by TMA with the operands, into a ring of scale slots.
 //
 // CTA layout (384 threads, one CTA per SM, persistent):
 //   warp 0       TMA producer (operands and scales of one k-block per stage)
 //   warp 1       TMEM allocator; lane 0 of the even CTA issues the MMAs
-//   warp 2       scale stager: per k-block, the activation x weight scale
-//                products of the tile's 256 token columns (one k-block ahead)
-//   warp 3       idle
-//   warps 4..11  epilogue: two warps per TMEM lane quarter, each owning 128 of
-//                the 256 token columns (128 fp32 accumulators per thread).
-//                TMEM is read in the 16x256b shape, so a thread holds 4 rows x
-//                32 token columns and one 8-byte scale load serves 8
-//                accumulators (a row-per-thread read would need a broadcast
-//                shared-memory load per accumulator, which the shared-memory
-//                pipe cannot sustain at the tensor core's rate).
+//   warps 2, 3   idle
+//   warps 4..11  epilogue: two warps per TMEM lane quarter (32 tokens), one
+//                for weight columns 0..127, one for 128..255
 // Registers: the first warpgroup gives its registers up (setmaxnreg.dec to
 // kCtrlRegs) and the two epilogue warpgroups take them (setmaxnreg.inc to
 // kEpiRegs).  The host checks, before every launch, that the split fits the
@@ -64,7 +62,6 @@ namespace {
 
 using gemm::decode_work;
 using gemm::kMaxGroups;
-using gemm::tile_n;
 using gemm::wait_plain;
 
 constexpr int BK = 128;      // E4M3 values (bytes) per k-block = promotion interval
@@ -77,30 +74,26 @@ constexpr int kCtrlRegs = 56, kEpiRegs = 224;
 constexpr int kSplitRegs = 128 * kCtrlRegs + 32 * kEpiWarps * kEpiRegs;
 constexpr int kStages = 6;
 constexpr int kTokTile = 256;
-constexpr int kA = 128 * BK, kB = 128 * BK;  // per CTA: 128 weight rows, up to 128 token rows
+constexpr int kA = 128 * BK, kB = 128 * BK;  // per CTA: 128 token rows, 128 weight rows
 constexpr int kStageBytes = kA + kB;
 constexpr int kBufCols = 256;
 constexpr int kTmemCols = 2 * kBufCols;
 // scale slot: activation scales of tokens x0 .. x0+263 (x0 = first token
 // rounded down to a multiple of 4, two boxes of 128 and 136), then a box of
-// 4 weight scales; each box starts on a 128-byte boundary
-constexpr int kSaBox1 = 128, kSaBox2 = 136, kSwBox = 4;
+// 2 x 4 weight scales; each box starts on a 128-byte boundary
+constexpr int kSaBox1 = 128, kSaBox2 = 136, kSwBox = 4, kSwRows = 2;
 constexpr int kSlotW = 1152;       // byte offset of the weight-scale box
 constexpr int kSlotBytes = 1280;
-constexpr int kScaleTx = 4 * (kSaBox1 + kSaBox2 + kSwBox);
+constexpr int kScaleTx = 4 * (kSaBox1 + kSaBox2 + kSwBox * kSwRows);
 constexpr int kSlots = 8;          // producer runs at most 8 k-blocks ahead of the epilogue
-constexpr int kProdBufs = 4;       // scale-product buffers (see the epilogue)
-// [w1 variant: 256 token columns][8 floats pad][w3 variant: 256 columns]: the
-// pad puts the two variants' same columns in different banks
-constexpr int kVar1 = 264;
-constexpr int kProdFloats = kVar1 + 256;
-// full[S], empty[S], accf[2], acce[2], drain, sfull[4], safull[8], saempty[8], pempty[4]
-constexpr int kNumBars = 2 * kStages + 5 + 2 * kProdBufs + 2 * kSlots;
-constexpr int kSmem = 1024 + kStages * kStageBytes + kSlots * kSlotBytes +
-                      kProdBufs * kProdFloats * 4 + kNumBars * 8 + 16 + 2 * (kMaxGroups + 1) * 4;
+// full[S], empty[S], accf[2], acce[2], drain, safull[8], saempty[8]
+constexpr int kNumBars = 2 * kStages + 5 + 2 * kSlots;
+constexpr int kSmem = 1024 + kStages * kStageBytes + kSlots * kSlotBytes + kNumBars * 8 + 16 +
+                      2 * (kMaxGroups + 1) * 4;
 static_assert(kStageBytes % 1024 == 0, "stages must keep 1024-byte alignment");
-static_assert(kSlotBytes % 128 == 0 && kSlotW % 128 == 0 && 4 * (kSaBox1 + kSaBox2) <= kSlotW,
-              "scale boxes start on 128-byte boundaries");
+static_assert(kSlotBytes % 128 == 0 && kSlotW % 128 == 0 && 4 * (kSaBox1 + kSaBox2) <= kSlotW &&
+                  kSlotW + 4 * kSwBox * kSwRows <= kSlotBytes,
+              "scale boxes start on 128-byte boundaries and fit the slot");
 static_assert(kSmem <= 227 * 1024, "shared memory");
 
 enum Fp8Mode : int { F8_SWIGLU = 0, F8_DOWN = 1 };
@@ -121,7 +114,6 @@ struct Item {
   int g, n, m;
   long long row0;  // first token row of the tile
   int rows_tile;   // token rows of the tile that belong to the group
-  int n_eff;       // MMA N (rows_tile rounded up to 32)
 };
 
 __device__ __forceinline__ Item item_of(int w, int NT, const int* mt_prefix, const int* row_start,
@@ -132,7 +124,6 @@ __device__ __forceinline__ Item item_of(int w, int NT, const int* mt_prefix, con
   const int tok0 = it.m * kTokTile;
   it.row0 = static_cast<long long>(row_start[it.g]) + tok0;
   it.rows_tile = (rows_g - tok0) < kTokTile ? rows_g - tok0 : kTokTile;
-  it.n_eff = tile_n(rows_g - tok0, kTokTile);
   return it;
 }
 
@@ -142,26 +133,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const __grid_constant__ CUtensorMap tmSa1,
                     const __grid_constant__ CUtensorMap tmSa2,
                     const __grid_constant__ CUtensorMap tmSw, const Fp8Params p) {
-  constexpr int kColTile = (MODE == F8_SWIGLU) ? 128 : 256;  // output columns per pair
-  constexpr int kNm = (MODE == F8_SWIGLU) ? 2 : 1;             // weight scales per k-block
   constexpr int S = kStages;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   const uint32_t tiles = (raw_addr + 1023u) & ~1023u;
   uint8_t* ring = smem_raw + (tiles - raw_addr) + S * kStageBytes;
   const uint32_t ring_addr = tiles + S * kStageBytes;
-  float* prod = reinterpret_cast<float*>(ring + kSlots * kSlotBytes);
-  uint8_t* meta = reinterpret_cast<uint8_t*>(prod + kProdBufs * kProdFloats);
+  uint8_t* meta = ring + kSlots * kSlotBytes;
   const uint32_t bars = smem_u32(meta);
   auto full_bar = [&](int s) { return bars + 8u * s; };
   auto empty_bar = [&](int s) { return bars + 8u * (S + s); };
   auto accf_bar = [&](int b) { return bars + 8u * (2 * S + b); };
   auto acce_bar = [&](int b) { return bars + 8u * (2 * S + 2 + b); };
   const uint32_t drain_bar = bars + 8u * (2 * S + 4);
-  auto sfull_bar = [&](int b) { return bars + 8u * (2 * S + 5 + b); };
-  auto safull_bar = [&](int k) { return bars + 8u * (2 * S + 5 + kProdBufs + k); };
-  auto saempty_bar = [&](int k) { return bars + 8u * (2 * S + 5 + kProdBufs + kSlots + k); };
-  auto pempty_bar = [&](int b) { return bars + 8u * (2 * S + 5 + kProdBufs + 2 * kSlots + b); };
+  auto safull_bar = [&](int k) { return bars + 8u * (2 * S + 5 + k); };
+  auto saempty_bar = [&](int k) { return bars + 8u * (2 * S + 5 + kSlots + k); };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(meta + 8 * kNumBars);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   int* mt_prefix = reinterpret_cast<int*>(meta + 8 * kNumBars + 16);
@@ -193,13 +179,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(accf_bar(b), 1);
         mbar_init(acce_bar(b), 2 * kEpiWarps);  // every epilogue warp of both CTAs
       }
-      for (int b = 0; b < kProdBufs; ++b) {
-        mbar_init(sfull_bar(b), 1);            // the scale stager
-        mbar_init(pempty_bar(b), kEpiWarps);   // every epilogue warp of this CTA
-      }
       for (int k = 0; k < kSlots; ++k) {
         mbar_init(safull_bar(k), 1);
-        mbar_init(saempty_bar(k), 1);          // the scale stager
+        mbar_init(saempty_bar(k), kEpiWarps);   // every epilogue warp of this CTA
       }
       mbar_init(drain_bar, 1);
       *abort_flag = 0;
@@ -216,7 +198,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
-  const int NT = (p.N + kColTile - 1) / kColTile;
+  // 256 weight rows per pair tile: 128 h columns (SwiGLU, w1/w3 interleaved)
+  // or 256 output columns (down projection)
+  const int NT = (MODE == F8_SWIGLU) ? p.N / 128 : (p.N + 255) / 256;
   const int total = mt_prefix[G] * NT;
   const int nkb = p.num_kb;
 
@@ -231,11 +215,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool ok = true;
         for (int w = unit_id; w < total && ok; w += n_units) {
           const Item t = item_of(w, NT, mt_prefix, row_start, G);
-          const int tok_row = static_cast<int>(t.row0) + static_cast<int>(rank) * (t.n_eff / 2);
+          const int tok_row = static_cast<int>(t.row0) + static_cast<int>(rank) * 128;
           const int w_row = t.g * p.w_rows_per_group + t.n * 256 + static_cast<int>(rank) * 128;
           const int sa_x = static_cast<int>(t.row0) & ~3;
+          // weight-scale rows of the tile: SwiGLU one (w1 and w3 side by
+          // side), down projection the tile's two 128-row blocks
           const int sw_row = (MODE == F8_SWIGLU) ? t.g * (p.N / 128) + t.n
-                                                 : t.g * (p.N / 128) + t.n * 2 + static_cast<int>(rank);
+                                                 : t.g * (p.N / 128) + t.n * 2;
           for (int j = 0; j < nkb; ++j, ++it) {
             const int s = static_cast<int>(it % S);
             const int k = static_cast<int>(it % kSlots);
@@ -249,13 +235,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_arrive_expect_tx(safull_bar(k), kScaleTx);
             tma_load_2d(slot, &tmSa1, safull_bar(k), sa_x, j, pol_tok);
             tma_load_2d(slot + 4 * kSaBox1, &tmSa2, safull_bar(k), sa_x + kSaBox1, j, pol_tok);
-            tma_load_2d(slot + kSlotW, &tmSw, safull_bar(k), (j * kNm) & ~3, sw_row, pol_w);
+            tma_load_2d(slot + kSlotW, &tmSw, safull_bar(k), (j * (MODE == F8_SWIGLU ? 2 : 1)) & ~3,
+                        sw_row, pol_w);
             // operands: both CTAs' copies complete on the even CTA's barrier
             const uint32_t sa = tiles + s * kStageBytes;
             if (rank == 0) mbar_arrive_expect_tx(full_bar(s), 2u * kStageBytes);
             const uint32_t fb = mapa_shared(full_bar(s), 0);
-            tma_load_2d_pair(sa, &tmW, fb, j * BK, w_row, pol_w);
-            tma_load_2d_pair(sa + kA, &tmX, fb, j * BK, tok_row, pol_tok);
+            tma_load_2d_pair(sa, &tmX, fb, j * BK, tok_row, pol_tok);
+            tma_load_2d_pair(sa + kA, &tmW, fb, j * BK, w_row, pol_w);
           }
         }
         if (!ok) {
@@ -276,9 +263,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0 && rank == 0) {
         uint32_t it = 0;
         bool ok = true, issued = false;
+        constexpr uint32_t idesc = umma_idesc_e4m3(256, 256);
         for (int w = unit_id; w < total && ok; w += n_units) {
-          const Item t = item_of(w, NT, mt_prefix, row_start, G);
-          const uint32_t idesc = umma_idesc_e4m3(256, t.n_eff);
           for (int j = 0; j < nkb; ++j, ++it) {
             const int b = static_cast<int>(it & 1u);
             if (!mbar_wait(acce_bar(b), ((it >> 1) & 1u) ^ 1u, abort_flag, p.status)) {
@@ -293,8 +279,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             tc_fence_after();
             const uint32_t sa = tiles + s * kStageBytes;
-            const uint64_t adesc = umma_sdesc_sw128(sa);
-            const uint64_t bdesc = umma_sdesc_sw128(sa + kA);
+            const uint64_t adesc = umma_sdesc_sw128(sa);        // tokens
+            const uint64_t bdesc = umma_sdesc_sw128(sa + kA);   // weights
             const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(b * kBufCols);
 #pragma unroll
             for (int k = 0; k < BK / UMMA_K; ++k)
@@ -310,203 +296,130 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       __syncwarp();
-    } else if (warp == 2) {
-      // ------------------------------------------------------ scale stager
-      // Per k-block: the activation scale of each token column times this
-      // CTA's weight scale(s), into product buffer v % 4 (8 columns per lane).
-      uint32_t v = 0;
-      bool ok = true;
-      for (int w = unit_id; w < total && ok; w += n_units) {
-        const Item t = item_of(w, NT, mt_prefix, row_start, G);
-        const int x0 = static_cast<int>(t.row0) & 3;
-        for (int j = 0; j < nkb; ++j, ++v) {
-          const int k = static_cast<int>(v % kSlots);
-          const int b = static_cast<int>(v % kProdBufs);
-          ok = __all_sync(0xFFFFFFFFu,
-                          mbar_wait(safull_bar(k), (v / kSlots) & 1u, abort_flag, p.status) &&
-                              mbar_wait(pempty_bar(b), ((v / kProdBufs) & 1u) ^ 1u, abort_flag,
-                                        p.status));
-          if (!ok) break;
-          const float* sl = reinterpret_cast<const float*>(ring + k * kSlotBytes);
-          const float* sw = sl + kSlotW / 4 + ((j * kNm) & 3);
-          const float w0 = sw[0], w1 = (MODE == F8_SWIGLU) ? sw[1] : 0.0f;
-          float* pb = prod + b * kProdFloats;
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const int col = lane + 32 * i;
-            const float a = col < t.rows_tile ? sl[x0 + col] : 0.0f;
-            pb[col] = a * w0;
-            if (MODE == F8_SWIGLU) pb[kVar1 + col] = a * w1;
-          }
-          __syncwarp();
-          if (lane == 0) {
-            mbar_arrive(sfull_bar(b));
-            mbar_arrive(saempty_bar(k));
-          }
-        }
-      }
-      __syncwarp();
     }
   } else {
     setmaxnreg_inc<kEpiRegs>();
     // ------------------------------------------------------------ epilogue
-    const int ew = warp - kEpiWarp0;      // 0..7
-    const int q = warp & 3;               // this warp may read TMEM lanes 32q .. 32q+31
-    const int half = ew >> 2;             // token columns half*128 .. half*128+127
-    const int tq = lane & 3, tr = lane >> 2;
-    const uint32_t taddr_lo = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
-    const uint32_t taddr_hi = tmem_base + (static_cast<uint32_t>(q * 32 + 16) << 16);
+    const int ew = warp - kEpiWarp0;  // 0..7
+    const int q = warp & 3;           // this warp may read TMEM lanes 32q .. 32q+31
+    const int half = ew >> 2;         // weight columns half*128 .. half*128+127
+    const int tl = static_cast<int>(rank) * 128 + q * 32 + lane;  // token within the tile
+    const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                           static_cast<uint32_t>(half * 128);
     __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out);
-
-    // TMEM reads of chunk c (32 token columns) of the buffer at column col0
-    auto tld = [&](uint32_t col0, int c, uint32_t (&lo)[16], uint32_t (&hi)[16]) {
-      tmem_ld16x256b_x4(taddr_lo + col0 + 32 * c, lo);
-      tmem_ld16x256b_x4(taddr_hi + col0 + 32 * c, hi);
-    };
 
     uint32_t u = 0;
     bool ok = true;
     for (int w = unit_id; w < total && ok; w += n_units) {
       const Item t = item_of(w, NT, mt_prefix, row_start, G);
-      int nc = t.n_eff - half * 128;
-      nc = nc < 0 ? 0 : (nc > 128 ? 128 : nc);
-      const int nch = nc / 32;
-      // acc[c][m][k]: chunk c (32 columns), repeat m (8 columns), row slot k
-      // (rows tr, tr+8, tr+16, tr+24 of this warp's lane quarter); .x/.y =
-      // columns half*128 + 32c + 8m + 2tq + {0, 1}
-      float2 acc[4][4][4];
+      // tokens of this warp's lane quarter that belong to the tile
+      const bool active = static_cast<int>(rank) * 128 + q * 32 < t.rows_tile;
+      const bool mine = tl < t.rows_tile && t.row0 + tl < p.R;
+      const int xoff = (static_cast<int>(t.row0) & 3) + tl;
+      // acc[c][i]: weight columns half*128 + 32c + 2i and + 2i + 1
+      float2 acc[4][16];
 #pragma unroll
       for (int c = 0; c < 4; ++c)
 #pragma unroll
-        for (int m = 0; m < 4; ++m)
-#pragma unroll
-          for (int k = 0; k < 4; ++k) acc[c][m][k] = make_float2(0.0f, 0.0f);
+        for (int i = 0; i < 16; ++i) acc[c][i] = make_float2(0.0f, 0.0f);
 
       for (int j = 0; j < nkb; ++j, ++u) {
-        const int pbi = static_cast<int>(u % kProdBufs);
+        const int k = static_cast<int>(u % kSlots);
         const int bsel = static_cast<int>(u & 1u);
         ok = __all_sync(0xFFFFFFFFu,
-                        mbar_wait(sfull_bar(pbi), (u / kProdBufs) & 1u, abort_flag, p.status) &&
+                        mbar_wait(safull_bar(k), (u / kSlots) & 1u, abort_flag, p.status) &&
                             mbar_wait(accf_bar(bsel), (u >> 1) & 1u, abort_flag, p.status));
         if (!ok) break;
         tc_fence_after();
-        const float* srow = prod + pbi * kProdFloats + ((MODE == F8_SWIGLU && (tr & 1)) ? kVar1 : 0) +
-                            half * 128 + 2 * tq;
-        const uint32_t col0 = static_cast<uint32_t>(bsel * kBufCols + half * 128);
-        // hand the TMEM buffer back as soon as its last chunk is in registers
+        // this token's scale products for the k-block: (gate, up) columns for
+        // SwiGLU, the column half's block for the down projection
+        const float* sl = reinterpret_cast<const float*>(ring + k * kSlotBytes);
+        const float sa = mine ? sl[xoff] : 0.0f;
+        float2 sc;
+        if (MODE == F8_SWIGLU) {
+          const float* sw = sl + kSlotW / 4 + ((2 * j) & 3);
+          sc = make_float2(sa * sw[0], sa * sw[1]);
+        } else {
+          const float wv = sl[kSlotW / 4 + half * kSwBox + (j & 3)];
+          sc = make_float2(sa * wv, sa * wv);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(saempty_bar(k));
         auto release = [&]() {
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive_remote(mapa_shared(acce_bar(bsel), 0));
         };
-        // acc += P * (activation scale x weight scale), one chunk
-        auto promote = [&](float2 (&a)[4][4], const uint32_t (&lo)[16], const uint32_t (&hi)[16],
-                           int c) {
+        auto promote = [&](float2 (&a)[16], const uint32_t (&r)[32]) {
 #pragma unroll
-          for (int m = 0; m < 4; ++m) {
-            const float2 sc2 = *reinterpret_cast<const float2*>(srow + 32 * c + 8 * m);
-            a[m][0] = __ffma2_rn(make_float2(__uint_as_float(lo[4 * m]), __uint_as_float(lo[4 * m + 1])),
-                                 sc2, a[m][0]);
-            a[m][1] = __ffma2_rn(make_float2(__uint_as_float(lo[4 * m + 2]),
-                                             __uint_as_float(lo[4 * m + 3])), sc2, a[m][1]);
-            a[m][2] = __ffma2_rn(make_float2(__uint_as_float(hi[4 * m]), __uint_as_float(hi[4 * m + 1])),
-                                 sc2, a[m][2]);
-            a[m][3] = __ffma2_rn(make_float2(__uint_as_float(hi[4 * m + 2]),
-                                             __uint_as_float(hi[4 * m + 3])), sc2, a[m][3]);
-          }
+          for (int i = 0; i < 16; ++i)
+            a[i] = __ffma2_rn(make_float2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1])),
+                              sc, a[i]);
         };
-        // two register buffers: chunk c+1 loads while chunk c is promoted
-        uint32_t lo0[16], hi0[16], lo1[16], hi1[16];
-        if (nch > 0) tld(col0, 0, lo0, hi0);
-        tmem_ld_wait();
-        reg_fence16(lo0);
-        reg_fence16(hi0);
-        if (nch > 1) tld(col0, 1, lo1, hi1);
-        else release();
-        if (nch > 0) promote(acc[0], lo0, hi0, 0);
-        if (nch > 1) {
-          tmem_ld_wait();
-          reg_fence16(lo1);
-          reg_fence16(hi1);
-          if (nch > 2) tld(col0, 2, lo0, hi0);
-          else release();
-          promote(acc[1], lo1, hi1, 1);
-        }
-        if (nch > 2) {
-          tmem_ld_wait();
-          reg_fence16(lo0);
-          reg_fence16(hi0);
-          if (nch > 3) tld(col0, 3, lo1, hi1);
-          else release();
-          promote(acc[2], lo0, hi0, 2);
-        }
-        if (nch > 3) {
-          tmem_ld_wait();
-          reg_fence16(lo1);
-          reg_fence16(hi1);
+        const uint32_t col0 = static_cast<uint32_t>(bsel * kBufCols);
+        if (!active) {
           release();
-          promote(acc[3], lo1, hi1, 3);
+        } else {
+          // two register buffers: chunk c+1 loads while chunk c is promoted
+          uint32_t r0[32], r1[32];
+          tmem_ld32(taddr + col0, r0);
+          tmem_ld_wait();
+          reg_fence32(r0);
+          tmem_ld32(taddr + col0 + 32, r1);
+          promote(acc[0], r0);
+          tmem_ld_wait();
+          reg_fence32(r1);
+          tmem_ld32(taddr + col0 + 64, r0);
+          promote(acc[1], r1);
+          tmem_ld_wait();
+          reg_fence32(r0);
+          tmem_ld32(taddr + col0 + 96, r1);
+          promote(acc[2], r0);
+          tmem_ld_wait();
+          reg_fence32(r1);
+          release();
+          promote(acc[3], r1);
         }
-        // the products of this k-block are no longer read
-        __syncwarp();
-        if (lane == 0) mbar_arrive(pempty_bar(pbi));
       }
       if (!ok) break;
 
-      // ---- store (tokens half*128 + 32c + 8m + 2tq + e, e = 0, 1)
-      const int t0 = half * 128;
-      int nvalid = t.rows_tile - t0;
-      if (nvalid > nc) nvalid = nc;
-      const long long over = t.row0 + t0 + nvalid - p.R;
-      if (over > 0) nvalid -= static_cast<int>(over);
-      __nv_bfloat16* obase = out + (t.row0 + t0) * p.ldo;
-      if (MODE == F8_SWIGLU) {
-        // rows tr + 8k are gate (tr even) or up (tr odd) of h column
-        // tr/2 + 4k; the partner row sits in lane ^ 4.  The gate lane makes
-        // and stores h for the even token of each pair, the up lane for the
-        // odd one.
-        const bool up = (tr & 1) != 0;
-        const int colb = t.n * 128 + static_cast<int>(rank) * 64 + q * 16 + (tr >> 1);
+      // ---- store this token's row segment
+      if (mine) {
+        __nv_bfloat16* orow = out + (t.row0 + tl) * p.ldo;
+        if (MODE == F8_SWIGLU) {
+          // columns 2i / 2i+1 of the tile are gate / up of h column
+          // n*128 + half*64 + (32c + 2i) / 2
+          uint4* dst = reinterpret_cast<uint4*>(orow + t.n * 128 + half * 64);
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          if (32 * c < nc) {
+          for (int c = 0; c < 4; ++c) {
+            uint32_t hw[8];
 #pragma unroll
-            for (int m = 0; m < 4; ++m) {
-              const int tok = 32 * c + 8 * m + 2 * tq + (up ? 1 : 0);
-#pragma unroll
-              for (int k = 0; k < 4; ++k) {
-                const float2 mine = acc[c][m][k];
-                const float ox = __shfl_xor_sync(0xFFFFFFFFu, mine.x, 4);
-                const float oy = __shfl_xor_sync(0xFFFFFFFFu, mine.y, 4);
-                const float g = up ? oy : mine.x;
-                const float v = up ? mine.y : ox;
-                const float h = g * __frcp_rn(1.0f + __expf(-g)) * v;
-                if (tok < nvalid)
-                  obase[static_cast<long long>(tok) * p.ldo + colb + 4 * k] = __float2bfloat16_rn(h);
-              }
+            for (int i = 0; i < 16; i += 2) {
+              const float g0 = acc[c][i].x, u0 = acc[c][i].y;
+              const float g1 = acc[c][i + 1].x, u1 = acc[c][i + 1].y;
+              const float h0 = g0 * __frcp_rn(1.0f + __expf(-g0)) * u0;
+              const float h1 = g1 * __frcp_rn(1.0f + __expf(-g1)) * u1;
+              const __nv_bfloat162 pr = __floats2bfloat162_rn(h0, h1);
+              hw[i / 2] = *reinterpret_cast<const uint32_t*>(&pr);
             }
+            dst[2 * c] = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+            dst[2 * c + 1] = make_uint4(hw[4], hw[5], hw[6], hw[7]);
           }
-        }
-      } else {
-        const int colb = t.n * 256 + static_cast<int>(rank) * 128 + q * 32 + tr;
+        } else {
+          const int col = t.n * 256 + half * 128;
+          if (col < p.N) {
+            uint4* dst = reinterpret_cast<uint4*>(orow + col);
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          if (32 * c < nc) {
+            for (int c = 0; c < 4; ++c) {
+              uint32_t v[16];
 #pragma unroll
-            for (int m = 0; m < 4; ++m) {
-              const int tok = 32 * c + 8 * m + 2 * tq;
-#pragma unroll
-              for (int k = 0; k < 4; ++k) {
-                const int col = colb + 8 * k;
-                if (col < p.N) {
-                  if (tok < nvalid)
-                    obase[static_cast<long long>(tok) * p.ldo + col] =
-                        __float2bfloat16_rn(acc[c][m][k].x);
-                  if (tok + 1 < nvalid)
-                    obase[static_cast<long long>(tok + 1) * p.ldo + col] =
-                        __float2bfloat16_rn(acc[c][m][k].y);
-                }
+              for (int i = 0; i < 16; ++i) {
+                const __nv_bfloat162 pr = __floats2bfloat162_rn(acc[c][i].x, acc[c][i].y);
+                v[i] = *reinterpret_cast<const uint32_t*>(&pr);
               }
+#pragma unroll
+              for (int e = 0; e < 4; ++e)
+                dst[4 * c + e] = make_uint4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
             }
           }
         }
@@ -526,14 +439,14 @@ bool make_map_u8(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer
   return gemm::make_map_sw128(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, ptr, inner, outer, 128);
 }
 
-// fp32 rows [outer, inner] (inner % 4 == 0), box = box_inner x 1, no swizzle.
+// fp32 rows [outer, inner] (inner % 4 == 0), box = box_inner x box_rows, no swizzle.
 bool make_map_f32_rows(CUtensorMap* m, const float* ptr, uint64_t inner, uint64_t outer,
-                       uint32_t box_inner) {
+                       uint32_t box_inner, uint32_t box_rows = 1) {
   auto fn = gemm::encode_fn();
   if (!fn) return false;
   cuuint64_t dims[2] = {inner, outer};
   cuuint64_t strides[1] = {inner * 4};
-  cuuint32_t box[2] = {box_inner, 1};
+  cuuint32_t box[2] = {box_inner, box_rows};
   cuuint32_t estr[2] = {1, 1};
   const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(ptr), dims,
                         strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -601,12 +514,17 @@ cudaError_t launch_grouped_swiglu_fp8(const uint8_t* a_q, const float* a_s, int 
       !make_map_f32_rows(&ta1, a_s, ld_as, kb1, kSaBox1) ||
       !make_map_f32_rows(&ta2, a_s, ld_as, kb1, kSaBox2) ||
       !make_map_f32_rows(&tsw13, w13_s, fp8_scale_pitch(2, d), static_cast<uint64_t>(G) * (I / 128),
-                         kSwBox) ||
+                         kSwBox, kSwRows) ||
       !make_map_f32_rows(&th1, h_s, ld_h, kb2, kSaBox1) ||
       !make_map_f32_rows(&th2, h_s, ld_h, kb2, kSaBox2) ||
       !make_map_f32_rows(&tsw2, w2_s, fp8_scale_pitch(1, I), static_cast<uint64_t>(G) * (d / 128),
-                         kSwBox))
+                         kSwBox, kSwRows))
     return cudaErrorInvalidValue;
+  // decode-sized groups (fewer than 64 rows on average): weights on M and the
+  // few tokens on N waste less than 256-token tiles
+  if (static_cast<long long>(R) < 64ll * G)
+    return launch_grouped_swiglu_fp8_small(a_q, ld_as, offsets, G, R, d, I, w13_q, w2_q, h, h_q, h_s,
+                                           y, status, ta1, ta2, tsw13, th1, th2, tsw2, s);
   Fp8Params p1{};
   p1.group_offsets = offsets;
   p1.G = G;

@@ -83,4 +83,15 @@ cudaError_t launch_grouped_swiglu_fp8(const uint8_t* a_q, const float* a_s, int 
                                       uint8_t* h_q, float* h_s, uint16_t* y, int32_t* status,
                                       cudaStream_t s);
 
+// Small-group orientation of the FP8 grouped experts (gemm_fp8_small.cu),
+// chosen by launch_grouped_swiglu_fp8; the scale maps are the caller's.
+cudaError_t launch_grouped_swiglu_fp8_small(const uint8_t* a_q, int ld_as, const int32_t* offsets,
+                                            int G, int R, int d, int I, const uint8_t* w13_q,
+                                            const uint8_t* w2_q, uint16_t* h, uint8_t* h_q,
+                                            float* h_s, uint16_t* y, int32_t* status,
+                                            const CUtensorMap& ta1, const CUtensorMap& ta2,
+                                            const CUtensorMap& tsw13, const CUtensorMap& th1,
+                                            const CUtensorMap& th2, const CUtensorMap& tsw2,
+                                            cudaStream_t s);
+
 }  // namespace moe

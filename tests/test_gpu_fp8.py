@@ -160,6 +160,11 @@ def oracle_experts(a, offsets, w1, w3, w2):
     ([513, 64, 200], 512, 384),               # three h column tiles, two down column tiles
     ([90, 170], 384, 256),                    # d % 256 == 128: half of the last down tile is empty
     ([400, 31], 1024, 256),
+    # decode-sized groups (fewer than 64 rows per group on average) take the
+    # small-group orientation of the kernel
+    ([3, 0, 7, 1, 30, 2], 256, 128),
+    ([40] * 8, 512, 256),
+    ([1, 63, 0, 0, 128], 384, 128),
 ])
 def test_grouped_swiglu_fp8_vs_oracle(sizes, d, I):
     G = len(sizes)
