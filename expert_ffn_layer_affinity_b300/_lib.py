@@ -32,6 +32,7 @@ _STATUS_NAMES = {
 
 # name -> (restype, argtypes); every pointer is passed as c_void_p
 P, I, F, Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+LL = ctypes.c_longlong
 SIGNATURES = {
     "moe_abi_version": (I, []),
     "moe_workspace_bytes": (Z, [I, I, I, I, I]),
@@ -49,6 +50,14 @@ SIGNATURES = {
     "moe_quantize_weights_fp8": (I, [P, P, I, I, I, P, P, P]),
     "moe_permute_fp8": (I, [P, P, I, I, I, I, P, P, P, I, P]),
     "moe_grouped_swiglu_fp8": (I, [P, P, I, P, I, I, I, I, P, P, P, P, P, P, P, P, P, P]),
+    "moe_combine_backward": (I, [P, P, P, P, I, I, I, P, P, P]),
+    "moe_swiglu_backward": (I, [P, P, P, I, I, P, P, P]),
+    "moe_grouped_gemm": (I, [P, P, I, I, I, I, P, P, P, P]),
+    "moe_grouped_gemm_wgrad": (I, [P, P, LL, P, I, I, I, P, P, P]),
+    "moe_transpose_grouped": (I, [P, P, I, I, I, P, LL, P, P]),
+    "moe_transpose_batched": (I, [P, I, I, I, P, LL, LL, P]),
+    "moe_router_backward": (I, [P, P, I, P, P, P, P, P, P, I, I, I, I, F, P, P, P, P, P]),
+    "moe_combine_dx": (I, [P, P, I, P, P, I, I, P, P]),
 }
 
 _lib = None
@@ -219,3 +228,60 @@ def moe_grouped_swiglu_fp8(a_q, a_s, ld_as, group_offsets, n_groups, R, d, I, w1
                                      _ptr(h), _ptr(h_q), _ptr(h_s), _ptr(y), _ptr(status_dev),
                                      _stream(stream))
     return _check("moe_grouped_swiglu_fp8", r) if check else r
+
+
+# ------------------------------------------------------------------ backward
+def moe_combine_backward(dy, y_perm, row_of, gate, T, K, d, dy_perm, dgate, stream=None, check=True):
+    r = lib().moe_combine_backward(_ptr(dy), _ptr(y_perm), _ptr(row_of), _ptr(gate), T, K, d,
+                                   _ptr(dy_perm), _ptr(dgate), _stream(stream))
+    return _check("moe_combine_backward", r) if check else r
+
+
+def moe_swiglu_backward(dh, a, c, R, I, dac, h, stream=None, check=True):
+    r = lib().moe_swiglu_backward(_ptr(dh), _ptr(a), _ptr(c), R, I, _ptr(dac), _ptr(h),
+                                  _stream(stream))
+    return _check("moe_swiglu_backward", r) if check else r
+
+
+def moe_grouped_gemm(a, group_offsets, n_groups, R, K, N, w, out, status_dev, stream=None,
+                     check=True):
+    r = lib().moe_grouped_gemm(_ptr(a), _ptr(group_offsets), n_groups, R, K, N, _ptr(w), _ptr(out),
+                               _ptr(status_dev), _stream(stream))
+    return _check("moe_grouped_gemm", r) if check else r
+
+
+def moe_grouped_gemm_wgrad(at, bt, ld, koff, n_groups, M, N, out, status_dev, stream=None,
+                           check=True):
+    r = lib().moe_grouped_gemm_wgrad(_ptr(at), _ptr(bt), ld, _ptr(koff), n_groups, M, N, _ptr(out),
+                                     _ptr(status_dev), _stream(stream))
+    return _check("moe_grouped_gemm_wgrad", r) if check else r
+
+
+def moe_transpose_grouped(src, group_offsets, n_groups, R, C, dst, ld, koff_out, stream=None,
+                          check=True):
+    r = lib().moe_transpose_grouped(_ptr(src), _ptr(group_offsets), n_groups, R, C, _ptr(dst), ld,
+                                    _ptr(koff_out), _stream(stream))
+    return _check("moe_transpose_grouped", r) if check else r
+
+
+def moe_transpose_batched(src, batches, rows, cols, dst, dst_ld, dst_batch_stride, stream=None,
+                          check=True):
+    r = lib().moe_transpose_batched(_ptr(src), batches, rows, cols, _ptr(dst), dst_ld,
+                                    dst_batch_stride, _stream(stream))
+    return _check("moe_transpose_batched", r) if check else r
+
+
+def moe_router_backward(dgate, topk_idx, ldk, affinity, w_r, x, row_of, tok_of, expert_offsets,
+                        T, d, E, K, route_scale, du, du_row, dx_router, dw_r, stream=None,
+                        check=True):
+    r = lib().moe_router_backward(_ptr(dgate), _ptr(topk_idx), ldk, _ptr(affinity), _ptr(w_r),
+                                  _ptr(x), _ptr(row_of), _ptr(tok_of), _ptr(expert_offsets), T, d,
+                                  E, K, float(route_scale), _ptr(du), _ptr(du_row), _ptr(dx_router),
+                                  _ptr(dw_r), _stream(stream))
+    return _check("moe_router_backward", r) if check else r
+
+
+def moe_combine_dx(dx_perm, row_of, K, dx_shared, dx_router, T, d, dx, stream=None, check=True):
+    r = lib().moe_combine_dx(_ptr(dx_perm), _ptr(row_of), K, _ptr(dx_shared), _ptr(dx_router), T, d,
+                             _ptr(dx), _stream(stream))
+    return _check("moe_combine_dx", r) if check else r

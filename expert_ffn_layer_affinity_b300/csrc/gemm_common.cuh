@@ -56,10 +56,12 @@ __device__ __forceinline__ int tile_n(int rows_left, int tok_tile) {
 
 // Writes a 32 (weight row = output column) x 32 (token) block, held one
 // output column per lane as 32 fp32 values along tokens, as 32 token rows of
-// 64 bytes (bf16).  `xp` is this warp's 32 x 80-byte staging area.
+// 64 bytes (bf16), or of its first cols_valid columns (a multiple of 8).
+// `xp` is this warp's 32 x 80-byte staging area.
 __device__ __forceinline__ void store_block_transposed(const uint32_t (&v)[32], uint8_t* xp,
                                                        int lane, __nv_bfloat16* out, long long row0,
-                                                       int rows_valid, int ldo, int col) {
+                                                       int rows_valid, int ldo, int col,
+                                                       int cols_valid = 32) {
   __nv_bfloat16* x = reinterpret_cast<__nv_bfloat16*>(xp);
 #pragma unroll
   for (int j = 0; j < 32; ++j) x[j * 40 + lane] = __float2bfloat16_rn(__uint_as_float(v[j]));
@@ -68,7 +70,8 @@ __device__ __forceinline__ void store_block_transposed(const uint32_t (&v)[32], 
     const uint4* src = reinterpret_cast<const uint4*>(xp + lane * 80);
     uint4* dst = reinterpret_cast<uint4*>(out + (row0 + lane) * ldo + col);
 #pragma unroll
-    for (int k = 0; k < 4; ++k) dst[k] = src[k];
+    for (int k = 0; k < 4; ++k)
+      if (8 * k < cols_valid) dst[k] = src[k];
   }
   __syncwarp();
 }

@@ -435,7 +435,8 @@ __global__ void __launch_bounds__(kThreads, 1)
               if (col_ok) store_block_transposed(v, xp, lane, out, row0 + c, valid, p.ldo, col);
             }
           } else if (col_ok) {
-            store_block_transposed(v, xp, lane, out, row0 + c, valid, p.ldo, col);
+            // a ragged last column block (N % 32 != 0) stores whole 8-column units
+            store_block_transposed(v, xp, lane, out, row0 + c, valid, p.ldo, col, p.N - col);
           }
         }
         if (!ok) break;
@@ -562,6 +563,30 @@ cudaError_t launch_grouped_swiglu(const uint16_t* a, const int32_t* offsets, int
   p2.ldo = d;
   const int mt2 = (R + C2::kTokTile - 1) / C2::kTokTile + G;
   return launch_gemm<MODE_DOWN>(tw2, tw2, th, p2, mt2 * ((d + 255) / 256), s);
+}
+
+cudaError_t launch_grouped_gemm_nt(const uint16_t* a, const int32_t* offsets, int G, int R, int K,
+                                   int N, const uint16_t* w, uint16_t* out, int32_t* status,
+                                   cudaStream_t s) {
+  if (R == 0 || G == 0) return cudaSuccess;
+  if (G > kMaxGroups) return cudaErrorInvalidValue;
+  using C2 = Cfg<MODE_DOWN>;
+  CUtensorMap tw, ta;
+  if (!make_map(&tw, w, K, static_cast<uint64_t>(G) * N, 128) || !make_map(&ta, a, K, R, 128))
+    return cudaErrorInvalidValue;
+  GemmParams p{};
+  p.group_offsets = offsets;
+  p.G = G;
+  p.N = N;
+  p.R = R;
+  p.num_kb = K / BK;
+  p.a_k_wrap_kb = K / BK;
+  p.w_rows_per_group = N;
+  p.out = out;
+  p.ldo = N;
+  p.status = status;
+  const int mt = (R + C2::kTokTile - 1) / C2::kTokTile + G;
+  return launch_gemm<MODE_DOWN>(tw, tw, ta, p, mt * ((N + 255) / 256), s);
 }
 
 cudaError_t launch_router_gemm(const uint16_t* x, const uint16_t* w_split, const float* offset,

@@ -94,4 +94,33 @@ cudaError_t launch_grouped_swiglu_fp8_small(const uint8_t* a_q, int ld_as, const
                                             const CUtensorMap& th2, const CUtensorMap& tsw2,
                                             cudaStream_t s);
 
+// ---- backward (backward.cu, gemm_wgrad.cu, gemm_tc.cu)
+cudaError_t launch_grouped_gemm_nt(const uint16_t* a, const int32_t* offsets, int G, int R, int K,
+                                   int N, const uint16_t* w, uint16_t* out, int32_t* status,
+                                   cudaStream_t s);
+cudaError_t launch_grouped_wgrad(const uint16_t* at, const uint16_t* bt, long long ld,
+                                 const int32_t* koff, int G, int M, int N, float* out,
+                                 int32_t* status, cudaStream_t s);
+cudaError_t launch_combine_backward(const uint16_t* dy, const uint16_t* y_perm,
+                                    const int32_t* row_of, const float* gate, int T, int K, int d,
+                                    uint16_t* dy_perm, float* dgate, cudaStream_t s);
+cudaError_t launch_swiglu_backward(const uint16_t* dh, const uint16_t* a, const uint16_t* c, int R,
+                                   int I, uint16_t* dac, uint16_t* h, cudaStream_t s);
+cudaError_t launch_router_backward(const float* dgate, const int32_t* idx, int ld_idx,
+                                   const float* affinity, const float* w_r, const uint16_t* x,
+                                   const int32_t* row_of, const int32_t* tok_of,
+                                   const int32_t* offsets, int T, int d, int E, int K, float scale,
+                                   float* du, float* du_row, float* dx_router, float* dw_r,
+                                   cudaStream_t s);
+cudaError_t launch_combine_dx(const uint16_t* dx_perm, const int32_t* row_of, int K,
+                              const uint16_t* dx_shared, const float* dx_router, int T, int d,
+                              uint16_t* dx, cudaStream_t s);
+cudaError_t launch_transpose_batched(const uint16_t* src, int batches, int rows, int cols,
+                                     uint16_t* dst, long long dst_ld, long long dst_batch_stride,
+                                     cudaStream_t s);
+cudaError_t launch_padded_offsets(const int32_t* off, int G, int32_t* poff, cudaStream_t s);
+cudaError_t launch_transpose_grouped(const uint16_t* src, const int32_t* off, const int32_t* poff,
+                                     int G, int R_bound, int C, long long ld, uint16_t* dst,
+                                     cudaStream_t s);
+
 }  // namespace moe

@@ -258,6 +258,122 @@ moe_status moe_grouped_swiglu_fp8(const void* a_q, const float* a_s, int ld_as,
       static_cast<uint16_t*>(y_bf16), status_dev, static_cast<cudaStream_t>(stream)));
 }
 
+// ------------------------------------------------------------------ backward
+moe_status moe_combine_backward(const void* dy_bf16, const void* y_perm_bf16,
+                                const int32_t* row_of, const float* gate, int T, int K, int d,
+                                void* dy_perm_bf16, float* dgate, moe_stream_t stream) {
+  if (T < 0 || K < 1 || K > 32 || d < 1) return MOE_ERR_INVALID_ARG;
+  if (T > 0 && (!dy_bf16 || !y_perm_bf16 || !row_of || !gate || !dy_perm_bf16 || !dgate))
+    return MOE_ERR_INVALID_ARG;
+  if (d % 8) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (T > 0 && (!aligned16(dy_bf16) || !aligned16(y_perm_bf16) || !aligned16(dy_perm_bf16)))
+    return MOE_ERR_UNSUPPORTED_SHAPE;
+  return cuda_status(launch_combine_backward(
+      static_cast<const uint16_t*>(dy_bf16), static_cast<const uint16_t*>(y_perm_bf16), row_of,
+      gate, T, K, d, static_cast<uint16_t*>(dy_perm_bf16), dgate, static_cast<cudaStream_t>(stream)));
+}
+
+moe_status moe_swiglu_backward(const void* dh_bf16, const void* a_bf16, const void* c_bf16, int R,
+                               int I, void* dac_bf16, void* h_bf16, moe_stream_t stream) {
+  if (R < 0 || I < 1) return MOE_ERR_INVALID_ARG;
+  if (R > 0 && (!dh_bf16 || !a_bf16 || !c_bf16 || !dac_bf16)) return MOE_ERR_INVALID_ARG;
+  if (I % 2) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (R > 0 && ((reinterpret_cast<uintptr_t>(dh_bf16) | reinterpret_cast<uintptr_t>(a_bf16) |
+                 reinterpret_cast<uintptr_t>(c_bf16) | reinterpret_cast<uintptr_t>(dac_bf16) |
+                 reinterpret_cast<uintptr_t>(h_bf16)) & 3u))
+    return MOE_ERR_UNSUPPORTED_SHAPE;
+  return cuda_status(launch_swiglu_backward(
+      static_cast<const uint16_t*>(dh_bf16), static_cast<const uint16_t*>(a_bf16),
+      static_cast<const uint16_t*>(c_bf16), R, I, static_cast<uint16_t*>(dac_bf16),
+      static_cast<uint16_t*>(h_bf16), static_cast<cudaStream_t>(stream)));
+}
+
+moe_status moe_grouped_gemm(const void* a_bf16, const int32_t* group_offsets, int n_groups, int R,
+                            int K, int N, const void* w_bf16, void* out_bf16, int32_t* status_dev,
+                            moe_stream_t stream) {
+  if (R < 0 || n_groups < 1 || K < 1 || N < 1) return MOE_ERR_INVALID_ARG;
+  if (R > 0 && (!a_bf16 || !group_offsets || !w_bf16 || !out_bf16)) return MOE_ERR_INVALID_ARG;
+  if (K % 64 || N % 8 || n_groups > 512) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (R > 0 && (!aligned16(a_bf16) || !aligned16(w_bf16) || !aligned16(out_bf16)))
+    return MOE_ERR_UNSUPPORTED_SHAPE;
+  return cuda_status(launch_grouped_gemm_nt(
+      static_cast<const uint16_t*>(a_bf16), group_offsets, n_groups, R, K, N,
+      static_cast<const uint16_t*>(w_bf16), static_cast<uint16_t*>(out_bf16), status_dev,
+      static_cast<cudaStream_t>(stream)));
+}
+
+moe_status moe_grouped_gemm_wgrad(const void* at_bf16, const void* bt_bf16, long long ld,
+                                  const int32_t* koff, int n_groups, int M, int N, float* out,
+                                  int32_t* status_dev, moe_stream_t stream) {
+  if (n_groups < 1 || M < 1 || N < 1 || ld < 64) return MOE_ERR_INVALID_ARG;
+  if (!at_bf16 || !bt_bf16 || !koff || !out) return MOE_ERR_INVALID_ARG;
+  if (ld % 64 || M % 8 || N % 8) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned16(at_bf16) || !aligned16(bt_bf16) || !aligned16(out)) return MOE_ERR_UNSUPPORTED_SHAPE;
+  return cuda_status(launch_grouped_wgrad(static_cast<const uint16_t*>(at_bf16),
+                                          static_cast<const uint16_t*>(bt_bf16), ld, koff, n_groups,
+                                          M, N, out, status_dev, static_cast<cudaStream_t>(stream)));
+}
+
+moe_status moe_transpose_grouped(const void* src_bf16, const int32_t* group_offsets, int n_groups,
+                                 int R, int C, void* dst_bf16, long long ld, int32_t* koff_out,
+                                 moe_stream_t stream) {
+  if (R < 0 || n_groups < 1 || C < 1 || ld < 0) return MOE_ERR_INVALID_ARG;
+  if (!src_bf16 || !group_offsets || !dst_bf16 || !koff_out) return MOE_ERR_INVALID_ARG;
+  if (ld % 64 || n_groups > 65535) return MOE_ERR_UNSUPPORTED_SHAPE;
+  // the padded groups end at most at round_up(R, 64) + 64 (G - 1)
+  if (ld < (static_cast<long long>(R) + 63) / 64 * 64 + 64ll * (n_groups - 1))
+    return MOE_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = launch_padded_offsets(group_offsets, n_groups, koff_out, st);
+  if (e != cudaSuccess) return cuda_status(e);
+  return cuda_status(launch_transpose_grouped(static_cast<const uint16_t*>(src_bf16),
+                                              group_offsets, koff_out, n_groups, R, C, ld,
+                                              static_cast<uint16_t*>(dst_bf16), st));
+}
+
+moe_status moe_transpose_batched(const void* src_bf16, int batches, int rows, int cols,
+                                 void* dst_bf16, long long dst_ld, long long dst_batch_stride,
+                                 moe_stream_t stream) {
+  if (batches < 0 || rows < 0 || cols < 0 || dst_ld < rows) return MOE_ERR_INVALID_ARG;
+  if (batches > 0 && rows > 0 && cols > 0 && (!src_bf16 || !dst_bf16)) return MOE_ERR_INVALID_ARG;
+  if (batches > 65535) return MOE_ERR_UNSUPPORTED_SHAPE;
+  return cuda_status(launch_transpose_batched(static_cast<const uint16_t*>(src_bf16), batches,
+                                              rows, cols, static_cast<uint16_t*>(dst_bf16), dst_ld,
+                                              dst_batch_stride, static_cast<cudaStream_t>(stream)));
+}
+
+moe_status moe_router_backward(const float* dgate, const int32_t* topk_idx, int ldk,
+                               const float* affinity, const float* w_r, const void* x_bf16,
+                               const int32_t* row_of, const int32_t* tok_of,
+                               const int32_t* expert_offsets, int T, int d, int E, int K,
+                               float route_scale, float* du, float* du_row, float* dx_router,
+                               float* dw_r, moe_stream_t stream) {
+  if (T < 0 || d < 1 || E < 1 || K < 1 || K > 32 || K > E || ldk < K) return MOE_ERR_INVALID_ARG;
+  if (!dw_r || (T > 0 && (!dgate || !topk_idx || !affinity || !w_r || !x_bf16 || !row_of ||
+                          !tok_of || !expert_offsets || !du || !du_row)))
+    return MOE_ERR_INVALID_ARG;
+  if (E > 65535) return MOE_ERR_UNSUPPORTED_SHAPE;
+  return cuda_status(launch_router_backward(
+      dgate, topk_idx, ldk, affinity, w_r, static_cast<const uint16_t*>(x_bf16), row_of, tok_of,
+      expert_offsets, T, d, E, K, route_scale, du, du_row, dx_router, dw_r,
+      static_cast<cudaStream_t>(stream)));
+}
+
+moe_status moe_combine_dx(const void* dx_perm_bf16, const int32_t* row_of, int K,
+                          const void* dx_shared_bf16, const float* dx_router, int T, int d,
+                          void* dx_bf16, moe_stream_t stream) {
+  if (T < 0 || K < 1 || d < 1) return MOE_ERR_INVALID_ARG;
+  if (T > 0 && (!dx_perm_bf16 || !row_of || !dx_bf16)) return MOE_ERR_INVALID_ARG;
+  if (d % 8) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (T > 0 && (!aligned16(dx_perm_bf16) || !aligned16(dx_bf16) ||
+                (dx_shared_bf16 && !aligned16(dx_shared_bf16)) || (dx_router && !aligned16(dx_router))))
+    return MOE_ERR_UNSUPPORTED_SHAPE;
+  return cuda_status(launch_combine_dx(static_cast<const uint16_t*>(dx_perm_bf16), row_of, K,
+                                       static_cast<const uint16_t*>(dx_shared_bf16), dx_router, T, d,
+                                       static_cast<uint16_t*>(dx_bf16),
+                                       static_cast<cudaStream_t>(stream)));
+}
+
 moe_status moe_replica_plan(const int32_t* load_host, int E, int n_redundant,
                             int32_t* slot_start_host, int32_t* slots_host,
                             int32_t* expert_of_slot_host) {

@@ -231,3 +231,13 @@ def make_groups(n_groups: int, total: int, seed: int = 0, empty_every: int = 0):
     sizes = torch.floor(w / w.sum() * total).to(torch.int64)
     sizes[int(torch.argmax(w))] += total - int(sizes.sum())
     return sizes
+
+
+def make_output_grad(cfg: LayerConfig, step: int = 0, device="cpu", seed: int | None = None,
+                     T: int | None = None) -> torch.Tensor:
+    """Upstream gradient dy bf16 [T, d] of a backward pass: N(0, 1), from a
+    seed of its own (seed + 2000003 + step)."""
+    seed = cfg.seed if seed is None else seed
+    T = cfg.T if T is None else T
+    g = _gen(seed + 2000003 + step, device)
+    return _normal((T, cfg.d), 1.0, g, device, torch.bfloat16)

@@ -280,6 +280,90 @@ moe_status moe_grouped_swiglu_fp8(const void* a_q, const float* a_s, int ld_as,
                                   const float* w2_s, void* h_bf16, void* h_q, float* h_s,
                                   void* y_bf16, int32_t* status_dev, moe_stream_t stream);
 
+/* ---------------------------------------------------------- backward pass
+ * Gradients of the layer output for a fixed choice of experts.  The bias only
+ * chooses experts and never enters a gate value ("Bias 仅用于路由",
+ * deepseekmodel1.org, "公式解密"; chenshi221 notes, "Auxiliary-loss-free
+ * 负载均衡"), so the router receives gradient through the gates, which depend
+ * on the raw affinities only, and the bias receives none:
+ *   g_k = scale s_k / S (S = sum of the K chosen s_j),
+ *   ds_k = scale (dg_k / S - sum_j dg_j s_j / S^2), du_k = ds_k s_k (1 - s_k).
+ * Expert FFN y = W2 (silu(a) c), a = W1 v, c = W3 v:
+ *   dh = W2^T dy, da = dh c silu'(a), dc = dh silu(a), dv = W1^T da + W3^T dc,
+ *   dW2 = dy h^T, dW1 = da v^T, dW3 = dc v^T.
+ * Reductions run in a fixed order (results are deterministic).  The weight
+ * gradients are fp32; the activation gradients bf16. */
+
+/* Combine backward: dy_perm[row_of[t,k]] = gate[t,k] dy[t] and
+ * dgate[t,k] = <dy[t], y_perm[row_of[t,k]]> (fp32).
+ *  dy, y_perm bf16 [T, d] / [T*K, d] (y_perm = the experts' outputs the forward
+ *  combined); row_of [T, K]; gate fp32 [T, K]; dy_perm bf16 [T*K, d] out;
+ *  dgate fp32 [T, K] out.  d % 8 == 0. */
+moe_status moe_combine_backward(const void* dy_bf16, const void* y_perm_bf16,
+                                const int32_t* row_of, const float* gate, int T, int K, int d,
+                                void* dy_perm_bf16, float* dgate, moe_stream_t stream);
+
+/* Elementwise SwiGLU backward per row: from dh, a = v.W1^T, c = v.W3^T
+ * (bf16 [R, I] each) write dac = [da | dc] (bf16 [R, 2I]) and the recomputed
+ * h = silu(a) c (bf16 [R, I]; NULL skips it).  I % 2 == 0. */
+moe_status moe_swiglu_backward(const void* dh_bf16, const void* a_bf16, const void* c_bf16, int R,
+                               int I, void* dac_bf16, void* h_bf16, moe_stream_t stream);
+
+/* Grouped bf16 GEMM on the tensor cores: out[r] = a[r] . w[g]^T for the rows r
+ * of group g (group_offsets [G+1] DEVICE).  a [R, K], w [G, N, K], out [R, N]
+ * bf16; K % 64 == 0, N % 8 == 0, 1 <= G <= 512.  Used for the recomputed a, c
+ * and, with transposed weights (moe_transpose_batched), dh = dy . W2 and
+ * dv = [da | dc] . [W1 ; W3]. */
+moe_status moe_grouped_gemm(const void* a_bf16, const int32_t* group_offsets, int n_groups, int R,
+                            int K, int N, const void* w_bf16, void* out_bf16, int32_t* status_dev,
+                            moe_stream_t stream);
+
+/* Grouped weight-gradient GEMM: out[g][m][n] = sum over the rows r of group g
+ * of A[r][m] B[r][n], fp32 [G, M, N], with the operands given TRANSPOSED:
+ * at bf16 [M, ld], bt bf16 [N, ld], group g owning columns koff[g] ..
+ * koff[g+1] (DEVICE [G+1], multiples of 64; rows beyond a group's tokens are
+ * zero), as written by moe_transpose_grouped.  ld % 64 == 0, M, N % 8 == 0.
+ * A group with no rows gets zeros. */
+moe_status moe_grouped_gemm_wgrad(const void* at_bf16, const void* bt_bf16, long long ld,
+                                  const int32_t* koff, int n_groups, int M, int N, float* out,
+                                  int32_t* status_dev, moe_stream_t stream);
+
+/* Transposes the row groups of src bf16 [R, C] (group_offsets [G+1] DEVICE)
+ * into columns of dst bf16 [C, ld]: group g's rows become columns koff[g] ..,
+ * zero-padded to a multiple of 64, koff written to koff_out [G+1] DEVICE.
+ * ld % 64 == 0 and ld >= round_up(R, 64) + 64 (G - 1), the most the padded
+ * groups can span. */
+moe_status moe_transpose_grouped(const void* src_bf16, const int32_t* group_offsets, int n_groups,
+                                 int R, int C, void* dst_bf16, long long ld, int32_t* koff_out,
+                                 moe_stream_t stream);
+
+/* Batched transpose: dst[b*dst_batch_stride + c*dst_ld + r] = src[b][r][c] for
+ * src bf16 [batches, rows, cols]; e.g. W2 [E, d, I] -> [E, I, d], and w1 / w3
+ * [E, I, d] -> the two halves of [E, d, 2I]. */
+moe_status moe_transpose_batched(const void* src_bf16, int batches, int rows, int cols,
+                                 void* dst_bf16, long long dst_ld, long long dst_batch_stride,
+                                 moe_stream_t stream);
+
+/* Router backward (chosen experts only): du fp32 [T, K] from dgate [T, K],
+ * the chosen experts topk_idx [T, ldk] (first K columns) and the forward's
+ * affinities fp32 [T, E]; dx_router fp32 [T, d] = du . w_r (or NULL);
+ * dw_r fp32 [E, d] = du^T x, summed per expert over its rows of the dispatch
+ * order (row_of [T, K], tok_of [T*K], expert_offsets [E+1] from moe_permute).
+ * du_row fp32 [T*K]: scratch.  x bf16 [T, d], w_r fp32 [E, d]. */
+moe_status moe_router_backward(const float* dgate, const int32_t* topk_idx, int ldk,
+                               const float* affinity, const float* w_r, const void* x_bf16,
+                               const int32_t* row_of, const int32_t* tok_of,
+                               const int32_t* expert_offsets, int T, int d, int E, int K,
+                               float route_scale, float* du, float* du_row, float* dx_router,
+                               float* dw_r, moe_stream_t stream);
+
+/* Input gradient: dx[t] = bf16( dx_shared[t] + dx_router[t] + sum_k
+ * dx_perm[row_of[t,k]] ) with fp32 sums in rank order.  dx_perm bf16 [T*K, d];
+ * dx_shared bf16 [T, d] or NULL; dx_router fp32 [T, d] or NULL; dx bf16 [T, d]. */
+moe_status moe_combine_dx(const void* dx_perm_bf16, const int32_t* row_of, int K,
+                          const void* dx_shared_bf16, const float* dx_router, int T, int d,
+                          void* dx_bf16, moe_stream_t stream);
+
 /* Step 5, bias feedback after the step:
  *   bias[e] = bias[e] - gamma  if E*load[e] > T*K   (overloaded)
  *   bias[e] = bias[e] + gamma  if E*load[e] < T*K   (underloaded)

@@ -121,3 +121,35 @@ def test_fp8_calls_reject_bad_arguments():
     # rows of activation scales must be whole 16-byte units (ld_as % 4 == 0)
     assert moe.moe_grouped_swiglu_fp8(FAKE, FAKE, 66, FAKE, 4, 64, 256, 128, FAKE, FAKE, FAKE,
                                       FAKE, FAKE, FAKE, FAKE, FAKE, None, **args) == E_SHAPE
+
+
+def test_backward_calls_reject_bad_arguments():
+    E_SHAPE, E_ARG = moe.MOE_ERR_UNSUPPORTED_SHAPE, moe.MOE_ERR_INVALID_ARG
+    args = dict(stream=0, check=False)
+    # d % 8, null input
+    assert moe.moe_combine_backward(FAKE, FAKE, FAKE, FAKE, 4, 2, 12, FAKE, FAKE, **args) == E_SHAPE
+    assert moe.moe_combine_backward(None, FAKE, FAKE, FAKE, 4, 2, 16, FAKE, FAKE, **args) == E_ARG
+    # odd I; null output (h may be null)
+    assert moe.moe_swiglu_backward(FAKE, FAKE, FAKE, 4, 7, FAKE, None, **args) == E_SHAPE
+    assert moe.moe_swiglu_backward(FAKE, FAKE, FAKE, 4, 8, None, None, **args) == E_ARG
+    # NT GEMM: K % 64, N % 8, too many groups
+    assert moe.moe_grouped_gemm(FAKE, FAKE, 2, 8, 96, 64, FAKE, FAKE, None, **args) == E_SHAPE
+    assert moe.moe_grouped_gemm(FAKE, FAKE, 2, 8, 128, 60, FAKE, FAKE, None, **args) == E_SHAPE
+    assert moe.moe_grouped_gemm(FAKE, FAKE, 513, 8, 128, 64, FAKE, FAKE, None, **args) == E_SHAPE
+    # wgrad: ld % 64, M % 8, null operand
+    assert moe.moe_grouped_gemm_wgrad(FAKE, FAKE, 96, FAKE, 2, 64, 64, FAKE, None, **args) == E_SHAPE
+    assert moe.moe_grouped_gemm_wgrad(FAKE, FAKE, 128, FAKE, 2, 60, 64, FAKE, None,
+                                      **args) == E_SHAPE
+    assert moe.moe_grouped_gemm_wgrad(None, FAKE, 128, FAKE, 2, 64, 64, FAKE, None, **args) == E_ARG
+    # grouped transpose: ld too small for the padded groups (R=100, G=3 -> 256)
+    assert moe.moe_transpose_grouped(FAKE, FAKE, 3, 100, 8, FAKE, 192, FAKE, **args) == E_ARG
+    assert moe.moe_transpose_grouped(FAKE, FAKE, 3, 100, 8, FAKE, 200, FAKE, **args) == E_SHAPE
+    # batched transpose: destination rows shorter than the source's
+    assert moe.moe_transpose_batched(FAKE, 2, 70, 33, FAKE, 64, 4096, **args) == E_ARG
+    # router backward: K > E, ldk < K
+    assert moe.moe_router_backward(FAKE, FAKE, 4, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 4, 16, 2, 4,
+                                   1.0, FAKE, FAKE, None, FAKE, **args) == E_ARG
+    assert moe.moe_router_backward(FAKE, FAKE, 1, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 4, 16, 8, 2,
+                                   1.0, FAKE, FAKE, None, FAKE, **args) == E_ARG
+    # combine_dx: d % 8
+    assert moe.moe_combine_dx(FAKE, FAKE, 2, None, None, 4, 12, FAKE, **args) == E_SHAPE

@@ -1,0 +1,340 @@
+"""Backward pass of the layer on the GPU against the fp64 backward oracle:
+each kernel on synthetic inputs, then whole passes on the tiny and mid
+workloads.
+
+Tolerances.  Weight gradients are fp32 sums of bf16 products (fp32 rounding
+only); activation gradients are bf16 and pass through at most six bf16
+roundings in sequence (g dy, dh, a, c, [da | dc], dv), unit roundoff 2^-9
+each, so a relative L2 error below 1e-2 against the fp64 oracle leaves a
+wide margin while a dropped term or a wrong index fails it by far."""
+import numpy as np
+import pytest
+import torch
+
+import expert_ffn_layer_affinity_b300 as moe
+from expert_ffn_layer_affinity_b300 import synth
+from expert_ffn_layer_affinity_b300.layer import MoELayer
+from oracle import moe_bwd_ref as B
+from oracle import moe_ref as ref
+from _util import HostExperts, bf16_to_np64, sync_status
+
+pytestmark = pytest.mark.gpu
+
+
+def _bf16(shape, seed, std=1.0):
+    g = torch.Generator().manual_seed(seed)
+    return (torch.randn(*shape, generator=g) * std).to(torch.bfloat16)
+
+
+def _offsets(sizes):
+    return np.concatenate([[0], np.cumsum(sizes)]).astype(np.int32)
+
+
+def _close(got, want, rel, abs_scale):
+    err = np.abs(got - want)
+    bound = rel * np.abs(want) + abs_scale
+    bad = err > bound
+    assert not bad.any(), (np.argwhere(bad)[:5], got[bad][:5], want[bad][:5])
+
+
+# ------------------------------------------------------------------ kernels
+@pytest.mark.parametrize("sizes,K,N", [
+    ([3, 0, 130, 64, 1, 257], 256, 136),
+    ([300, 290, 0, 511, 17, 256, 700, 2], 2048, 1408),
+    ([1], 64, 8),
+])
+def test_grouped_gemm_nt(sizes, K, N):
+    G, R = len(sizes), sum(sizes)
+    off = _offsets(sizes)
+    a = _bf16((R, K), 1)
+    w = _bf16((G, N, K), 2, 0.05)
+    out = torch.full((R, N), float("nan"), dtype=torch.bfloat16, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    moe.moe_grouped_gemm(a.cuda(), torch.from_numpy(off).cuda(), G, R, K, N, w.cuda(), out, st)
+    assert sync_status(st) == 0
+    a64, w64, got = bf16_to_np64(a), bf16_to_np64(w), bf16_to_np64(out)
+    want = np.concatenate([a64[off[g]:off[g + 1]] @ w64[g].T for g in range(G)])
+    rms = np.sqrt(np.mean(want ** 2))
+    _close(got, want, 2.0 ** -8, 1e-4 * rms)
+
+
+def _host_transposed(M, sizes, seed, std=1.0):
+    """A [R, M] bf16 and its grouped transpose [M, ld] with 64-padded groups."""
+    R = sum(sizes)
+    a = _bf16((R, M), seed, std)
+    poff = np.concatenate([[0], np.cumsum([(s + 63) // 64 * 64 for s in sizes])]).astype(np.int32)
+    ld = max(64, int(poff[-1]))
+    at = torch.zeros(M, ld, dtype=torch.bfloat16)
+    off = _offsets(sizes)
+    for g in range(len(sizes)):
+        at[:, poff[g]:poff[g] + sizes[g]] = a[off[g]:off[g + 1]].T
+    return a, at, poff, ld
+
+
+@pytest.mark.parametrize("sizes,M,N", [
+    ([0, 1, 63, 64, 65, 200], 200, 136),
+    ([310, 0, 290, 511, 129], 2048, 1408),
+    ([4096], 256, 512),
+])
+def test_grouped_wgrad(sizes, M, N):
+    G = len(sizes)
+    a, at, poff, ld = _host_transposed(M, sizes, 3)
+    b, bt, _, _ = _host_transposed(N, sizes, 4)
+    out = torch.full((G, M, N), float("nan"), dtype=torch.float32, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    moe.moe_grouped_gemm_wgrad(at.cuda(), bt.cuda(), ld, torch.from_numpy(poff).cuda(), G, M, N,
+                               out, st)
+    assert sync_status(st) == 0
+    got = out.cpu().numpy().astype(np.float64)
+    a64, b64 = bf16_to_np64(a), bf16_to_np64(b)
+    off = _offsets(sizes)
+    for g in range(G):
+        A, Bm = a64[off[g]:off[g + 1]], b64[off[g]:off[g + 1]]
+        want = A.T @ Bm
+        if sizes[g] == 0:
+            assert np.all(got[g] == 0.0)
+            continue
+        _close(got[g], want, 0.0, 4e-6 * (np.abs(A).T @ np.abs(Bm)) + 1e-30)
+
+
+def test_transposes_exact():
+    sizes = [5, 0, 64, 65, 1]
+    R, C = sum(sizes), 40
+    src = _bf16((R, C), 5)
+    off = _offsets(sizes)
+    ld = (R + 63) // 64 * 64 + 64 * (len(sizes) - 1)
+    dst = torch.full((C, ld), 7.0, dtype=torch.bfloat16, device="cuda")
+    koff = torch.zeros(len(sizes) + 1, dtype=torch.int32, device="cuda")
+    moe.moe_transpose_grouped(src.cuda(), torch.from_numpy(off).cuda(), len(sizes), R, C, dst, ld,
+                              koff)
+    torch.cuda.synchronize()
+    _, want, poff, _ = _host_transposed(C, sizes, 5)
+    np.testing.assert_array_equal(koff.cpu().numpy(), poff)
+    got = dst.cpu()[:, :poff[-1]]
+    assert torch.equal(got.view(torch.int16), want[:, :poff[-1]].view(torch.int16))
+    # batched: [3, 70, 33] -> rows of stride 80, batch stride 70*80+8
+    w = _bf16((3, 70, 33), 6)
+    dst = torch.zeros(3 * (33 * 80) + 16, dtype=torch.bfloat16, device="cuda")
+    moe.moe_transpose_batched(w.cuda(), 3, 70, 33, dst, 80, 33 * 80)
+    torch.cuda.synchronize()
+    got = dst.cpu()[:3 * 33 * 80].view(3, 33, 80)[:, :, :70]
+    assert torch.equal(got.view(torch.int16), w.transpose(1, 2).contiguous().view(torch.int16))
+
+
+def _routing(T, K, E, seed):
+    rng = np.random.default_rng(seed)
+    idx = np.stack([rng.permutation(E)[:K] for _ in range(T)]).astype(np.int32)
+    off, row_of, tok_of = ref.permute(idx, E)
+    return idx, off.astype(np.int32), row_of.astype(np.int32), tok_of.astype(np.int32)
+
+
+def test_combine_backward_and_swiglu_backward():
+    T, K, E, d, I = 300, 3, 8, 136, 72
+    idx, off, row_of, tok_of = _routing(T, K, E, 7)
+    dy, y_perm = _bf16((T, d), 8), _bf16((T * K, d), 9)
+    gate = torch.rand(T, K, generator=torch.Generator().manual_seed(10)) * 2.5
+    dy_perm = torch.empty(T * K, d, dtype=torch.bfloat16, device="cuda")
+    dgate = torch.empty(T, K, dtype=torch.float32, device="cuda")
+    moe.moe_combine_backward(dy.cuda(), y_perm.cuda(), torch.from_numpy(row_of).cuda(),
+                             gate.cuda(), T, K, d, dy_perm, dgate)
+    torch.cuda.synchronize()
+    dy64, y64, g64 = bf16_to_np64(dy), bf16_to_np64(y_perm), gate.numpy().astype(np.float64)
+    want_perm = np.zeros((T * K, d))
+    want_perm[row_of.reshape(-1)] = (g64[:, :, None] * dy64[:, None, :]).reshape(T * K, d)
+    _close(bf16_to_np64(dy_perm), want_perm, 2.0 ** -8, 0.0)
+    ysel = y64[row_of]                                   # [T, K, d]
+    want_dg = np.einsum("td,tkd->tk", dy64, ysel)
+    _close(dgate.cpu().numpy().astype(np.float64), want_dg, 0.0,
+           1e-5 * np.einsum("td,tkd->tk", np.abs(dy64), np.abs(ysel)))
+    # SwiGLU backward
+    R = 500
+    dh, a, c = _bf16((R, I), 11), _bf16((R, I), 12, 3.0), _bf16((R, I), 13)
+    dac = torch.empty(R, 2 * I, dtype=torch.bfloat16, device="cuda")
+    h = torch.empty(R, I, dtype=torch.bfloat16, device="cuda")
+    moe.moe_swiglu_backward(dh.cuda(), a.cuda(), c.cuda(), R, I, dac, h)
+    torch.cuda.synchronize()
+    dh64, a64, c64 = bf16_to_np64(dh), bf16_to_np64(a), bf16_to_np64(c)
+    da = dh64 * c64 * B.silu_deriv64(a64)
+    dc = dh64 * ref.silu64(a64)
+    got = bf16_to_np64(dac)
+    scale = 1e-6 * np.abs(dh64 * c64).max()
+    _close(got[:, :I], da, 2.0 ** -7, scale)
+    _close(got[:, I:], dc, 2.0 ** -7, scale)
+    _close(bf16_to_np64(h), ref.silu64(a64) * c64, 2.0 ** -7, 1e-6 * np.abs(a64 * c64).max())
+
+
+@pytest.mark.parametrize("T,K,E,d,scale", [(400, 4, 16, 200, 2.5), (1, 8, 256, 64, 1.0),
+                                           (257, 1, 8, 16, 1.0)])
+def test_router_backward(T, K, E, d, scale):
+    idx, off, row_of, tok_of = _routing(T, K, E, 20 + T)
+    rng = np.random.default_rng(21)
+    aff = rng.uniform(0.05, 0.95, (T, E)).astype(np.float32)
+    dgate = rng.standard_normal((T, K)).astype(np.float32)
+    w_r = (rng.standard_normal((E, d)) * 0.1).astype(np.float32)
+    x = _bf16((T, d), 22)
+    dev = "cuda"
+    du = torch.empty(T, K, dtype=torch.float32, device=dev)
+    du_row = torch.empty(T * K, dtype=torch.float32, device=dev)
+    dx_r = torch.empty(T, d, dtype=torch.float32, device=dev)
+    dw_r = torch.full((E, d), float("nan"), dtype=torch.float32, device=dev)
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+    moe.moe_router_backward(t(dgate), t(idx), K, t(aff), t(w_r), x.to(dev), t(row_of), t(tok_of),
+                            t(off), T, d, E, K, scale, du, du_row, dx_r, dw_r)
+    torch.cuda.synchronize()
+    s_sel = np.take_along_axis(aff.astype(np.float64), idx, axis=1)
+    ds = B.gate_bwd64(s_sel, dgate.astype(np.float64), scale)
+    want_du = ds * s_sel * (1.0 - s_sel)
+    mag = scale * np.abs(dgate).max() / s_sel.sum(1, keepdims=True)
+    _close(du.cpu().numpy().astype(np.float64), want_du, 0.0, 1e-5 * mag)
+    du_full = np.zeros((T, E))
+    np.put_along_axis(du_full, idx, want_du, axis=1)
+    # the error bound of each du entry (s (1 - s) <= 1/4) carried through the sums
+    du_abs = np.zeros((T, E))
+    np.put_along_axis(du_abs, idx, np.abs(want_du) + 0.25 * mag, axis=1)
+    w64, x64 = w_r.astype(np.float64), bf16_to_np64(x)
+    _close(dx_r.cpu().numpy().astype(np.float64), du_full @ w64, 0.0,
+           1e-5 * (du_abs @ np.abs(w64)) + 1e-30)
+    _close(dw_r.cpu().numpy().astype(np.float64), du_full.T @ x64, 0.0,
+           1e-5 * (du_abs.T @ np.abs(x64)) + 1e-30)
+    if K == 1:   # one chosen expert: its gate is the constant route scale
+        assert not du.abs().max().item() and not dw_r.abs().max().item()
+
+
+def test_combine_dx():
+    T, K, E, d = 333, 3, 8, 72
+    idx, off, row_of, tok_of = _routing(T, K, E, 30)
+    dxp, dxs = _bf16((T * K, d), 31), _bf16((T, d), 32)
+    dxr = torch.randn(T, d, generator=torch.Generator().manual_seed(33))
+    out = torch.empty(T, d, dtype=torch.bfloat16, device="cuda")
+    moe.moe_combine_dx(dxp.cuda(), torch.from_numpy(row_of).cuda(), K, dxs.cuda(), dxr.cuda(), T, d,
+                       out)
+    torch.cuda.synchronize()
+    want = bf16_to_np64(dxs) + dxr.numpy().astype(np.float64) + bf16_to_np64(dxp)[row_of].sum(1)
+    _close(bf16_to_np64(out), want, 2.0 ** -8, 1e-6)
+    moe.moe_combine_dx(dxp.cuda(), torch.from_numpy(row_of).cuda(), K, None, None, T, d, out)
+    torch.cuda.synchronize()
+    _close(bf16_to_np64(out), bf16_to_np64(dxp)[row_of].sum(1), 2.0 ** -8, 1e-6)
+
+
+# -------------------------------------------------------------------- layer
+def _layer_case(cfg, p, T=None):
+    """Forward + backward on the GPU; the oracle's own routing and gates.
+    Tokens whose choice is a near tie for the oracle get dy = 0 on both
+    sides, so they contribute nothing to any gradient."""
+    T = cfg.T if T is None else T
+    x = synth.make_tokens(cfg, 0, "cpu", T=T)
+    dy = synth.make_output_grad(cfg, 0, "cpu", T=T)
+    x64 = bf16_to_np64(x)
+    off = p["logit_offset"].numpy() if p["logit_offset"] is not None else None
+    s64 = ref.router_affinity64(x64, p["w_r"].numpy(), off)
+    b = p["bias"].numpy()
+    idx64, gate64 = ref.select_experts(s64, b.astype(np.float64), cfg.K, cfg.n_groups,
+                                       cfg.topk_groups, cfg.route_scale, precision="fp64")
+    kth, grp = ref.near_tie_tokens(s64, b, cfg.K, cfg.n_groups, cfg.topk_groups)
+    tie = kth | grp
+    dy[torch.from_numpy(tie)] = 0
+    layer = MoELayer(cfg, p, max_T=T, keep_affinity=True)
+    layer.forward(x.cuda())
+    g = layer.backward(x.cuda(), dy.cuda())
+    torch.cuda.synchronize()
+    assert layer.device_status() == 0
+    gidx = layer.idx[:T, :cfg.K].cpu().numpy()
+    mism = np.any(np.sort(gidx, 1) != np.sort(idx64, 1), axis=1)
+    assert not np.any(mism & ~tie)
+    return dict(x64=x64, dy64=bf16_to_np64(dy), off=off, idx64=idx64, gate64=gate64, tie=tie,
+                gidx=gidx, g={k: v.cpu() for k, v in g.items()})
+
+
+def _by_gpu_slot(want_tk, idx64, gidx, E):
+    """The oracle's per-(token, slot) values, moved to the GPU's slot order
+    (the same experts in each token's row, possibly listed differently)."""
+    full = np.zeros((want_tk.shape[0], E))
+    np.put_along_axis(full, idx64, want_tk, axis=1)
+    return np.take_along_axis(full, gidx, axis=1)
+
+
+def _np(t):
+    return bf16_to_np64(t) if t.dtype == torch.bfloat16 else t.numpy().astype(np.float64)
+
+
+def test_layer_backward_tiny_all_gradients():
+    cfg = synth.CONFIGS["tiny"]
+    p = synth.make_params(cfg, "cpu")
+    c = _layer_case(cfg, p)
+    host = HostExperts(p)
+    want = B.moe_layer_bwd64(c["x64"], p["w_r"].numpy(), c["off"], c["idx64"], cfg.route_scale,
+                             host, host.shared(), cfg.n_shared, c["dy64"])
+    g = c["g"]
+    assert ref.rel_l2(_np(g["dx"]), want["dx"]) < 1e-2
+    dg_want = _by_gpu_slot(want["dgate"], c["idx64"], c["gidx"], cfg.E)
+    assert ref.rel_l2(_np(g["dgate"]), dg_want) < 1e-2
+    du_want = np.take_along_axis(want["du"], c["gidx"], axis=1)
+    assert ref.rel_l2(_np(g["du"]), du_want) < 1e-2
+    assert ref.rel_l2(_np(g["dw_r"]), want["dw_r"]) < 1e-2
+    I = cfg.I
+    dw13, dw2 = _np(g["dw13"]), _np(g["dw2"])
+    for e in range(cfg.E):
+        if e in want["experts"]:
+            w1, w3, w2 = want["experts"][e]
+        else:
+            w1 = w3 = np.zeros((I, cfg.d))
+            w2 = np.zeros((cfg.d, I))
+        got = np.concatenate([dw13[e].ravel(), dw2[e].ravel()])
+        ref_e = np.concatenate([w1.ravel(), w3.ravel(), w2.ravel()])
+        if not np.any(ref_e):
+            assert not np.any(got)
+        else:
+            assert ref.rel_l2(got, ref_e) < 1e-2, e
+    s1, s3, s2 = want["shared"]
+    nI = cfg.n_shared * I
+    assert ref.rel_l2(_np(g["dws13"])[:nI], s1) < 1e-2
+    assert ref.rel_l2(_np(g["dws13"])[nI:], s3) < 1e-2
+    assert ref.rel_l2(_np(g["dws2"]), s2) < 1e-2
+
+
+def test_layer_backward_deterministic():
+    cfg = synth.CONFIGS["tiny"]
+    p = synth.make_params(cfg, "cpu")
+    x = synth.make_tokens(cfg, 0, "cuda")
+    dy = synth.make_output_grad(cfg, 0, "cuda")
+    layer = MoELayer(cfg, p, keep_affinity=True)
+    runs = []
+    for _ in range(2):
+        layer.forward(x)
+        g = layer.backward(x, dy)
+        runs.append({k: v.clone() for k, v in g.items()})
+    torch.cuda.synchronize()
+    for k in runs[0]:
+        assert torch.equal(runs[0][k].view(torch.int16) if runs[0][k].dtype == torch.bfloat16
+                           else runs[0][k].view(torch.int32),
+                           runs[1][k].view(torch.int16) if runs[1][k].dtype == torch.bfloat16
+                           else runs[1][k].view(torch.int32)), k
+
+
+def test_layer_backward_mid_sampled():
+    """mid workload: dx, dgate and du on 256 sampled tokens (each token's
+    gradients depend on that token alone for a fixed choice of experts), the
+    weight gradients of three experts over all their tokens."""
+    cfg = synth.CONFIGS["mid"]
+    p = synth.make_params(cfg, "cpu")
+    c = _layer_case(cfg, p)
+    host = HostExperts(p)
+    tok = np.random.default_rng(1).choice(cfg.T, 256, replace=False)
+    tok = tok[~c["tie"][tok]]
+    want = B.moe_layer_bwd64(c["x64"][tok], p["w_r"].numpy(), c["off"], c["idx64"][tok],
+                             cfg.route_scale, host, host.shared(), cfg.n_shared, c["dy64"][tok])
+    g = c["g"]
+    assert ref.rel_l2(_np(g["dx"])[tok], want["dx"]) < 1e-2
+    gidx = c["gidx"][tok]
+    assert ref.rel_l2(_np(g["dgate"])[tok],
+                      _by_gpu_slot(want["dgate"], c["idx64"][tok], gidx, cfg.E)) < 1e-2
+    assert ref.rel_l2(_np(g["du"])[tok], np.take_along_axis(want["du"], gidx, 1)) < 1e-2
+    dw13, dw2 = _np(g["dw13"]), _np(g["dw2"])
+    for e in (0, 17, 63):
+        rows, slots = np.nonzero(c["idx64"] == e)
+        W1, W3, W2 = host(e)
+        dYe = c["gate64"][rows, slots][:, None] * c["dy64"][rows]
+        _, dW1, dW3, dW2 = B.swiglu_ffn_bwd64(c["x64"][rows], W1, W3, W2, dYe)
+        assert ref.rel_l2(dw13[e, :cfg.I], dW1) < 1e-2, e
+        assert ref.rel_l2(dw13[e, cfg.I:], dW3) < 1e-2, e
+        assert ref.rel_l2(dw2[e], dW2) < 1e-2, e
