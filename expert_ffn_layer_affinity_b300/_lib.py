@@ -53,9 +53,8 @@ SIGNATURES = {
     "moe_combine_backward": (I, [P, P, P, P, I, I, I, P, P, P]),
     "moe_swiglu_backward": (I, [P, P, P, I, I, P, P, P]),
     "moe_grouped_gemm": (I, [P, P, I, I, I, I, P, P, P, P]),
-    "moe_grouped_gemm_wgrad": (I, [P, P, LL, P, I, I, I, P, P, P]),
-    "moe_transpose_grouped": (I, [P, P, I, I, I, P, LL, P, P]),
-    "moe_transpose_batched": (I, [P, I, I, I, P, LL, LL, P]),
+    "moe_grouped_gemm_wgrad": (I, [P, P, P, I, I, I, I, P, P, P]),
+    "moe_grouped_gemm_kn": (I, [P, P, I, I, I, I, P, P, P, P, P]),
     "moe_router_backward": (I, [P, P, I, P, P, P, P, P, P, I, I, I, I, F, P, P, P, P, P]),
     "moe_combine_dx": (I, [P, P, I, P, P, I, I, P, P]),
 }
@@ -250,25 +249,18 @@ def moe_grouped_gemm(a, group_offsets, n_groups, R, K, N, w, out, status_dev, st
     return _check("moe_grouped_gemm", r) if check else r
 
 
-def moe_grouped_gemm_wgrad(at, bt, ld, koff, n_groups, M, N, out, status_dev, stream=None,
+def moe_grouped_gemm_wgrad(a, b, group_offsets, n_groups, R, M, N, out, status_dev, stream=None,
                            check=True):
-    r = lib().moe_grouped_gemm_wgrad(_ptr(at), _ptr(bt), ld, _ptr(koff), n_groups, M, N, _ptr(out),
-                                     _ptr(status_dev), _stream(stream))
+    r = lib().moe_grouped_gemm_wgrad(_ptr(a), _ptr(b), _ptr(group_offsets), n_groups, R, M, N,
+                                     _ptr(out), _ptr(status_dev), _stream(stream))
     return _check("moe_grouped_gemm_wgrad", r) if check else r
 
 
-def moe_transpose_grouped(src, group_offsets, n_groups, R, C, dst, ld, koff_out, stream=None,
-                          check=True):
-    r = lib().moe_transpose_grouped(_ptr(src), _ptr(group_offsets), n_groups, R, C, _ptr(dst), ld,
-                                    _ptr(koff_out), _stream(stream))
-    return _check("moe_transpose_grouped", r) if check else r
-
-
-def moe_transpose_batched(src, batches, rows, cols, dst, dst_ld, dst_batch_stride, stream=None,
-                          check=True):
-    r = lib().moe_transpose_batched(_ptr(src), batches, rows, cols, _ptr(dst), dst_ld,
-                                    dst_batch_stride, _stream(stream))
-    return _check("moe_transpose_batched", r) if check else r
+def moe_grouped_gemm_kn(a, group_offsets, n_groups, R, K, N, w0, w1, out, status_dev, stream=None,
+                        check=True):
+    r = lib().moe_grouped_gemm_kn(_ptr(a), _ptr(group_offsets), n_groups, R, K, N, _ptr(w0),
+                                  _ptr(w1), _ptr(out), _ptr(status_dev), _stream(stream))
+    return _check("moe_grouped_gemm_kn", r) if check else r
 
 
 def moe_router_backward(dgate, topk_idx, ldk, affinity, w_r, x, row_of, tok_of, expert_offsets,

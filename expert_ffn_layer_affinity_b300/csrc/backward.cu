@@ -224,70 +224,6 @@ __global__ void __launch_bounds__(256) combine_dx_kernel(
   }
 }
 
-// Group g's rows off[g] .. off[g+1] of src [R, C] become columns
-// poff[g] .. poff[g] + rows of dst [C, ld], zeros up to the next multiple of
-// 64 (poff[g+1]).  32 x 32 tiles through shared memory.
-__global__ void __launch_bounds__(256) transpose_grouped_kernel(
-    const uint16_t* __restrict__ src, const int32_t* __restrict__ off,
-    const int32_t* __restrict__ poff, int G, int C, long long ld, uint16_t* __restrict__ dst) {
-  __shared__ uint16_t tile[32][33];
-  const int g = blockIdx.z;
-  const int pr0 = poff[g], pr1 = poff[g + 1];  // padded column range of the group
-  const int r0 = off[g], rows = off[g + 1] - off[g];
-  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;  // 32 x 8
-  const int c0 = blockIdx.y * 32;
-  for (int j0 = blockIdx.x * 32; j0 < pr1 - pr0; j0 += gridDim.x * 32) {
-    // load rows j0 .. j0+31 of the group (zero beyond its rows), columns c0 .. c0+31
-    for (int i = ty; i < 32; i += 8) {
-      const int j = j0 + i, c = c0 + tx;
-      uint16_t v = 0;
-      if (j < rows && c < C) v = src[static_cast<size_t>(r0 + j) * C + c];
-      tile[i][tx] = v;
-    }
-    __syncthreads();
-    for (int i = ty; i < 32; i += 8) {
-      const int c = c0 + i, j = j0 + tx;
-      if (c < C && j < pr1 - pr0) dst[static_cast<size_t>(c) * ld + pr0 + j] = tile[tx][i];
-    }
-    __syncthreads();
-  }
-}
-
-// dst[b*dbs + c*dst_ld + r] = src[b*sbs + r*cols + c]: a transpose of each of
-// `batches` [rows, cols] matrices into rows of stride dst_ld (32 x 32 tiles).
-__global__ void __launch_bounds__(256) transpose_batched_kernel(
-    const uint16_t* __restrict__ src, int rows, int cols, long long sbs,
-    uint16_t* __restrict__ dst, long long dst_ld, long long dbs) {
-  __shared__ uint16_t tile[32][33];
-  const long long b = blockIdx.z;
-  const int r0 = blockIdx.x * 32, c0 = blockIdx.y * 32;
-  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
-  const uint16_t* sp = src + b * sbs;
-  uint16_t* dp = dst + b * dbs;
-  for (int i = ty; i < 32; i += 8) {
-    const int r = r0 + i, c = c0 + tx;
-    tile[i][tx] = (r < rows && c < cols) ? sp[static_cast<size_t>(r) * cols + c] : 0;
-  }
-  __syncthreads();
-  for (int i = ty; i < 32; i += 8) {
-    const int c = c0 + i, r = r0 + tx;
-    if (c < cols && r < rows) dp[static_cast<size_t>(c) * dst_ld + r] = tile[tx][i];
-  }
-}
-
-// poff[g] = sum over earlier groups of their rows rounded up to 64.
-__global__ void padded_offsets_kernel(const int32_t* __restrict__ off, int G,
-                                      int32_t* __restrict__ poff) {
-  if (threadIdx.x != 0 || blockIdx.x != 0) return;
-  int acc = 0;
-  for (int g = 0; g < G; ++g) {
-    poff[g] = acc;
-    const int rows = off[g + 1] - off[g];
-    acc += (rows + 63) & ~63;
-  }
-  poff[G] = acc;
-}
-
 int grid_cap(long long work, int per_block, int cap_per_sm) {
   long long b = (work + per_block - 1) / per_block;
   const long long cap = static_cast<long long>(sm_count()) * cap_per_sm;
@@ -346,34 +282,6 @@ cudaError_t launch_combine_dx(const uint16_t* dx_perm, const int32_t* row_of, in
   combine_dx_kernel<<<grid_cap(static_cast<long long>(T) * chunks, 256, 8), 256, 0, s>>>(
       reinterpret_cast<const uint4*>(dx_perm), row_of, K, reinterpret_cast<const uint4*>(dx_shared),
       reinterpret_cast<const float4*>(dx_router), T, chunks, reinterpret_cast<uint4*>(dx));
-  return cudaGetLastError();
-}
-
-cudaError_t launch_transpose_batched(const uint16_t* src, int batches, int rows, int cols,
-                                     uint16_t* dst, long long dst_ld, long long dst_batch_stride,
-                                     cudaStream_t s) {
-  if (batches == 0 || rows == 0 || cols == 0) return cudaSuccess;
-  if (batches > 65535) return cudaErrorInvalidValue;
-  transpose_batched_kernel<<<dim3((rows + 31) / 32, (cols + 31) / 32, batches), 256, 0, s>>>(
-      src, rows, cols, static_cast<long long>(rows) * cols, dst, dst_ld, dst_batch_stride);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_padded_offsets(const int32_t* off, int G, int32_t* poff, cudaStream_t s) {
-  padded_offsets_kernel<<<1, 32, 0, s>>>(off, G, poff);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_transpose_grouped(const uint16_t* src, const int32_t* off, const int32_t* poff,
-                                     int G, int R_bound, int C, long long ld, uint16_t* dst,
-                                     cudaStream_t s) {
-  if (G == 0 || C == 0) return cudaSuccess;
-  // blocks along the group's padded rows: enough for the largest group is
-  // unknown on the host, so each block strides over them
-  int gx = (R_bound + 31) / 32;
-  if (gx > 64) gx = 64;
-  if (gx < 1) gx = 1;
-  transpose_grouped_kernel<<<dim3(gx, (C + 31) / 32, G), 256, 0, s>>>(src, off, poff, G, C, ld, dst);
   return cudaGetLastError();
 }
 

@@ -5,6 +5,12 @@
 //   MODE_SWIGLU  h[r, :] = silu(a[r] . w1[g]^T) * (a[r] . w3[g]^T)  -> bf16
 //   MODE_DOWN    y[r, :] = h[r] . w2[g]^T                            -> bf16
 //   MODE_ROUTER  s[t, e] = sigmoid(x[t] . w_r[e] + o[e])             -> fp32
+//   MODE_DGRAD   o[r, :] = a[r] . [w[g] ; w'[g]]                     -> bf16
+//
+// MODE_DGRAD is the data-gradient product of the backward pass, e.g.
+// dh = dy . W2 and dv = [da | dc] . [W1 ; W3]: the weights stay in their
+// forward layout [K, N] (N contiguous) and are read MN-major by the MMA
+// (the transpose bit of A), up to two stacked parts along K from two maps.
 //
 // Experts as shared + fine-grained routed FFNs follow weigao.cc "DeepSeek-V3
 // Technical Report：中英对照解读", §2 table rows "DeepSeekMoE" and "Shared
@@ -59,7 +65,7 @@ using gemm::tile_n;
 using gemm::store_block_transposed;
 constexpr int kRouterChunkKb = 4;
 
-enum Mode : int { MODE_SWIGLU = 0, MODE_DOWN = 1, MODE_ROUTER = 2 };
+enum Mode : int { MODE_SWIGLU = 0, MODE_DOWN = 1, MODE_ROUTER = 2, MODE_DGRAD = 3 };
 
 template <int MODE>
 struct Tr;
@@ -83,6 +89,10 @@ struct Tr<MODE_DOWN> {
                        kBufCols = 256;
   static constexpr int kA = 128 * BK * 2, kB = 128 * BK * 2;
 };
+// Data-gradient pair tile: as MODE_DOWN, the weight tile staged MN-major
+// (two 64-column chunks of 64 k-rows per CTA).
+template <>
+struct Tr<MODE_DGRAD> : Tr<MODE_DOWN> {};
 template <>
 struct Tr<MODE_ROUTER> {
   static constexpr bool kPair = false;
@@ -121,6 +131,7 @@ struct GemmParams {
   int num_kb;            // reduction length / BK
   int a_k_wrap_kb;       // router: x's k-block = kb % a_k_wrap_kb
   int w_rows_per_group;  // rows of the weight operand's 2-D view per group
+  int w_part_kb;         // DGRAD: k-blocks from tmA, the rest from tmA2
   void* out;
   int ldo;               // output row stride in elements
   const float* col_offset;  // router: per-expert logit offset or nullptr
@@ -256,6 +267,15 @@ __global__ void __launch_bounds__(kThreads, 1)
               } else if (MODE == MODE_SWIGLU) {
                 tma_load_2d_pair(aj, &tmA, fb, kx, w_row, pol_w);
                 tma_load_2d_pair(aj + 64 * 128, &tmA2, fb, kx, w_row, pol_w);
+              } else if (MODE == MODE_DGRAD) {
+                // weights [K, N]: rows are k, columns the output columns of
+                // this CTA's 128 (two 64-wide chunks)
+                const int kb = kb0 + j;
+                const bool second = kb >= p.w_part_kb;
+                const int krow = g * p.w_rows_per_group + (second ? kb - p.w_part_kb : kb) * BK;
+                const int ncol = n * C::kColTile + static_cast<int>(rank) * 128;
+                tma_load_2d_pair(aj, second ? &tmA2 : &tmA, fb, ncol, krow, pol_w);
+                tma_load_2d_pair(aj + 64 * BK * 2, second ? &tmA2 : &tmA, fb, ncol + 64, krow, pol_w);
               } else {
                 tma_load_2d_pair(aj, &tmA, fb, kx, w_row, pol_w);
               }
@@ -286,7 +306,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           idesc = umma_idesc_bf16(128, C::kColTile);
         } else {
           const int rows_g = row_start[g + 1] - row_start[g];
-          idesc = umma_idesc_bf16(256, tile_n(rows_g - m * C::kTokTile, C::kTokTile));
+          idesc = umma_idesc_bf16(256, tile_n(rows_g - m * C::kTokTile, C::kTokTile)) |
+                  (MODE == MODE_DGRAD ? (1u << 15) : 0u);  // A (weights) MN-major
         }
         for (int st0 = 0; st0 < num_st && ok; st0 += chunk_st, ++unit) {
           const int b = static_cast<int>(unit % NB);
@@ -310,14 +331,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int nbox = (p.num_kb - kb0) < C::kBoxes ? p.num_kb - kb0 : C::kBoxes;
             const uint32_t sa = tiles + s * C::kStageBytes;
             for (int j = 0; j < nbox; ++j) {
-              const uint64_t adesc = umma_sdesc_sw128(sa + static_cast<uint32_t>(j * C::kA));
+              const uint64_t adesc = MODE == MODE_DGRAD
+                                         ? umma_sdesc_mn_sw128(sa + static_cast<uint32_t>(j * C::kA))
+                                         : umma_sdesc_sw128(sa + static_cast<uint32_t>(j * C::kA));
               const uint64_t bdesc =
                   umma_sdesc_sw128(sa + static_cast<uint32_t>(C::kBoxes * C::kA + j * C::kB));
+              // the next 16 of K: 32 bytes along a K-major row, or 16
+              // 128-byte rows of an MN-major chunk
+              constexpr uint64_t a_step = MODE == MODE_DGRAD ? (16 * 128) >> 4 : 2;
 #pragma unroll
               for (int k = 0; k < BK / UMMA_K; ++k) {
                 const uint32_t acc = (st > st0 || j > 0 || k > 0) ? 1u : 0u;
-                if (PAIR) umma_bf16_pair(d_tmem, adesc + 2ull * k, bdesc + 2ull * k, idesc, acc);
-                else umma_bf16(d_tmem, adesc + 2ull * k, bdesc + 2ull * k, idesc, acc);
+                if (PAIR) umma_bf16_pair(d_tmem, adesc + a_step * k, bdesc + 2ull * k, idesc, acc);
+                else umma_bf16(d_tmem, adesc + a_step * k, bdesc + 2ull * k, idesc, acc);
               }
             }
             issued = true;
@@ -587,6 +613,35 @@ cudaError_t launch_grouped_gemm_nt(const uint16_t* a, const int32_t* offsets, in
   p.status = status;
   const int mt = (R + C2::kTokTile - 1) / C2::kTokTile + G;
   return launch_gemm<MODE_DOWN>(tw, tw, ta, p, mt * ((N + 255) / 256), s);
+}
+
+cudaError_t launch_grouped_gemm_kn(const uint16_t* a, const int32_t* offsets, int G, int R, int K,
+                                   int N, const uint16_t* w0, int K0, const uint16_t* w1,
+                                   uint16_t* out, int32_t* status, cudaStream_t s) {
+  if (R == 0 || G == 0) return cudaSuccess;
+  if (G > kMaxGroups) return cudaErrorInvalidValue;
+  using C = Cfg<MODE_DGRAD>;
+  CUtensorMap tw0, tw1, ta;
+  const int K1 = K - K0;
+  if (!make_map(&tw0, w0, N, static_cast<uint64_t>(G) * K0, BK) ||
+      !make_map(&tw1, K1 > 0 ? w1 : w0, N, static_cast<uint64_t>(G) * (K1 > 0 ? K1 : K0), BK) ||
+      !make_map(&ta, a, K, R, 128))
+    return cudaErrorInvalidValue;
+  GemmParams p{};
+  p.group_offsets = offsets;
+  p.G = G;
+  p.N = N;
+  p.R = R;
+  p.num_kb = K / BK;
+  p.a_k_wrap_kb = K / BK;
+  p.w_rows_per_group = K0;  // rows of each part per group: K0 and K1
+  p.w_part_kb = K0 / BK;
+  p.out = out;
+  p.ldo = N;
+  p.status = status;
+  // (the second part's rows per group equal the first's whenever it exists)
+  const int mt = (R + C::kTokTile - 1) / C::kTokTile + G;
+  return launch_gemm<MODE_DGRAD>(tw0, tw1, ta, p, mt * ((N + 255) / 256), s);
 }
 
 cudaError_t launch_router_gemm(const uint16_t* x, const uint16_t* w_split, const float* offset,

@@ -95,12 +95,15 @@ cudaError_t launch_grouped_swiglu_fp8_small(const uint8_t* a_q, int ld_as, const
                                             cudaStream_t s);
 
 // ---- backward (backward.cu, gemm_wgrad.cu, gemm_tc.cu)
+cudaError_t launch_grouped_gemm_kn(const uint16_t* a, const int32_t* offsets, int G, int R, int K,
+                                   int N, const uint16_t* w0, int K0, const uint16_t* w1,
+                                   uint16_t* out, int32_t* status, cudaStream_t s);
 cudaError_t launch_grouped_gemm_nt(const uint16_t* a, const int32_t* offsets, int G, int R, int K,
                                    int N, const uint16_t* w, uint16_t* out, int32_t* status,
                                    cudaStream_t s);
-cudaError_t launch_grouped_wgrad(const uint16_t* at, const uint16_t* bt, long long ld,
-                                 const int32_t* koff, int G, int M, int N, float* out,
-                                 int32_t* status, cudaStream_t s);
+cudaError_t launch_grouped_wgrad(const uint16_t* a, const uint16_t* b, const int32_t* offsets,
+                                 int G, int R, int M, int N, float* out, int32_t* status,
+                                 cudaStream_t s);
 cudaError_t launch_combine_backward(const uint16_t* dy, const uint16_t* y_perm,
                                     const int32_t* row_of, const float* gate, int T, int K, int d,
                                     uint16_t* dy_perm, float* dgate, cudaStream_t s);
@@ -115,12 +118,6 @@ cudaError_t launch_router_backward(const float* dgate, const int32_t* idx, int l
 cudaError_t launch_combine_dx(const uint16_t* dx_perm, const int32_t* row_of, int K,
                               const uint16_t* dx_shared, const float* dx_router, int T, int d,
                               uint16_t* dx, cudaStream_t s);
-cudaError_t launch_transpose_batched(const uint16_t* src, int batches, int rows, int cols,
-                                     uint16_t* dst, long long dst_ld, long long dst_batch_stride,
-                                     cudaStream_t s);
-cudaError_t launch_padded_offsets(const int32_t* off, int G, int32_t* poff, cudaStream_t s);
-cudaError_t launch_transpose_grouped(const uint16_t* src, const int32_t* off, const int32_t* poff,
-                                     int G, int R_bound, int C, long long ld, uint16_t* dst,
-                                     cudaStream_t s);
+
 
 }  // namespace moe

@@ -302,44 +302,37 @@ moe_status moe_grouped_gemm(const void* a_bf16, const int32_t* group_offsets, in
       static_cast<cudaStream_t>(stream)));
 }
 
-moe_status moe_grouped_gemm_wgrad(const void* at_bf16, const void* bt_bf16, long long ld,
-                                  const int32_t* koff, int n_groups, int M, int N, float* out,
-                                  int32_t* status_dev, moe_stream_t stream) {
-  if (n_groups < 1 || M < 1 || N < 1 || ld < 64) return MOE_ERR_INVALID_ARG;
-  if (!at_bf16 || !bt_bf16 || !koff || !out) return MOE_ERR_INVALID_ARG;
-  if (ld % 64 || M % 8 || N % 8) return MOE_ERR_UNSUPPORTED_SHAPE;
-  if (!aligned16(at_bf16) || !aligned16(bt_bf16) || !aligned16(out)) return MOE_ERR_UNSUPPORTED_SHAPE;
-  return cuda_status(launch_grouped_wgrad(static_cast<const uint16_t*>(at_bf16),
-                                          static_cast<const uint16_t*>(bt_bf16), ld, koff, n_groups,
-                                          M, N, out, status_dev, static_cast<cudaStream_t>(stream)));
+moe_status moe_grouped_gemm_kn(const void* a_bf16, const int32_t* group_offsets, int n_groups,
+                               int R, int K, int N, const void* w0_bf16, const void* w1_bf16,
+                               void* out_bf16, int32_t* status_dev, moe_stream_t stream) {
+  if (R < 0 || n_groups < 1 || K < 1 || N < 1) return MOE_ERR_INVALID_ARG;
+  if (R > 0 && (!a_bf16 || !group_offsets || !w0_bf16 || !out_bf16)) return MOE_ERR_INVALID_ARG;
+  const int K0 = w1_bf16 ? K / 2 : K;
+  if (K0 % 64 || (w1_bf16 && K % 128) || N % 8 || n_groups > 512) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (R > 0 && (!aligned16(a_bf16) || !aligned16(w0_bf16) || !aligned16(out_bf16) ||
+                (w1_bf16 && !aligned16(w1_bf16))))
+    return MOE_ERR_UNSUPPORTED_SHAPE;
+  return cuda_status(launch_grouped_gemm_kn(
+      static_cast<const uint16_t*>(a_bf16), group_offsets, n_groups, R, K, N,
+      static_cast<const uint16_t*>(w0_bf16), K0, static_cast<const uint16_t*>(w1_bf16),
+      static_cast<uint16_t*>(out_bf16), status_dev, static_cast<cudaStream_t>(stream)));
 }
 
-moe_status moe_transpose_grouped(const void* src_bf16, const int32_t* group_offsets, int n_groups,
-                                 int R, int C, void* dst_bf16, long long ld, int32_t* koff_out,
-                                 moe_stream_t stream) {
-  if (R < 0 || n_groups < 1 || C < 1 || ld < 0) return MOE_ERR_INVALID_ARG;
-  if (!src_bf16 || !group_offsets || !dst_bf16 || !koff_out) return MOE_ERR_INVALID_ARG;
-  if (ld % 64 || n_groups > 65535) return MOE_ERR_UNSUPPORTED_SHAPE;
-  // the padded groups end at most at round_up(R, 64) + 64 (G - 1)
-  if (ld < (static_cast<long long>(R) + 63) / 64 * 64 + 64ll * (n_groups - 1))
-    return MOE_ERR_INVALID_ARG;
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-  cudaError_t e = launch_padded_offsets(group_offsets, n_groups, koff_out, st);
-  if (e != cudaSuccess) return cuda_status(e);
-  return cuda_status(launch_transpose_grouped(static_cast<const uint16_t*>(src_bf16),
-                                              group_offsets, koff_out, n_groups, R, C, ld,
-                                              static_cast<uint16_t*>(dst_bf16), st));
-}
-
-moe_status moe_transpose_batched(const void* src_bf16, int batches, int rows, int cols,
-                                 void* dst_bf16, long long dst_ld, long long dst_batch_stride,
-                                 moe_stream_t stream) {
-  if (batches < 0 || rows < 0 || cols < 0 || dst_ld < rows) return MOE_ERR_INVALID_ARG;
-  if (batches > 0 && rows > 0 && cols > 0 && (!src_bf16 || !dst_bf16)) return MOE_ERR_INVALID_ARG;
-  if (batches > 65535) return MOE_ERR_UNSUPPORTED_SHAPE;
-  return cuda_status(launch_transpose_batched(static_cast<const uint16_t*>(src_bf16), batches,
-                                              rows, cols, static_cast<uint16_t*>(dst_bf16), dst_ld,
-                                              dst_batch_stride, static_cast<cudaStream_t>(stream)));
+moe_status moe_grouped_gemm_wgrad(const void* a_bf16, const void* b_bf16,
+                                  const int32_t* group_offsets, int n_groups, int R, int M, int N,
+                                  float* out, int32_t* status_dev, moe_stream_t stream) {
+  if (R < 0 || n_groups < 1 || M < 1 || N < 1) return MOE_ERR_INVALID_ARG;
+  if (!group_offsets || !out || (R > 0 && (!a_bf16 || !b_bf16))) return MOE_ERR_INVALID_ARG;
+  if (M % 8 || N % 8 || n_groups > 65535) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned16(out) || (R > 0 && (!aligned16(a_bf16) || !aligned16(b_bf16))))
+    return MOE_ERR_UNSUPPORTED_SHAPE;
+  // with no rows the maps still need a valid address: the output stands in
+  const void* a = R > 0 ? a_bf16 : out;
+  const void* b = R > 0 ? b_bf16 : out;
+  return cuda_status(launch_grouped_wgrad(static_cast<const uint16_t*>(a),
+                                          static_cast<const uint16_t*>(b), group_offsets, n_groups,
+                                          R, M, N, out, status_dev,
+                                          static_cast<cudaStream_t>(stream)));
 }
 
 moe_status moe_router_backward(const float* dgate, const int32_t* topk_idx, int ldk,

@@ -166,6 +166,22 @@ __device__ __forceinline__ uint64_t umma_sdesc_sw128(uint32_t saddr) {
   return d;
 }
 
+// Shared-memory matrix descriptor for an MN-major operand tile stored with
+// the 128-byte swizzle, as a TMA box of 64 MN elements x k rows writes it:
+// one 128-byte row per k, 8-row groups 1024 B apart (stride offset), 64-wide
+// MN chunks `chunk_bytes` apart (leading offset).  The next 16 of K start
+// 16 rows (2048 B) further on.  The tile must start on a 1024-byte boundary.
+__device__ __forceinline__ uint64_t umma_sdesc_mn_sw128(uint32_t saddr,
+                                                        uint32_t chunk_bytes = 64 * 64 * 2) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);       // start address
+  d |= static_cast<uint64_t>(chunk_bytes >> 4) << 16;         // leading byte offset
+  d |= static_cast<uint64_t>(1024 >> 4) << 32;                // stride byte offset
+  d |= static_cast<uint64_t>(1) << 46;                        // descriptor version
+  d |= static_cast<uint64_t>(2) << 61;                        // swizzle: 128 B
+  return d;
+}
+
 // 32 TMEM lanes x 32 consecutive 32-bit columns: thread i of the warp gets
 // lane (base lane + i), columns col..col+31.
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {

@@ -340,34 +340,13 @@ class MoELayer:
         return int(self.status.item())
 
     # ------------------------------------------------------------- backward
-    def prepare_backward(self):
-        """Weight copies the data-gradient GEMMs read (once per weight
-        version): W2^T [E, I, d] and [W1 ; W3]^T [E, d, 2I], likewise for the
-        shared experts."""
-        c = self.cfg
-        E, d, I, nI = c.E, c.d, c.I, c.n_shared * c.I
-        dev, bf = self.device, torch.bfloat16
-        if getattr(self, "w2t", None) is None:
-            self.w2t = torch.empty(E, I, d, dtype=bf, device=dev)
-            self.w13t = torch.empty(E, d, 2 * I, dtype=bf, device=dev)
-            self.ws2t = torch.empty(nI, d, dtype=bf, device=dev)
-            self.ws13t = torch.empty(d, 2 * nI, dtype=bf, device=dev)
-        L.moe_transpose_batched(self.w2, E, d, I, self.w2t, d, I * d)
-        L.moe_transpose_batched(self.w1, E, I, d, self.w13t, 2 * I, d * 2 * I)
-        L.moe_transpose_batched(self.w3, E, I, d, self.w13t[:, :, I:], 2 * I, d * 2 * I)
-        L.moe_transpose_batched(self.ws2, 1, d, nI, self.ws2t, d, 0)
-        L.moe_transpose_batched(self.ws1, 1, nI, d, self.ws13t, 2 * nI, 0)
-        L.moe_transpose_batched(self.ws3, 1, nI, d, self.ws13t[:, nI:], 2 * nI, 0)
-
     def _alloc_backward(self, T: int):
         c = self.cfg
         E, d, I, K, nI = c.E, c.d, c.I, c.K, c.n_shared * c.I
         R = T * K
-        dev, bf, f32, i32 = self.device, torch.bfloat16, torch.float32, torch.int32
-        ld = (R + 63) // 64 * 64 + 64 * (E - 1)    # padded token columns, routed
-        lds = (T + 63) // 64 * 64                  # shared
+        dev, bf, f32 = self.device, torch.bfloat16, torch.float32
         self.bwd = dict(
-            T=T, ld=ld, lds=lds,
+            T=T,
             dy_perm=torch.empty(R, d, dtype=bf, device=dev),
             dgate=torch.empty(T, K, dtype=f32, device=dev),
             a=torch.empty(R, I, dtype=bf, device=dev),
@@ -375,11 +354,6 @@ class MoELayer:
             dh=torch.empty(R, I, dtype=bf, device=dev),
             dac=torch.empty(R, 2 * I, dtype=bf, device=dev),
             dx_perm=torch.empty(R, d, dtype=bf, device=dev),
-            koff=torch.empty(E + 1, dtype=i32, device=dev),
-            dyT=torch.empty(d, ld, dtype=bf, device=dev),
-            hT=torch.empty(I, ld, dtype=bf, device=dev),
-            dacT=torch.empty(2 * I, ld, dtype=bf, device=dev),
-            xT=torch.empty(d, ld, dtype=bf, device=dev),
             dw2=torch.empty(E, d, I, dtype=f32, device=dev),
             dw13=torch.empty(E, 2 * I, d, dtype=f32, device=dev),
             a_s=torch.empty(T, nI, dtype=bf, device=dev),
@@ -387,11 +361,6 @@ class MoELayer:
             dh_s=torch.empty(T, nI, dtype=bf, device=dev),
             dac_s=torch.empty(T, 2 * nI, dtype=bf, device=dev),
             dx_s=torch.empty(T, d, dtype=bf, device=dev),
-            koff_s=torch.empty(2, dtype=i32, device=dev),
-            dyT_s=torch.empty(d, lds, dtype=bf, device=dev),
-            hT_s=torch.empty(nI, lds, dtype=bf, device=dev),
-            dacT_s=torch.empty(2 * nI, lds, dtype=bf, device=dev),
-            xT_s=torch.empty(d, lds, dtype=bf, device=dev),
             dws2=torch.empty(1, d, nI, dtype=f32, device=dev),
             dws13=torch.empty(1, 2 * nI, d, dtype=f32, device=dev),
             du=torch.empty(T, K, dtype=f32, device=dev),
@@ -408,8 +377,9 @@ class MoELayer:
         keep_affinity=True, bf16 precision and the standard layout.
 
         Expert activations a = v.W1^T and c = v.W3^T are recomputed, the
-        weight gradients reduce over each expert's tokens on the tensor cores
-        (fp32 results), and every step is one library call.  Returns views of
+        data gradients read the weights in their forward layout, the weight
+        gradients reduce over each expert's tokens on the tensor cores (fp32
+        results), and every step is one library call.  Returns views of
         internal buffers valid until the next call: dx bf16 [T, d], dw_r fp32
         [E, d], dw13 fp32 [E, 2I, d] (dW1 rows 0..I-1, dW3 rows I..2I-1 of each
         expert), dw2 fp32 [E, d, I], dws13 fp32 [2 nI, d], dws2 fp32 [d, nI],
@@ -422,8 +392,6 @@ class MoELayer:
         E, d, I, K, nI = c.E, c.d, c.I, c.K, c.n_shared * c.I
         T = x.shape[0]
         R = T * K
-        if getattr(self, "w2t", None) is None:
-            self.prepare_backward()
         if getattr(self, "bwd", None) is None or self.bwd["T"] < T:
             self._alloc_backward(T)
         b = self.bwd
@@ -435,31 +403,24 @@ class MoELayer:
         # dv = [da | dc] [W1 ; W3]
         L.moe_grouped_gemm(self.x_perm, self.offsets, E, R, d, I, self.w1, b["a"], st, s)
         L.moe_grouped_gemm(self.x_perm, self.offsets, E, R, d, I, self.w3, b["c"], st, s)
-        L.moe_grouped_gemm(b["dy_perm"], self.offsets, E, R, d, I, self.w2t, b["dh"], st, s)
+        L.moe_grouped_gemm_kn(b["dy_perm"], self.offsets, E, R, d, I, self.w2, None, b["dh"], st, s)
         L.moe_swiglu_backward(b["dh"], b["a"], b["c"], R, I, b["dac"], None, s)
-        L.moe_grouped_gemm(b["dac"], self.offsets, E, R, 2 * I, d, self.w13t, b["dx_perm"], st, s)
-        # weight gradients: dW2 = dY^T h, [dW1 ; dW3] = [da | dc]^T v per expert
-        ld = b["ld"]
-        L.moe_transpose_grouped(b["dy_perm"], self.offsets, E, R, d, b["dyT"], ld, b["koff"], s)
-        L.moe_transpose_grouped(self.h, self.offsets, E, R, I, b["hT"], ld, b["koff"], s)
-        L.moe_transpose_grouped(b["dac"], self.offsets, E, R, 2 * I, b["dacT"], ld, b["koff"], s)
-        L.moe_transpose_grouped(self.x_perm, self.offsets, E, R, d, b["xT"], ld, b["koff"], s)
-        L.moe_grouped_gemm_wgrad(b["dyT"], b["hT"], ld, b["koff"], E, d, I, b["dw2"], st, s)
-        L.moe_grouped_gemm_wgrad(b["dacT"], b["xT"], ld, b["koff"], E, 2 * I, d, b["dw13"], st, s)
+        L.moe_grouped_gemm_kn(b["dac"], self.offsets, E, R, 2 * I, d, self.w1, self.w3,
+                              b["dx_perm"], st, s)
+        # weight gradients: dW2 = dY^T h, [dW1 ; dW3] = [da | dc]^T v per expert,
+        # straight from the dispatch-order buffers
+        L.moe_grouped_gemm_wgrad(b["dy_perm"], self.h, self.offsets, E, R, d, I, b["dw2"], st, s)
+        L.moe_grouped_gemm_wgrad(b["dac"], self.x_perm, self.offsets, E, R, 2 * I, d, b["dw13"],
+                                 st, s)
         # shared experts: one group of all T tokens with gate 1
-        so, lds = self.shared_offsets, b["lds"]
+        so = self.shared_offsets
         L.moe_grouped_gemm(x, so, 1, T, d, nI, self.ws1, b["a_s"], st, s)
         L.moe_grouped_gemm(x, so, 1, T, d, nI, self.ws3, b["c_s"], st, s)
-        L.moe_grouped_gemm(dy, so, 1, T, d, nI, self.ws2t, b["dh_s"], st, s)
+        L.moe_grouped_gemm_kn(dy, so, 1, T, d, nI, self.ws2, None, b["dh_s"], st, s)
         L.moe_swiglu_backward(b["dh_s"], b["a_s"], b["c_s"], T, nI, b["dac_s"], None, s)
-        L.moe_grouped_gemm(b["dac_s"], so, 1, T, 2 * nI, d, self.ws13t, b["dx_s"], st, s)
-        L.moe_transpose_grouped(dy, so, 1, T, d, b["dyT_s"], lds, b["koff_s"], s)
-        L.moe_transpose_grouped(self.h_sh, so, 1, T, nI, b["hT_s"], lds, b["koff_s"], s)
-        L.moe_transpose_grouped(b["dac_s"], so, 1, T, 2 * nI, b["dacT_s"], lds, b["koff_s"], s)
-        L.moe_transpose_grouped(x, so, 1, T, d, b["xT_s"], lds, b["koff_s"], s)
-        L.moe_grouped_gemm_wgrad(b["dyT_s"], b["hT_s"], lds, b["koff_s"], 1, d, nI, b["dws2"], st, s)
-        L.moe_grouped_gemm_wgrad(b["dacT_s"], b["xT_s"], lds, b["koff_s"], 1, 2 * nI, d,
-                                 b["dws13"], st, s)
+        L.moe_grouped_gemm_kn(b["dac_s"], so, 1, T, 2 * nI, d, self.ws1, self.ws3, b["dx_s"], st, s)
+        L.moe_grouped_gemm_wgrad(dy, self.h_sh, so, 1, T, d, nI, b["dws2"], st, s)
+        L.moe_grouped_gemm_wgrad(b["dac_s"], x, so, 1, T, 2 * nI, d, b["dws13"], st, s)
         # router: gates -> raw affinities -> logits -> w_r and x
         L.moe_router_backward(b["dgate"], self.idx, K, self.affinity, self.w_r, x, self.row_of,
                               self.tok_of, self.offsets, T, d, E, K, c.route_scale, b["du"],

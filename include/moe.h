@@ -311,38 +311,30 @@ moe_status moe_swiglu_backward(const void* dh_bf16, const void* a_bf16, const vo
 
 /* Grouped bf16 GEMM on the tensor cores: out[r] = a[r] . w[g]^T for the rows r
  * of group g (group_offsets [G+1] DEVICE).  a [R, K], w [G, N, K], out [R, N]
- * bf16; K % 64 == 0, N % 8 == 0, 1 <= G <= 512.  Used for the recomputed a, c
- * and, with transposed weights (moe_transpose_batched), dh = dy . W2 and
- * dv = [da | dc] . [W1 ; W3]. */
+ * bf16; K % 64 == 0, N % 8 == 0, 1 <= G <= 512.  Recomputes a = v W1^T and
+ * c = v W3^T in the backward pass. */
 moe_status moe_grouped_gemm(const void* a_bf16, const int32_t* group_offsets, int n_groups, int R,
                             int K, int N, const void* w_bf16, void* out_bf16, int32_t* status_dev,
                             moe_stream_t stream);
 
-/* Grouped weight-gradient GEMM: out[g][m][n] = sum over the rows r of group g
- * of A[r][m] B[r][n], fp32 [G, M, N], with the operands given TRANSPOSED:
- * at bf16 [M, ld], bt bf16 [N, ld], group g owning columns koff[g] ..
- * koff[g+1] (DEVICE [G+1], multiples of 64; rows beyond a group's tokens are
- * zero), as written by moe_transpose_grouped.  ld % 64 == 0, M, N % 8 == 0.
- * A group with no rows gets zeros. */
-moe_status moe_grouped_gemm_wgrad(const void* at_bf16, const void* bt_bf16, long long ld,
-                                  const int32_t* koff, int n_groups, int M, int N, float* out,
-                                  int32_t* status_dev, moe_stream_t stream);
+/* Grouped data-gradient GEMM: out[r] = a[r] . w[g] for the rows r of group g,
+ * the weights in their forward layout w [G, K, N] (N contiguous), or stacked
+ * along K from two halves w0, w1 [G, K/2, N] each (w1 NULL: one part):
+ * dh = (g dy) . W2 with W2 [E, d, I], and dv = [da | dc] . [W1 ; W3] with
+ * W1, W3 [E, I, d].  a [R, K], out [R, N] bf16; each part's K % 64 == 0,
+ * N % 8 == 0, 1 <= G <= 512. */
+moe_status moe_grouped_gemm_kn(const void* a_bf16, const int32_t* group_offsets, int n_groups,
+                               int R, int K, int N, const void* w0_bf16, const void* w1_bf16,
+                               void* out_bf16, int32_t* status_dev, moe_stream_t stream);
 
-/* Transposes the row groups of src bf16 [R, C] (group_offsets [G+1] DEVICE)
- * into columns of dst bf16 [C, ld]: group g's rows become columns koff[g] ..,
- * zero-padded to a multiple of 64, koff written to koff_out [G+1] DEVICE.
- * ld % 64 == 0 and ld >= round_up(R, 64) + 64 (G - 1), the most the padded
- * groups can span. */
-moe_status moe_transpose_grouped(const void* src_bf16, const int32_t* group_offsets, int n_groups,
-                                 int R, int C, void* dst_bf16, long long ld, int32_t* koff_out,
-                                 moe_stream_t stream);
-
-/* Batched transpose: dst[b*dst_batch_stride + c*dst_ld + r] = src[b][r][c] for
- * src bf16 [batches, rows, cols]; e.g. W2 [E, d, I] -> [E, I, d], and w1 / w3
- * [E, I, d] -> the two halves of [E, d, 2I]. */
-moe_status moe_transpose_batched(const void* src_bf16, int batches, int rows, int cols,
-                                 void* dst_bf16, long long dst_ld, long long dst_batch_stride,
-                                 moe_stream_t stream);
+/* Grouped weight-gradient GEMM: out[g][m][n] = sum over the rows r of group
+ * g of A[r][m] B[r][n], fp32 [G, M, N], reading the dispatch-order buffers as
+ * they are: A bf16 [R, M] (e.g. g dy or [da | dc]) and B bf16 [R, N] (h or
+ * the dispatched tokens), groups by group_offsets [G+1] (DEVICE, as written
+ * by moe_permute).  M % 8 == 0, N % 8 == 0.  A group with no rows gets zeros. */
+moe_status moe_grouped_gemm_wgrad(const void* a_bf16, const void* b_bf16,
+                                  const int32_t* group_offsets, int n_groups, int R, int M, int N,
+                                  float* out, int32_t* status_dev, moe_stream_t stream);
 
 /* Router backward (chosen experts only): du fp32 [T, K] from dgate [T, K],
  * the chosen experts topk_idx [T, ldk] (first K columns) and the forward's

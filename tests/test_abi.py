@@ -136,16 +136,20 @@ def test_backward_calls_reject_bad_arguments():
     assert moe.moe_grouped_gemm(FAKE, FAKE, 2, 8, 96, 64, FAKE, FAKE, None, **args) == E_SHAPE
     assert moe.moe_grouped_gemm(FAKE, FAKE, 2, 8, 128, 60, FAKE, FAKE, None, **args) == E_SHAPE
     assert moe.moe_grouped_gemm(FAKE, FAKE, 513, 8, 128, 64, FAKE, FAKE, None, **args) == E_SHAPE
-    # wgrad: ld % 64, M % 8, null operand
-    assert moe.moe_grouped_gemm_wgrad(FAKE, FAKE, 96, FAKE, 2, 64, 64, FAKE, None, **args) == E_SHAPE
-    assert moe.moe_grouped_gemm_wgrad(FAKE, FAKE, 128, FAKE, 2, 60, 64, FAKE, None,
+    # wgrad: M % 8, N % 8, null operand
+    assert moe.moe_grouped_gemm_wgrad(FAKE, FAKE, FAKE, 2, 64, 60, 64, FAKE, None,
                                       **args) == E_SHAPE
-    assert moe.moe_grouped_gemm_wgrad(None, FAKE, 128, FAKE, 2, 64, 64, FAKE, None, **args) == E_ARG
-    # grouped transpose: ld too small for the padded groups (R=100, G=3 -> 256)
-    assert moe.moe_transpose_grouped(FAKE, FAKE, 3, 100, 8, FAKE, 192, FAKE, **args) == E_ARG
-    assert moe.moe_transpose_grouped(FAKE, FAKE, 3, 100, 8, FAKE, 200, FAKE, **args) == E_SHAPE
-    # batched transpose: destination rows shorter than the source's
-    assert moe.moe_transpose_batched(FAKE, 2, 70, 33, FAKE, 64, 4096, **args) == E_ARG
+    assert moe.moe_grouped_gemm_wgrad(FAKE, FAKE, FAKE, 2, 64, 64, 12, FAKE, None,
+                                      **args) == E_SHAPE
+    assert moe.moe_grouped_gemm_wgrad(None, FAKE, FAKE, 2, 64, 64, 64, FAKE, None, **args) == E_ARG
+    # K-N GEMM: K % 64 per part, N % 8
+    assert moe.moe_grouped_gemm_kn(FAKE, FAKE, 2, 8, 96, 64, FAKE, None, FAKE, None, **args) == E_SHAPE
+    assert moe.moe_grouped_gemm_kn(FAKE, FAKE, 2, 8, 192, 64, FAKE, FAKE, FAKE, None,
+                                   **args) == E_SHAPE
+    assert moe.moe_grouped_gemm_kn(FAKE, FAKE, 2, 8, 128, 60, FAKE, None, FAKE, None,
+                                   **args) == E_SHAPE
+    assert moe.moe_grouped_gemm_kn(None, FAKE, 2, 8, 128, 64, FAKE, None, FAKE, None,
+                                   **args) == E_ARG
     # router backward: K > E, ldk < K
     assert moe.moe_router_backward(FAKE, FAKE, 4, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 4, 16, 2, 4,
                                    1.0, FAKE, FAKE, None, FAKE, **args) == E_ARG

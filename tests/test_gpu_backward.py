@@ -58,67 +58,79 @@ def test_grouped_gemm_nt(sizes, K, N):
     _close(got, want, 2.0 ** -8, 1e-4 * rms)
 
 
-def _host_transposed(M, sizes, seed, std=1.0):
-    """A [R, M] bf16 and its grouped transpose [M, ld] with 64-padded groups."""
-    R = sum(sizes)
-    a = _bf16((R, M), seed, std)
-    poff = np.concatenate([[0], np.cumsum([(s + 63) // 64 * 64 for s in sizes])]).astype(np.int32)
-    ld = max(64, int(poff[-1]))
-    at = torch.zeros(M, ld, dtype=torch.bfloat16)
-    off = _offsets(sizes)
-    for g in range(len(sizes)):
-        at[:, poff[g]:poff[g] + sizes[g]] = a[off[g]:off[g + 1]].T
-    return a, at, poff, ld
-
-
 @pytest.mark.parametrize("sizes,M,N", [
-    ([0, 1, 63, 64, 65, 200], 200, 136),
+    ([0, 1, 63, 64, 65, 200], 200, 136),       # ragged tails, empty group, ragged M and N
     ([310, 0, 290, 511, 129], 2048, 1408),
     ([4096], 256, 512),
+    ([0, 0, 5], 64, 64),
+    ([3] * 40 + [700], 128, 264),              # many tails in a row, one long group
 ])
 def test_grouped_wgrad(sizes, M, N):
-    G = len(sizes)
-    a, at, poff, ld = _host_transposed(M, sizes, 3)
-    b, bt, _, _ = _host_transposed(N, sizes, 4)
+    G, R = len(sizes), sum(sizes)
+    a, b = _bf16((R, M), 3), _bf16((R, N), 4)
+    off = _offsets(sizes)
     out = torch.full((G, M, N), float("nan"), dtype=torch.float32, device="cuda")
     st = torch.zeros(1, dtype=torch.int32, device="cuda")
-    moe.moe_grouped_gemm_wgrad(at.cuda(), bt.cuda(), ld, torch.from_numpy(poff).cuda(), G, M, N,
-                               out, st)
+    moe.moe_grouped_gemm_wgrad(a.cuda(), b.cuda(), torch.from_numpy(off).cuda(), G, R, M, N, out,
+                               st)
     assert sync_status(st) == 0
     got = out.cpu().numpy().astype(np.float64)
     a64, b64 = bf16_to_np64(a), bf16_to_np64(b)
-    off = _offsets(sizes)
     for g in range(G):
         A, Bm = a64[off[g]:off[g + 1]], b64[off[g]:off[g + 1]]
-        want = A.T @ Bm
         if sizes[g] == 0:
-            assert np.all(got[g] == 0.0)
+            assert np.all(got[g] == 0.0), g
             continue
-        _close(got[g], want, 0.0, 4e-6 * (np.abs(A).T @ np.abs(Bm)) + 1e-30)
+        _close(got[g], A.T @ Bm, 0.0, 4e-6 * (np.abs(A).T @ np.abs(Bm)) + 1e-30)
 
 
-def test_transposes_exact():
-    sizes = [5, 0, 64, 65, 1]
-    R, C = sum(sizes), 40
-    src = _bf16((R, C), 5)
+def test_grouped_wgrad_ignores_neighbour_rows():
+    """The rows after a group's last token (next group, here huge values)
+    must not leak into a ragged tail."""
+    sizes = [37, 64, 1]
+    G, R, M, N = 3, 102, 64, 64
+    a, b = _bf16((R, M), 5), _bf16((R, N), 6)
+    a[37:101] = 3.0e4
+    b[37:101] = -3.0e4
     off = _offsets(sizes)
-    ld = (R + 63) // 64 * 64 + 64 * (len(sizes) - 1)
-    dst = torch.full((C, ld), 7.0, dtype=torch.bfloat16, device="cuda")
-    koff = torch.zeros(len(sizes) + 1, dtype=torch.int32, device="cuda")
-    moe.moe_transpose_grouped(src.cuda(), torch.from_numpy(off).cuda(), len(sizes), R, C, dst, ld,
-                              koff)
-    torch.cuda.synchronize()
-    _, want, poff, _ = _host_transposed(C, sizes, 5)
-    np.testing.assert_array_equal(koff.cpu().numpy(), poff)
-    got = dst.cpu()[:, :poff[-1]]
-    assert torch.equal(got.view(torch.int16), want[:, :poff[-1]].view(torch.int16))
-    # batched: [3, 70, 33] -> rows of stride 80, batch stride 70*80+8
-    w = _bf16((3, 70, 33), 6)
-    dst = torch.zeros(3 * (33 * 80) + 16, dtype=torch.bfloat16, device="cuda")
-    moe.moe_transpose_batched(w.cuda(), 3, 70, 33, dst, 80, 33 * 80)
-    torch.cuda.synchronize()
-    got = dst.cpu()[:3 * 33 * 80].view(3, 33, 80)[:, :, :70]
-    assert torch.equal(got.view(torch.int16), w.transpose(1, 2).contiguous().view(torch.int16))
+    out = torch.empty((G, M, N), dtype=torch.float32, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    moe.moe_grouped_gemm_wgrad(a.cuda(), b.cuda(), torch.from_numpy(off).cuda(), G, R, M, N, out,
+                               st)
+    assert sync_status(st) == 0
+    a64, b64 = bf16_to_np64(a), bf16_to_np64(b)
+    A, Bm = a64[:37], b64[:37]
+    _close(out[0].cpu().numpy().astype(np.float64), A.T @ Bm, 0.0,
+           4e-6 * (np.abs(A).T @ np.abs(Bm)) + 1e-30)
+
+
+@pytest.mark.parametrize("sizes,K,N,two", [
+    ([3, 0, 130, 64, 1, 257], 256, 136, False),
+    ([3, 0, 130, 64, 1, 257], 256, 136, True),
+    ([300, 290, 0, 511, 17, 256, 700, 2], 2048, 1408, False),
+    ([300, 290, 0, 511, 17, 256, 700, 2], 2816, 2048, True),
+    ([1], 128, 8, True),
+])
+def test_grouped_gemm_kn(sizes, K, N, two):
+    """out[r] = a[r] . w[g] with w [G, K, N] (or two stacked halves along K)."""
+    G, R = len(sizes), sum(sizes)
+    off = _offsets(sizes)
+    a = _bf16((R, K), 41)
+    K0 = K // 2 if two else K
+    w0 = _bf16((G, K0, N), 42, 0.05)
+    w1 = _bf16((G, K0, N), 43, 0.05) if two else None
+    out = torch.full((R, N), float("nan"), dtype=torch.bfloat16, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    moe.moe_grouped_gemm_kn(a.cuda(), torch.from_numpy(off).cuda(), G, R, K, N, w0.cuda(),
+                            w1.cuda() if two else None, out, st)
+    assert sync_status(st) == 0
+    a64, got = bf16_to_np64(a), bf16_to_np64(out)
+    w64 = bf16_to_np64(w0)
+    if two:
+        w64 = np.concatenate([w64, bf16_to_np64(w1)], axis=1)
+    want = np.concatenate([a64[off[g]:off[g + 1]] @ w64[g] for g in range(G)])
+    rms = np.sqrt(np.mean(want ** 2))
+    _close(got, want, 2.0 ** -8, 1e-4 * rms)
 
 
 def _routing(T, K, E, seed):
