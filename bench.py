@@ -5,6 +5,7 @@ combine, bias update) on B300.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--config v3]
   python bench.py --impl reference ...     (the CPU oracle, timed on host cores)
+  python bench.py --pass train ...         (forward + backward + bias update per step)
 
 One step = one pass of the whole path over one batch of T tokens plus the
 bias update.  For N > 1 (launched with torch.distributed.run), every rank
@@ -36,6 +37,10 @@ CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.a
 # kernels change.
 GEMM_TRAFFIC_PER_EXPERT = (1.042742e9 + 16.753152e6 + 0.497552e9 + 48.797696e6) / 16
 KERNELS_PER_STEP = 12  # router GEMM, selection, 4 permute, 2+2 grouped GEMM, combine, bias update
+# backward: combine 1; routed: 2 recompute GEMMs, dh GEMM, SwiGLU, dv GEMM, 2 weight-gradient
+# GEMMs; shared: the same 7; router 3; input gradient 1
+KERNELS_PER_BACKWARD = 19
+METRIC_TRAIN = "MoE-layer forward+backward tokens/s (V3-shaped, bf16, all gradients)"
 
 
 def parse():
@@ -62,6 +67,9 @@ def parse():
                     help="run the shared expert on a second stream")
     ap.add_argument("--precision", choices=["bf16", "fp8"], default="bf16",
                     help="expert GEMM inputs: bf16, or E4M3 with 1x128 / 128x128 scales")
+    ap.add_argument("--pass", dest="pass_", choices=["forward", "train"], default="forward",
+                    help="train: each step is the forward pass, the backward pass (all "
+                         "gradients) and the bias update")
     return ap.parse_args()
 
 
@@ -434,6 +442,180 @@ def run_ours(args):
 
 
 # --------------------------------------------------------------------------
+def backward_bytes(cfg):
+    """Algorithmic bytes of the routed weight-gradient GEMMs: fp32 gradients
+    of every expert written once (zeros for an expert without tokens), and
+    their bf16 operands read once."""
+    T, d, E, K, I = cfg.T, cfg.d, cfg.E, cfg.K, cfg.I
+    R = T * K
+    return 4.0 * E * 3 * I * d + 2.0 * R * (d + I) + 2.0 * R * (2 * I + d)
+
+
+def cpu_baseline_train(cfg, layer, x, dy, n_tokens):
+    """The forward and backward oracles as they stand, on `n_tokens` tokens of
+    the first batch (weights fetched to host memory before timing)."""
+    import numpy as np
+    import torch
+    from oracle import moe_bwd_ref as B
+    from oracle import moe_ref as ref
+
+    def f64(t):
+        return ref.bf16_to_f64(t.cpu().contiguous().view(torch.int16).numpy().view(np.uint16))
+
+    rng = np.random.default_rng(0)
+    tok = torch.from_numpy(np.sort(rng.choice(x.shape[0], n_tokens, replace=False))).to(x.device)
+    x_h, dy_h = x[tok].cpu(), dy[tok].cpu()
+    w_r = layer.w_r.cpu().numpy()
+    bias = layer.bias.cpu().numpy()
+    off = layer.logit_offset.cpu().numpy() if layer.logit_offset is not None else None
+    s = ref.router_affinity64(f64(x_h), w_r, off)
+    idx, _ = ref.select_experts(s, bias.astype(np.float64), cfg.K, cfg.n_groups, cfg.topk_groups,
+                                cfg.route_scale, precision="fp64")
+    host = {int(e): (layer.w1[e].cpu(), layer.w3[e].cpu(), layer.w2[e].cpu())
+            for e in np.unique(idx)}
+    shared_h = (layer.ws1.cpu(), layer.ws3.cpu(), layer.ws2.cpu())
+    t0 = time.perf_counter()
+    x64, dy64 = f64(x_h), f64(dy_h)
+    s = ref.router_affinity64(x64, w_r, off)
+    idx, gate = ref.select_experts(s, bias.astype(np.float64), cfg.K, cfg.n_groups,
+                                   cfg.topk_groups, cfg.route_scale, precision="fp64")
+    experts = lambda e: tuple(f64(w) for w in host[e])
+    shared = tuple(f64(w) for w in shared_h)
+    ref.moe_output64(x64, idx, gate, experts, shared, cfg.n_shared)
+    B.moe_layer_bwd64(x64, w_r, off, idx, cfg.route_scale, experts, shared, cfg.n_shared, dy64)
+    ref.bias_update(ref.expert_load(idx, cfg.E), bias, n_tokens, cfg.K, cfg.E, cfg.gamma)
+    dt = time.perf_counter() - t0
+    return {"value": n_tokens / dt, "unit": "tokens/s", "cores": blas_threads(), "kind": "oracle",
+            "sample": f"{n_tokens} random tokens of the first {cfg.T}-token batch: routing, "
+                      f"forward and backward of the {cfg.K} routed + {cfg.n_shared} shared "
+                      f"SwiGLU experts and the router in fp64, bias update; {dt:.1f} s"}
+
+
+def run_train(args):
+    """Forward + backward (+ bias update) per step, one GPU."""
+    import torch
+    from expert_ffn_layer_affinity_b300 import synth
+    from expert_ffn_layer_affinity_b300.layer import MoELayer
+
+    if int(os.environ.get("WORLD_SIZE", "1")) > 1 and int(os.environ.get("RANK", "0")) != 0:
+        return                                    # one replica measures (no cross-rank gradients)
+    torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+    cfg = load_config(args.config)
+    p = synth.make_params(cfg, "cuda")
+    layer = MoELayer(cfg, p, keep_affinity=True)
+    del p
+    xs = [synth.make_tokens(cfg, step=i, device="cuda") for i in range(2)]
+    dys = [synth.make_output_grad(cfg, step=i, device="cuda") for i in range(2)]
+    stream = torch.cuda.current_stream()
+    fnames = ["route", "permute", "routed", "shared", "combine"]
+    bnames = ["bwd_combine", "bwd_routed_dgrad", "bwd_routed_wgrad", "bwd_shared", "bwd_router",
+              "bwd_dx"]
+
+    def step(i, marks=None):
+        layer.forward(xs[i % 2], marks=marks)
+        layer.backward(xs[i % 2], dys[i % 2], marks=marks)
+        layer.bias_update(cfg.T)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    if layer.device_status() != 0:
+        raise RuntimeError(f"device status {layer.device_status()} during warm-up")
+    marks = [{n: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for n in fnames + bnames} for _ in range(args.steps)]
+    clocks = ClockSampler(int(os.environ.get("LOCAL_RANK", "0")))
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks.mark_start()
+    ev0.record(stream)
+    for i in range(args.steps):
+        step(i, marks[i])
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    clocks.mark_stop()
+    clk = clocks.stop()
+    ms = ev0.elapsed_time(ev1)
+    status = layer.device_status()
+    per = {n: statistics.mean(m[n][0].elapsed_time(m[n][1]) for m in marks)
+           for n in fnames + bnames}
+    ms_step = ms / args.steps
+
+    # end to end: x and dy from pinned host memory, dx back, every step
+    e2e = None
+    if not args.no_e2e:
+        x_host = [x.cpu().pin_memory() for x in xs]
+        dy_host = [g.cpu().pin_memory() for g in dys]
+        dx_host = torch.empty(cfg.T, cfg.d, dtype=torch.bfloat16).pin_memory()
+        x_dev = torch.empty_like(xs[0])
+        dy_dev = torch.empty_like(dys[0])
+
+        def host_step(i):
+            x_dev.copy_(x_host[i % 2], non_blocking=True)
+            dy_dev.copy_(dy_host[i % 2], non_blocking=True)
+            layer.forward(x_dev)
+            g = layer.backward(x_dev, dy_dev)
+            layer.bias_update(cfg.T)
+            dx_host.copy_(g["dx"], non_blocking=True)
+
+        for i in range(2):
+            host_step(i)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(args.steps):
+            host_step(i)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ems = e0.elapsed_time(e1)
+        nb = cfg.T * cfg.d * 2
+        e2e = {"value": round(cfg.T * args.steps / (ems / 1e3), 1), "unit": "tokens/s",
+               "h2d_bytes_per_step": 2 * nb, "d2h_bytes_per_step": nb,
+               "ms_per_step": ems / args.steps,
+               "api": "MoELayer.forward + backward with x, dy copied in and dx copied out "
+                      "each step (weight gradients stay on the device)"}
+
+    pk = peaks()
+    wg_bytes = backward_bytes(cfg)
+    wg_gbs = wg_bytes / (per["bwd_routed_wgrad"] * 1e-3) / 1e9
+    T, d, I, R = cfg.T, cfg.d, cfg.I, cfg.R
+    dgrad_flops = 2.0 * R * d * I * 4           # recompute a, c; dh; dv (2I deep)
+    kernels = {n: {"ms": round(per[n], 4)} for n in fnames + bnames}
+    kernels["bwd_routed_dgrad"]["tflops"] = round(dgrad_flops / (per["bwd_routed_dgrad"] * 1e-3)
+                                                  / 1e12, 1)
+    kernels["bwd_routed_wgrad"]["gbs"] = round(wg_gbs, 1)
+    kernels["bwd_routed_wgrad"]["tflops"] = round(6.0 * R * d * I
+                                                  / (per["bwd_routed_wgrad"] * 1e-3) / 1e12, 1)
+    line = {
+        "metric": METRIC_TRAIN, "value": round(cfg.T * args.steps / (ms / 1e3), 1),
+        "unit": "tokens/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(ms_step, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16 (fp32 weight gradients)",
+        "data": "synthetic (seeded N(0,1) tokens and output gradients, N(0,0.02) weights)",
+        "config": {"workload": f"{cfg.name}: T={cfg.T} d={cfg.d} E={cfg.E} K={cfg.K} "
+                               f"shared={cfg.n_shared} I={cfg.I} groups={cfg.n_groups}/"
+                               f"{cfg.topk_groups} scale={cfg.route_scale}",
+                   "pass": "train (forward, backward: dx, dW_r, dW1/dW3/dW2 of every routed "
+                           "and shared expert; bias update)",
+                   "l2": "inputs larger than L2 (22.6 GB of weights read, 45 GB of fp32 "
+                         "weight gradients written per step)" if cfg.d == 7168 else
+                         "two alternating batches"},
+        "roofline": {"bound": "hbm", "achieved": round(wg_gbs, 1), "peak": pk["hbm"],
+                     "unit": "GB/s", "frac": round(wg_gbs / pk["hbm"], 4), "traffic": None,
+                     "kernel": "moe_grouped_gemm_wgrad, routed (dW2 and [dW1; dW3] launches)",
+                     "peak_kind": f"HBM copy, {pk['src']}",
+                     "bytes_per_launch_pair": wg_bytes},
+        "kernels": kernels,
+        "gpu_launches": (KERNELS_PER_STEP + KERNELS_PER_BACKWARD) * args.steps,
+        "device_status": status,
+        "clocks": clk,
+        "e2e": e2e,
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline_train(cfg, layer, xs[0], dys[0], args.cpu_sample)
+    print(json.dumps(line), flush=True)
+
+
+# --------------------------------------------------------------------------
 def run_reference(args):
     """The CPU oracle on the host cores, one bounded sample of the workload per
     step: `ref_sample` tokens routed and run through their experts in fp64,
@@ -511,6 +693,8 @@ def main():
     args = parse()
     if args.impl == "reference":
         run_reference(args)
+    elif args.pass_ == "train":
+        run_train(args)
     else:
         run_ours(args)
 

@@ -370,7 +370,8 @@ class MoELayer:
             dx=torch.empty(T, d, dtype=bf, device=dev),
         )
 
-    def backward(self, x: torch.Tensor, dy: torch.Tensor, stream=None) -> dict:
+    def backward(self, x: torch.Tensor, dy: torch.Tensor, stream=None,
+                 marks: dict | None = None) -> dict:
         """Gradients of <dy, layer(x)> for the experts the last forward(x)
         chose (that pass's routing, gates, dispatch order and expert outputs
         are reused; the bias and the selection take no gradient).  Needs
@@ -383,7 +384,11 @@ class MoELayer:
         internal buffers valid until the next call: dx bf16 [T, d], dw_r fp32
         [E, d], dw13 fp32 [E, 2I, d] (dW1 rows 0..I-1, dW3 rows I..2I-1 of each
         expert), dw2 fp32 [E, d, I], dws13 fp32 [2 nI, d], dws2 fp32 [d, nI],
-        dgate fp32 [T, K], du fp32 [T, K]."""
+        dgate fp32 [T, K], du fp32 [T, K].
+
+        `marks`, if given, maps part names ("bwd_combine", "bwd_routed_dgrad",
+        "bwd_routed_wgrad", "bwd_shared", "bwd_router", "bwd_dx") to a pair
+        of CUDA events recorded around that part."""
         if self.fp8 or self.shared_as_routed or self.n_redundant:
             raise NotImplementedError("backward: bf16 precision and the standard layout only")
         if self.affinity is None:
@@ -396,9 +401,18 @@ class MoELayer:
             self._alloc_backward(T)
         b = self.bwd
         st, s = self.status, stream
+        main = torch.cuda.current_stream() if stream is None else stream
+
+        def mark(name, i):
+            if marks is not None and name in marks:
+                marks[name][i].record(main)
+
+        mark("bwd_combine", 0)
         # combine backward: dY_perm = g dy, dgate = <dy, y_perm>
         L.moe_combine_backward(dy, self.y_perm, self.row_of, self.gate, T, K, d, b["dy_perm"],
                                b["dgate"], s)
+        mark("bwd_combine", 1)
+        mark("bwd_routed_dgrad", 0)
         # routed experts: recompute a and c, dh = dY W2, SwiGLU backward,
         # dv = [da | dc] [W1 ; W3]
         L.moe_grouped_gemm(self.x_perm, self.offsets, E, R, d, I, self.w1, b["a"], st, s)
@@ -407,11 +421,15 @@ class MoELayer:
         L.moe_swiglu_backward(b["dh"], b["a"], b["c"], R, I, b["dac"], None, s)
         L.moe_grouped_gemm_kn(b["dac"], self.offsets, E, R, 2 * I, d, self.w1, self.w3,
                               b["dx_perm"], st, s)
+        mark("bwd_routed_dgrad", 1)
+        mark("bwd_routed_wgrad", 0)
         # weight gradients: dW2 = dY^T h, [dW1 ; dW3] = [da | dc]^T v per expert,
         # straight from the dispatch-order buffers
         L.moe_grouped_gemm_wgrad(b["dy_perm"], self.h, self.offsets, E, R, d, I, b["dw2"], st, s)
         L.moe_grouped_gemm_wgrad(b["dac"], self.x_perm, self.offsets, E, R, 2 * I, d, b["dw13"],
                                  st, s)
+        mark("bwd_routed_wgrad", 1)
+        mark("bwd_shared", 0)
         # shared experts: one group of all T tokens with gate 1
         so = self.shared_offsets
         L.moe_grouped_gemm(x, so, 1, T, d, nI, self.ws1, b["a_s"], st, s)
@@ -421,11 +439,16 @@ class MoELayer:
         L.moe_grouped_gemm_kn(b["dac_s"], so, 1, T, 2 * nI, d, self.ws1, self.ws3, b["dx_s"], st, s)
         L.moe_grouped_gemm_wgrad(dy, self.h_sh, so, 1, T, d, nI, b["dws2"], st, s)
         L.moe_grouped_gemm_wgrad(b["dac_s"], x, so, 1, T, 2 * nI, d, b["dws13"], st, s)
+        mark("bwd_shared", 1)
+        mark("bwd_router", 0)
         # router: gates -> raw affinities -> logits -> w_r and x
         L.moe_router_backward(b["dgate"], self.idx, K, self.affinity, self.w_r, x, self.row_of,
                               self.tok_of, self.offsets, T, d, E, K, c.route_scale, b["du"],
                               b["du_row"], b["dx_router"], b["dw_r"], s)
+        mark("bwd_router", 1)
+        mark("bwd_dx", 0)
         L.moe_combine_dx(b["dx_perm"], self.row_of, K, b["dx_s"], b["dx_router"], T, d, b["dx"], s)
+        mark("bwd_dx", 1)
         return dict(dx=b["dx"][:T], dw_r=b["dw_r"], dw13=b["dw13"], dw2=b["dw2"],
                     dws13=b["dws13"][0], dws2=b["dws2"][0], dgate=b["dgate"][:T], du=b["du"][:T])
 
