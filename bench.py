@@ -37,9 +37,9 @@ CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.a
 # kernels change.
 GEMM_TRAFFIC_PER_EXPERT = (1.042742e9 + 16.753152e6 + 0.497552e9 + 48.797696e6) / 16
 KERNELS_PER_STEP = 12  # router GEMM, selection, 4 permute, 2+2 grouped GEMM, combine, bias update
-# backward: combine 1; routed: 2 recompute GEMMs, dh GEMM, SwiGLU, dv GEMM, 2 weight-gradient
-# GEMMs; shared: the same 7; router 3; input gradient 1
-KERNELS_PER_BACKWARD = 19
+# backward: combine 1; routed: dh GEMM, SwiGLU, dv GEMM, 2 weight-gradient GEMMs; shared:
+# the same 5; router 3; input gradient 1 (the forward keeps the pre-activations)
+KERNELS_PER_BACKWARD = 15
 METRIC_TRAIN = "MoE-layer forward+backward tokens/s (V3-shaped, bf16, all gradients)"
 
 
@@ -502,7 +502,7 @@ def run_train(args):
     torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
     cfg = load_config(args.config)
     p = synth.make_params(cfg, "cuda")
-    layer = MoELayer(cfg, p, keep_affinity=True)
+    layer = MoELayer(cfg, p, training=True)
     del p
     xs = [synth.make_tokens(cfg, step=i, device="cuda") for i in range(2)]
     dys = [synth.make_output_grad(cfg, step=i, device="cuda") for i in range(2)]
@@ -578,7 +578,7 @@ def run_train(args):
     wg_bytes = backward_bytes(cfg)
     wg_gbs = wg_bytes / (per["bwd_routed_wgrad"] * 1e-3) / 1e9
     T, d, I, R = cfg.T, cfg.d, cfg.I, cfg.R
-    dgrad_flops = 2.0 * R * d * I * 4           # recompute a, c; dh; dv (2I deep)
+    dgrad_flops = 2.0 * R * d * I * 3           # dh; dv (2I deep)
     kernels = {n: {"ms": round(per[n], 4)} for n in fnames + bnames}
     kernels["bwd_routed_dgrad"]["tflops"] = round(dgrad_flops / (per["bwd_routed_dgrad"] * 1e-3)
                                                   / 1e12, 1)

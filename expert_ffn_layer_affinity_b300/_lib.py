@@ -50,6 +50,7 @@ SIGNATURES = {
     "moe_quantize_weights_fp8": (I, [P, P, I, I, I, P, P, P]),
     "moe_permute_fp8": (I, [P, P, I, I, I, I, P, P, P, I, P]),
     "moe_grouped_swiglu_fp8": (I, [P, P, I, P, I, I, I, I, P, P, P, P, P, P, P, P, P, P]),
+    "moe_grouped_swiglu_save": (I, [P, P, I, I, I, I, P, P, P, P, P, P, P, P, P]),
     "moe_combine_backward": (I, [P, P, P, P, I, I, I, P, P, P]),
     "moe_swiglu_backward": (I, [P, P, P, I, I, P, P, P]),
     "moe_grouped_gemm": (I, [P, P, I, I, I, I, P, P, P, P]),
@@ -230,6 +231,15 @@ def moe_grouped_swiglu_fp8(a_q, a_s, ld_as, group_offsets, n_groups, R, d, I, w1
 
 
 # ------------------------------------------------------------------ backward
+def moe_grouped_swiglu_save(a, group_offsets, n_groups, R, d, I, w1, w3, w2, h, y, pre_a, pre_c,
+                            status_dev, stream=None, check=True):
+    r = lib().moe_grouped_swiglu_save(_ptr(a), _ptr(group_offsets), n_groups, R, d, I, _ptr(w1),
+                                      _ptr(w3), _ptr(w2), _ptr(h), _ptr(y), _ptr(pre_a),
+                                      _ptr(pre_c), _ptr(status_dev), _stream(stream))
+    return _check("moe_grouped_swiglu_save", r) if check else r
+
+
+
 def moe_combine_backward(dy, y_perm, row_of, gate, T, K, d, dy_perm, dgate, stream=None, check=True):
     r = lib().moe_combine_backward(_ptr(dy), _ptr(y_perm), _ptr(row_of), _ptr(gate), T, K, d,
                                    _ptr(dy_perm), _ptr(dgate), _stream(stream))

@@ -132,6 +132,8 @@ struct GemmParams {
   int a_k_wrap_kb;       // router: x's k-block = kb % a_k_wrap_kb
   int w_rows_per_group;  // rows of the weight operand's 2-D view per group
   int w_part_kb;         // DGRAD: k-blocks from tmA, the rest from tmA2
+  void* out_a;           // SWIGLU: also store the pre-activations a and c (or nullptr)
+  void* out_c;
   void* out;
   int ldo;               // output row stride in elements
   const float* col_offset;  // router: per-expert logit offset or nullptr
@@ -451,6 +453,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             } else {
               ok = __all_sync(0xFFFFFFFFu, mbar_wait(xfull_bar(pr, xb), xph, abort_flag, p.status));
               if (!ok) break;
+              if (p.out_a != nullptr && col_ok) {
+                // training: keep a = v.w1 and c = v.w3 for the backward pass
+                uint32_t cv[32];
+#pragma unroll
+                for (int j = 0; j < 32; ++j) cv[j] = __float_as_uint(xrow[j]);
+                store_block_transposed(v, xp, lane, static_cast<__nv_bfloat16*>(p.out_a), row0 + c,
+                                       valid, p.ldo, col);
+                store_block_transposed(cv, xp, lane, static_cast<__nv_bfloat16*>(p.out_c), row0 + c,
+                                       valid, p.ldo, col);
+              }
 #pragma unroll
               for (int j = 0; j < 32; ++j) {
                 const float a = __uint_as_float(v[j]);
@@ -550,7 +562,7 @@ cudaError_t launch_gemm(const CUtensorMap& a, const CUtensorMap& a2, const CUten
 cudaError_t launch_grouped_swiglu(const uint16_t* a, const int32_t* offsets, int G, int R, int d,
                                   int I, const uint16_t* w1, const uint16_t* w3,
                                   const uint16_t* w2, uint16_t* h, uint16_t* y, int32_t* status,
-                                  cudaStream_t s) {
+                                  cudaStream_t s, uint16_t* a_out, uint16_t* c_out) {
   if (R == 0 || G == 0) return cudaSuccess;
   if (G > kMaxGroups) return cudaErrorInvalidValue;
   using C1 = Cfg<MODE_SWIGLU>;
@@ -576,10 +588,13 @@ cudaError_t launch_grouped_swiglu(const uint16_t* a, const int32_t* offsets, int
   p1.out = h;
   p1.ldo = I;
   p1.status = status;
+  p1.out_a = a_out;
+  p1.out_c = c_out;
   const int mt1 = (R + C1::kTokTile - 1) / C1::kTokTile + G;
   cudaError_t e = launch_gemm<MODE_SWIGLU>(w13 ? tw13 : tw1, tw3, tx, p1, mt1 * ((I + 127) / 128), s);
   if (e != cudaSuccess) return e;
   GemmParams p2 = p1;
+  p2.out_a = p2.out_c = nullptr;
   p2.w13_3d = 0;
   p2.N = d;
   p2.num_kb = I / BK;

@@ -66,7 +66,8 @@ cudaError_t launch_router_gemm(const uint16_t* x, const uint16_t* w_split, const
 cudaError_t launch_grouped_swiglu(const uint16_t* a, const int32_t* offsets, int G, int R, int d,
                                   int I, const uint16_t* w1, const uint16_t* w3,
                                   const uint16_t* w2, uint16_t* h, uint16_t* y, int32_t* status,
-                                  cudaStream_t s);
+                                  cudaStream_t s, uint16_t* a_out = nullptr,
+                                  uint16_t* c_out = nullptr);
 
 // ---- FP8 path (quant_fp8.cu, gemm_fp8.cu)
 cudaError_t launch_quantize_rows(const uint16_t* in, int rows, int cols, uint8_t* q, float* s,

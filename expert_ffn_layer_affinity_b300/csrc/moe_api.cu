@@ -193,6 +193,29 @@ moe_status moe_grouped_swiglu(const void* a_bf16, const int32_t* group_offsets, 
       static_cast<uint16_t*>(y_bf16), status_dev, static_cast<cudaStream_t>(stream)));
 }
 
+moe_status moe_grouped_swiglu_save(const void* a_bf16, const int32_t* group_offsets,
+                                   int n_groups, int R, int d, int I, const void* w1_bf16,
+                                   const void* w3_bf16, const void* w2_bf16, void* h_bf16,
+                                   void* y_bf16, void* pre_a_bf16, void* pre_c_bf16,
+                                   int32_t* status_dev, moe_stream_t stream) {
+  if (R > 0 && (!pre_a_bf16 || !pre_c_bf16)) return MOE_ERR_INVALID_ARG;
+  if (R > 0 && (!aligned16(pre_a_bf16) || !aligned16(pre_c_bf16))) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (R < 0 || n_groups < 1 || d < 1 || I < 1) return MOE_ERR_INVALID_ARG;
+  if (R > 0 && (!a_bf16 || !group_offsets || !w1_bf16 || !w3_bf16 || !w2_bf16 || !h_bf16 ||
+                !y_bf16))
+    return MOE_ERR_INVALID_ARG;
+  if (d % 64 || I % 64 || n_groups > 512) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (R > 0 && (!aligned16(a_bf16) || !aligned16(w1_bf16) || !aligned16(w3_bf16) ||
+                !aligned16(w2_bf16) || !aligned16(h_bf16) || !aligned16(y_bf16)))
+    return MOE_ERR_UNSUPPORTED_SHAPE;
+  return cuda_status(launch_grouped_swiglu(
+      static_cast<const uint16_t*>(a_bf16), group_offsets, n_groups, R, d, I,
+      static_cast<const uint16_t*>(w1_bf16), static_cast<const uint16_t*>(w3_bf16),
+      static_cast<const uint16_t*>(w2_bf16), static_cast<uint16_t*>(h_bf16),
+      static_cast<uint16_t*>(y_bf16), status_dev, static_cast<cudaStream_t>(stream),
+      static_cast<uint16_t*>(pre_a_bf16), static_cast<uint16_t*>(pre_c_bf16)));
+}
+
 // ------------------------------------------------------------------ FP8 path
 moe_status moe_quantize_fp8(const void* x_bf16, int rows, int cols, void* q_out, float* s_out,
                             int ld_s, moe_stream_t stream) {

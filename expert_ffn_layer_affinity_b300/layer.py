@@ -40,9 +40,15 @@ class MoELayer:
     def __init__(self, cfg: LayerConfig, params: dict, max_T: int | None = None,
                  device: str = "cuda", keep_affinity: bool = False,
                  shared_stream: bool = False, shared_as_routed: bool = False,
-                 n_redundant: int = 0, precision: str = "bf16"):
+                 n_redundant: int = 0, precision: str = "bf16", training: bool = False):
         if precision not in ("bf16", "fp8"):
             raise ValueError(f"precision must be 'bf16' or 'fp8', not {precision!r}")
+        if training and (precision != "bf16" or shared_as_routed or n_redundant):
+            raise NotImplementedError("training: bf16 precision and the standard layout only")
+        # training keeps what the backward pass reads: the affinities and the
+        # experts' pre-activations a = v.W1^T, c = v.W3^T
+        self.training = training
+        keep_affinity = keep_affinity or training
         self.cfg = cfg
         self.fp8 = precision == "fp8"
         self.device = torch.device(device)
@@ -157,6 +163,11 @@ class MoELayer:
         self.out = torch.empty(T, d, dtype=bf, device=dev)
         self.affinity = (torch.empty(T, E, dtype=torch.float32, device=dev)
                          if self.keep_affinity else None)
+        if self.training:
+            self.pre_a = torch.empty(R, I, dtype=bf, device=dev)
+            self.pre_c = torch.empty(R, I, dtype=bf, device=dev)
+            self.pre_a_sh = torch.empty(T, ns * I, dtype=bf, device=dev)
+            self.pre_c_sh = torch.empty(T, ns * I, dtype=bf, device=dev)
         self.ws_bytes = L.moe_workspace_bytes(T, d, self.E_phys, K, I)
         self.ws = torch.empty(max(self.ws_bytes, 256), dtype=torch.uint8, device=dev)
         self.shared_offsets = torch.tensor([0, T], dtype=i32, device=dev)
@@ -248,23 +259,35 @@ class MoELayer:
                       self.x_perm, self.status, self.ws, self.ws_bytes, stream)
         mark("permute", 1)
         separate_shared = not self.shared_as_routed
+
+        def shared(s):
+            if self.training:
+                L.moe_grouped_swiglu_save(x, self.shared_offsets, 1, T, c.d, c.n_shared * c.I,
+                                          self.ws1, self.ws3, self.ws2, self.h_sh, self.y_sh,
+                                          self.pre_a_sh, self.pre_c_sh, self.status, s)
+            else:
+                L.moe_grouped_swiglu(x, self.shared_offsets, 1, T, c.d, c.n_shared * c.I, self.ws1,
+                                     self.ws3, self.ws2, self.h_sh, self.y_sh, self.status, s)
+
         if self.side is not None and separate_shared:
             self.side.wait_stream(main)
             mark("shared", 0, self.side)
-            L.moe_grouped_swiglu(x, self.shared_offsets, 1, T, c.d, c.n_shared * c.I, self.ws1,
-                                 self.ws3, self.ws2, self.h_sh, self.y_sh, self.status,
-                                 self.side)
+            shared(self.side)
             mark("shared", 1, self.side)
         mark("routed", 0)
-        L.moe_grouped_swiglu(self.x_perm, self.offsets, self.E_phys, R, c.d, c.I, self.w1,
-                             self.w3, self.w2, self.h, self.y_perm, self.status, stream)
+        if self.training:
+            L.moe_grouped_swiglu_save(self.x_perm, self.offsets, self.E_phys, R, c.d, c.I, self.w1,
+                                      self.w3, self.w2, self.h, self.y_perm, self.pre_a,
+                                      self.pre_c, self.status, stream)
+        else:
+            L.moe_grouped_swiglu(self.x_perm, self.offsets, self.E_phys, R, c.d, c.I, self.w1,
+                                 self.w3, self.w2, self.h, self.y_perm, self.status, stream)
         mark("routed", 1)
         if self.side is not None and separate_shared:
             main.wait_stream(self.side)
         elif separate_shared:
             mark("shared", 0)
-            L.moe_grouped_swiglu(x, self.shared_offsets, 1, T, c.d, c.n_shared * c.I, self.ws1,
-                                 self.ws3, self.ws2, self.h_sh, self.y_sh, self.status, stream)
+            shared(stream)
             mark("shared", 1)
         dst = self.out[:T] if out is None else out
         mark("combine", 0)
@@ -349,15 +372,15 @@ class MoELayer:
             T=T,
             dy_perm=torch.empty(R, d, dtype=bf, device=dev),
             dgate=torch.empty(T, K, dtype=f32, device=dev),
-            a=torch.empty(R, I, dtype=bf, device=dev),
-            c=torch.empty(R, I, dtype=bf, device=dev),
+            a=None if self.training else torch.empty(R, I, dtype=bf, device=dev),
+            c=None if self.training else torch.empty(R, I, dtype=bf, device=dev),
             dh=torch.empty(R, I, dtype=bf, device=dev),
             dac=torch.empty(R, 2 * I, dtype=bf, device=dev),
             dx_perm=torch.empty(R, d, dtype=bf, device=dev),
             dw2=torch.empty(E, d, I, dtype=f32, device=dev),
             dw13=torch.empty(E, 2 * I, d, dtype=f32, device=dev),
-            a_s=torch.empty(T, nI, dtype=bf, device=dev),
-            c_s=torch.empty(T, nI, dtype=bf, device=dev),
+            a_s=None if self.training else torch.empty(T, nI, dtype=bf, device=dev),
+            c_s=None if self.training else torch.empty(T, nI, dtype=bf, device=dev),
             dh_s=torch.empty(T, nI, dtype=bf, device=dev),
             dac_s=torch.empty(T, 2 * nI, dtype=bf, device=dev),
             dx_s=torch.empty(T, d, dtype=bf, device=dev),
@@ -374,11 +397,14 @@ class MoELayer:
                  marks: dict | None = None) -> dict:
         """Gradients of <dy, layer(x)> for the experts the last forward(x)
         chose (that pass's routing, gates, dispatch order and expert outputs
-        are reused; the bias and the selection take no gradient).  Needs
-        keep_affinity=True, bf16 precision and the standard layout.
+        are reused; the bias and the selection take no gradient).  Needs a
+        layer built with training=True (or keep_affinity=True), bf16
+        precision and the standard layout.
 
-        Expert activations a = v.W1^T and c = v.W3^T are recomputed, the
-        data gradients read the weights in their forward layout, the weight
+        Expert pre-activations a = v.W1^T and c = v.W3^T come from the
+        forward pass when the layer was built with training=True (else they
+        are recomputed), the data gradients read the weights in their
+        forward layout, the weight
         gradients reduce over each expert's tokens on the tensor cores (fp32
         results), and every step is one library call.  Returns views of
         internal buffers valid until the next call: dx bf16 [T, d], dw_r fp32
@@ -392,7 +418,8 @@ class MoELayer:
         if self.fp8 or self.shared_as_routed or self.n_redundant:
             raise NotImplementedError("backward: bf16 precision and the standard layout only")
         if self.affinity is None:
-            raise ValueError("backward needs the forward's affinities: build with keep_affinity=True")
+            raise ValueError("backward needs the forward's affinities: build with training=True "
+                             "(or keep_affinity=True to recompute the expert pre-activations)")
         c = self.cfg
         E, d, I, K, nI = c.E, c.d, c.I, c.K, c.n_shared * c.I
         T = x.shape[0]
@@ -415,10 +442,14 @@ class MoELayer:
         mark("bwd_routed_dgrad", 0)
         # routed experts: recompute a and c, dh = dY W2, SwiGLU backward,
         # dv = [da | dc] [W1 ; W3]
-        L.moe_grouped_gemm(self.x_perm, self.offsets, E, R, d, I, self.w1, b["a"], st, s)
-        L.moe_grouped_gemm(self.x_perm, self.offsets, E, R, d, I, self.w3, b["c"], st, s)
+        if self.training:
+            pa, pc = self.pre_a, self.pre_c
+        else:
+            pa, pc = b["a"], b["c"]
+            L.moe_grouped_gemm(self.x_perm, self.offsets, E, R, d, I, self.w1, pa, st, s)
+            L.moe_grouped_gemm(self.x_perm, self.offsets, E, R, d, I, self.w3, pc, st, s)
         L.moe_grouped_gemm_kn(b["dy_perm"], self.offsets, E, R, d, I, self.w2, None, b["dh"], st, s)
-        L.moe_swiglu_backward(b["dh"], b["a"], b["c"], R, I, b["dac"], None, s)
+        L.moe_swiglu_backward(b["dh"], pa, pc, R, I, b["dac"], None, s)
         L.moe_grouped_gemm_kn(b["dac"], self.offsets, E, R, 2 * I, d, self.w1, self.w3,
                               b["dx_perm"], st, s)
         mark("bwd_routed_dgrad", 1)
@@ -432,10 +463,14 @@ class MoELayer:
         mark("bwd_shared", 0)
         # shared experts: one group of all T tokens with gate 1
         so = self.shared_offsets
-        L.moe_grouped_gemm(x, so, 1, T, d, nI, self.ws1, b["a_s"], st, s)
-        L.moe_grouped_gemm(x, so, 1, T, d, nI, self.ws3, b["c_s"], st, s)
+        if self.training:
+            pa, pc = self.pre_a_sh, self.pre_c_sh
+        else:
+            pa, pc = b["a_s"], b["c_s"]
+            L.moe_grouped_gemm(x, so, 1, T, d, nI, self.ws1, pa, st, s)
+            L.moe_grouped_gemm(x, so, 1, T, d, nI, self.ws3, pc, st, s)
         L.moe_grouped_gemm_kn(dy, so, 1, T, d, nI, self.ws2, None, b["dh_s"], st, s)
-        L.moe_swiglu_backward(b["dh_s"], b["a_s"], b["c_s"], T, nI, b["dac_s"], None, s)
+        L.moe_swiglu_backward(b["dh_s"], pa, pc, T, nI, b["dac_s"], None, s)
         L.moe_grouped_gemm_kn(b["dac_s"], so, 1, T, 2 * nI, d, self.ws1, self.ws3, b["dx_s"], st, s)
         L.moe_grouped_gemm_wgrad(dy, self.h_sh, so, 1, T, d, nI, b["dws2"], st, s)
         L.moe_grouped_gemm_wgrad(b["dac_s"], x, so, 1, T, 2 * nI, d, b["dws13"], st, s)

@@ -166,6 +166,16 @@ moe_status moe_grouped_swiglu(const void* a_bf16, const int32_t* group_offsets, 
                               const void* w2_bf16, void* h_bf16, void* y_bf16,
                               int32_t* status_dev, moe_stream_t stream);
 
+/* The same call for a training step: also writes the pre-activations
+ * pre_a[r] = a[r] . w1[g]^T and pre_c[r] = a[r] . w3[g]^T (bf16 [R, I] each),
+ * which the backward pass needs (da = dh c silu'(a), dc = dh silu(a)), from
+ * the GEMM's own fp32 accumulators. */
+moe_status moe_grouped_swiglu_save(const void* a_bf16, const int32_t* group_offsets,
+                                   int n_groups, int R, int d, int I, const void* w1_bf16,
+                                   const void* w3_bf16, const void* w2_bf16, void* h_bf16,
+                                   void* y_bf16, void* pre_a_bf16, void* pre_c_bf16,
+                                   int32_t* status_dev, moe_stream_t stream);
+
 /* Step 4c, combine:
  *   out[t] = bf16( y_shared[t] + sum_k topk_gate[t,k] * y_perm[row_of[t,k]] )
  * accumulated in fp32 in rank order (y_shared may be NULL).  Gather form:

@@ -229,7 +229,7 @@ def test_combine_dx():
 
 
 # -------------------------------------------------------------------- layer
-def _layer_case(cfg, p, T=None):
+def _layer_case(cfg, p, T=None, training=True):
     """Forward + backward on the GPU; the oracle's own routing and gates.
     Tokens whose choice is a near tie for the oracle get dy = 0 on both
     sides, so they contribute nothing to any gradient."""
@@ -245,7 +245,8 @@ def _layer_case(cfg, p, T=None):
     kth, grp = ref.near_tie_tokens(s64, b, cfg.K, cfg.n_groups, cfg.topk_groups)
     tie = kth | grp
     dy[torch.from_numpy(tie)] = 0
-    layer = MoELayer(cfg, p, max_T=T, keep_affinity=True)
+    layer = (MoELayer(cfg, p, max_T=T, training=True) if training
+             else MoELayer(cfg, p, max_T=T, keep_affinity=True))
     layer.forward(x.cuda())
     g = layer.backward(x.cuda(), dy.cuda())
     torch.cuda.synchronize()
@@ -269,10 +270,13 @@ def _np(t):
     return bf16_to_np64(t) if t.dtype == torch.bfloat16 else t.numpy().astype(np.float64)
 
 
-def test_layer_backward_tiny_all_gradients():
+@pytest.mark.parametrize("training", [True, False])
+def test_layer_backward_tiny_all_gradients(training):
+    """training=True: the pre-activations come from the forward pass;
+    False: the backward recomputes them."""
     cfg = synth.CONFIGS["tiny"]
     p = synth.make_params(cfg, "cpu")
-    c = _layer_case(cfg, p)
+    c = _layer_case(cfg, p, training=training)
     host = HostExperts(p)
     want = B.moe_layer_bwd64(c["x64"], p["w_r"].numpy(), c["off"], c["idx64"], cfg.route_scale,
                              host, host.shared(), cfg.n_shared, c["dy64"])
@@ -309,7 +313,7 @@ def test_layer_backward_deterministic():
     p = synth.make_params(cfg, "cpu")
     x = synth.make_tokens(cfg, 0, "cuda")
     dy = synth.make_output_grad(cfg, 0, "cuda")
-    layer = MoELayer(cfg, p, keep_affinity=True)
+    layer = MoELayer(cfg, p, training=True)
     runs = []
     for _ in range(2):
         layer.forward(x)
@@ -350,3 +354,35 @@ def test_layer_backward_mid_sampled():
         assert ref.rel_l2(dw13[e, :cfg.I], dW1) < 1e-2, e
         assert ref.rel_l2(dw13[e, cfg.I:], dW3) < 1e-2, e
         assert ref.rel_l2(dw2[e], dW2) < 1e-2, e
+
+
+def test_forward_keeps_pre_activations():
+    """training=True: the forward writes a = v.W1^T and c = v.W3^T of every
+    dispatched row (bf16 of the GEMM's fp32 accumulators), and its output is
+    the inference forward's, bit for bit."""
+    cfg = synth.CONFIGS["tiny"]
+    p = synth.make_params(cfg, "cpu")
+    x = synth.make_tokens(cfg, 0, "cpu")
+    lt = MoELayer(cfg, p, training=True)
+    li = MoELayer(cfg, p)
+    yt = lt.forward(x.cuda()).clone()
+    yi = li.forward(x.cuda()).clone()
+    torch.cuda.synchronize()
+    assert torch.equal(yt.view(torch.int16), yi.view(torch.int16))
+    R = cfg.T * cfg.K
+    tok = lt.tok_of[:R].cpu().numpy()
+    off = lt.offsets.cpu().numpy()
+    expert = np.searchsorted(off, np.arange(R), side="right") - 1
+    x64 = bf16_to_np64(x)
+    host = HostExperts(p)
+    got_a, got_c = bf16_to_np64(lt.pre_a[:R]), bf16_to_np64(lt.pre_c[:R])
+    for e in np.unique(expert):
+        rows = np.nonzero(expert == e)[0]
+        W1, W3, _ = host(e)
+        want_a, want_c = x64[tok[rows]] @ W1.T, x64[tok[rows]] @ W3.T
+        scale = 1e-4 * np.sqrt(np.mean(want_a ** 2))
+        _close(got_a[rows], want_a, 2.0 ** -8, scale)
+        _close(got_c[rows], want_c, 2.0 ** -8, scale)
+    ws1, ws3, _ = host.shared()
+    _close(bf16_to_np64(lt.pre_a_sh[:cfg.T]), x64 @ ws1.T, 2.0 ** -8, 1e-4)
+    _close(bf16_to_np64(lt.pre_c_sh[:cfg.T]), x64 @ ws3.T, 2.0 ** -8, 1e-4)
