@@ -540,30 +540,25 @@ def run_train(args):
            for n in fnames + bnames}
     ms_step = ms / args.steps
 
-    # end to end: x and dy from pinned host memory, dx back, every step
+    # end to end through the public API (HostPipeline, train=True): every step
+    # copies x and dy from pinned host memory in and dx out, the copies of
+    # neighbouring steps overlapping this step's compute
     e2e = None
     if not args.no_e2e:
+        from expert_ffn_layer_affinity_b300.layer import HostPipeline
         x_host = [x.cpu().pin_memory() for x in xs]
         dy_host = [g.cpu().pin_memory() for g in dys]
-        dx_host = torch.empty(cfg.T, cfg.d, dtype=torch.bfloat16).pin_memory()
-        x_dev = torch.empty_like(xs[0])
-        dy_dev = torch.empty_like(dys[0])
-
-        def host_step(i):
-            x_dev.copy_(x_host[i % 2], non_blocking=True)
-            dy_dev.copy_(dy_host[i % 2], non_blocking=True)
-            layer.forward(x_dev)
-            g = layer.backward(x_dev, dy_dev)
-            layer.bias_update(cfg.T)
-            dx_host.copy_(g["dx"], non_blocking=True)
-
-        for i in range(2):
-            host_step(i)
+        dx_host = [torch.empty(cfg.T, cfg.d, dtype=torch.bfloat16).pin_memory() for _ in range(2)]
+        pipe = HostPipeline(layer, cfg.T, train=True)
+        for i in range(3):
+            pipe.step(i, x_host[i % 2], dx_host[i % 2], dy_host=dy_host[i % 2])
+        pipe.finish()
         torch.cuda.synchronize()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
         for i in range(args.steps):
-            host_step(i)
+            pipe.step(i, x_host[i % 2], dx_host[i % 2], dy_host=dy_host[i % 2])
+        pipe.finish()
         e1.record(stream)
         torch.cuda.synchronize()
         ems = e0.elapsed_time(e1)
@@ -571,8 +566,8 @@ def run_train(args):
         e2e = {"value": round(cfg.T * args.steps / (ems / 1e3), 1), "unit": "tokens/s",
                "h2d_bytes_per_step": 2 * nb, "d2h_bytes_per_step": nb,
                "ms_per_step": ems / args.steps,
-               "api": "MoELayer.forward + backward with x, dy copied in and dx copied out "
-                      "each step (weight gradients stay on the device)"}
+               "api": "HostPipeline(train=True): x and dy copied in, dx copied out each step, "
+                      "copies overlapping neighbouring steps (weight gradients stay on the device)"}
 
     pk = peaks()
     wg_bytes = backward_bytes(cfg)

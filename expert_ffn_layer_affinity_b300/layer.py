@@ -394,7 +394,7 @@ class MoELayer:
         )
 
     def backward(self, x: torch.Tensor, dy: torch.Tensor, stream=None,
-                 marks: dict | None = None) -> dict:
+                 marks: dict | None = None, dx_out: torch.Tensor | None = None) -> dict:
         """Gradients of <dy, layer(x)> for the experts the last forward(x)
         chose (that pass's routing, gates, dispatch order and expert outputs
         are reused; the bias and the selection take no gradient).  Needs a
@@ -412,7 +412,8 @@ class MoELayer:
         expert), dw2 fp32 [E, d, I], dws13 fp32 [2 nI, d], dws2 fp32 [d, nI],
         dgate fp32 [T, K], du fp32 [T, K].
 
-        `marks`, if given, maps part names ("bwd_combine", "bwd_routed_dgrad",
+        `dx_out`, if given, receives dx (bf16 [T, d]) instead of an internal
+        buffer.  `marks`, if given, maps part names ("bwd_combine", "bwd_routed_dgrad",
         "bwd_routed_wgrad", "bwd_shared", "bwd_router", "bwd_dx") to a pair
         of CUDA events recorded around that part."""
         if self.fp8 or self.shared_as_routed or self.n_redundant:
@@ -482,9 +483,10 @@ class MoELayer:
                               b["du_row"], b["dx_router"], b["dw_r"], s)
         mark("bwd_router", 1)
         mark("bwd_dx", 0)
-        L.moe_combine_dx(b["dx_perm"], self.row_of, K, b["dx_s"], b["dx_router"], T, d, b["dx"], s)
+        dx = b["dx"][:T] if dx_out is None else dx_out
+        L.moe_combine_dx(b["dx_perm"], self.row_of, K, b["dx_s"], b["dx_router"], T, d, dx, s)
         mark("bwd_dx", 1)
-        return dict(dx=b["dx"][:T], dw_r=b["dw_r"], dw13=b["dw13"], dw2=b["dw2"],
+        return dict(dx=dx, dw_r=b["dw_r"], dw13=b["dw13"], dw2=b["dw2"],
                     dws13=b["dws13"][0], dws2=b["dws2"][0], dgate=b["dgate"][:T], du=b["du"][:T])
 
 
@@ -495,31 +497,46 @@ class HostPipeline:
     both directions at once).  Every step still moves its whole input to the
     device and its whole output back; device buffers are double-buffered and
     ordered with events.  Usage: pipe.step(i, x_host, out_host) for i = 0, 1,
-    ...; pipe.finish() orders the caller's stream after the last copy out."""
+    ...; pipe.finish() orders the caller's stream after the last copy out.
 
-    def __init__(self, layer: MoELayer, T: int):
+    With train=True (a layer built with training=True) a step also copies in
+    the output gradient dy_host, runs forward, backward and the bias update,
+    and copies out dx into out_host; the weight gradients stay on the device
+    (returned by layer.backward into the layer's buffers)."""
+
+    def __init__(self, layer: MoELayer, T: int, train: bool = False):
         self.layer = layer
+        self.train = train
         dev = layer.device
         d = layer.cfg.d
         self.h2d = torch.cuda.Stream(device=dev)
         self.d2h = torch.cuda.Stream(device=dev)
         self.x_dev = [torch.empty(T, d, dtype=torch.bfloat16, device=dev) for _ in range(2)]
         self.out_dev = [torch.empty(T, d, dtype=torch.bfloat16, device=dev) for _ in range(2)]
+        self.dy_dev = ([torch.empty(T, d, dtype=torch.bfloat16, device=dev) for _ in range(2)]
+                       if train else None)
         self.ev_in = [torch.cuda.Event() for _ in range(2)]
         self.ev_done = [torch.cuda.Event() for _ in range(2)]
         self.ev_out = [torch.cuda.Event() for _ in range(2)]
 
     def step(self, i: int, x_host: torch.Tensor, out_host: torch.Tensor, group=None,
-             stats_out=None) -> None:
+             stats_out=None, dy_host: torch.Tensor | None = None) -> None:
         b = i % 2
         comp = torch.cuda.current_stream()
         self.h2d.wait_event(self.ev_done[b])         # step i-2 no longer reads x_dev[b]
         with torch.cuda.stream(self.h2d):
             self.x_dev[b].copy_(x_host, non_blocking=True)
+            if self.train:
+                self.dy_dev[b].copy_(dy_host, non_blocking=True)
         self.ev_in[b].record(self.h2d)
         comp.wait_event(self.ev_in[b])
         comp.wait_event(self.ev_out[b])              # step i-2's output has left out_dev[b]
-        self.layer.step(self.x_dev[b], group=group, stats_out=stats_out, out=self.out_dev[b])
+        if self.train:
+            self.layer.forward(self.x_dev[b])
+            self.layer.backward(self.x_dev[b], self.dy_dev[b], dx_out=self.out_dev[b])
+            self.layer.bias_update(self.x_dev[b].shape[0], group=group, stats_out=stats_out)
+        else:
+            self.layer.step(self.x_dev[b], group=group, stats_out=stats_out, out=self.out_dev[b])
         self.ev_done[b].record(comp)
         self.d2h.wait_event(self.ev_done[b])
         with torch.cuda.stream(self.d2h):
