@@ -45,35 +45,57 @@ __global__ void __launch_bounds__(kTile) count_kernel(const int32_t* __restrict_
 }
 
 // One block.  tile_counts [n_tiles, E] is turned in place into the first row
-// of each (tile, expert) in x_perm.
+// of each (tile, expert) in x_perm.  The tiles of each expert are split into
+// `segs` runs, one thread per (run, expert), so the column sums read many
+// tiles at once instead of walking all of them one after the other.
 __global__ void __launch_bounds__(1024) scan_kernel(int32_t* __restrict__ tile_counts, int n_tiles,
                                                     int E, int32_t* __restrict__ offsets) {
-  extern __shared__ int32_t total[];  // [E] totals, then offsets
+  extern __shared__ int32_t sm[];  // [segs][E] run sums -> run bases, then [E] expert bases
   __shared__ int32_t warp_sums[32];
-  for (int e = threadIdx.x; e < E; e += blockDim.x) {
-    int32_t run = 0;
-    for (int t = 0; t < n_tiles; ++t) {
-      int32_t* c = tile_counts + static_cast<size_t>(t) * E + e;
-      const int32_t v = *c;
-      *c = run;
-      run += v;
+  const int segs = blockDim.x / E;  // >= 1 (E <= 512 < 1024)
+  const int len = (n_tiles + segs - 1) / segs;
+  int32_t* run_sum = sm;
+  int32_t* base = sm + segs * E;
+  const int e = threadIdx.x % E, seg = threadIdx.x / E;
+  const bool active = seg < segs;
+  const int t0 = seg * len, t1 = min(n_tiles, t0 + len);
+  if (active) {
+    int32_t sum = 0;
+    for (int t = t0; t < t1; t += 8) {
+      int32_t v[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        v[j] = (t + j < t1) ? __ldcg(tile_counts + static_cast<size_t>(t + j) * E + e) : 0;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) sum += v[j];
     }
-    total[e] = run;
+    run_sum[seg * E + e] = sum;
   }
   __syncthreads();
-  // exclusive scan of total[0..E) in chunks of blockDim.x
+  // per expert: exclusive scan over its runs, and its total
+  for (int x = threadIdx.x; x < E; x += blockDim.x) {
+    int32_t run = 0;
+    for (int k = 0; k < segs; ++k) {
+      const int32_t v = run_sum[k * E + x];
+      run_sum[k * E + x] = run;
+      run += v;
+    }
+    base[x] = run;
+  }
+  __syncthreads();
+  // exclusive scan of the totals over experts in chunks of blockDim.x
   int32_t carry = 0;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
-  for (int base = 0; base < E; base += blockDim.x) {
-    const int e = base + threadIdx.x;
-    const int32_t v = (e < E) ? total[e] : 0;
-    int32_t x = v;
+  for (int b0 = 0; b0 < E; b0 += blockDim.x) {
+    const int x = b0 + threadIdx.x;
+    const int32_t v = (x < E) ? base[x] : 0;
+    int32_t incl = v;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-      const int32_t y = __shfl_up_sync(0xFFFFFFFFu, x, o);
-      if (lane >= o) x += y;
+      const int32_t y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+      if (lane >= o) incl += y;
     }
-    if (lane == 31) warp_sums[warp] = x;
+    if (lane == 31) warp_sums[warp] = incl;
     __syncthreads();
     if (warp == 0) {
       int32_t w = (lane < nw) ? warp_sums[lane] : 0;
@@ -85,10 +107,10 @@ __global__ void __launch_bounds__(1024) scan_kernel(int32_t* __restrict__ tile_c
       if (lane < nw) warp_sums[lane] = w;
     }
     __syncthreads();
-    const int32_t incl = x + (warp > 0 ? warp_sums[warp - 1] : 0) + carry;
-    if (e < E) {
-      offsets[e] = incl - v;
-      total[e] = incl - v;
+    incl += (warp > 0 ? warp_sums[warp - 1] : 0) + carry;
+    if (x < E) {
+      offsets[x] = incl - v;
+      base[x] = incl - v;
     }
     const int32_t chunk_total = warp_sums[nw - 1];
     __syncthreads();
@@ -96,9 +118,21 @@ __global__ void __launch_bounds__(1024) scan_kernel(int32_t* __restrict__ tile_c
   }
   if (threadIdx.x == 0) offsets[E] = carry;
   __syncthreads();
-  for (int e = threadIdx.x; e < E; e += blockDim.x) {
-    const int32_t off = total[e];
-    for (int t = 0; t < n_tiles; ++t) tile_counts[static_cast<size_t>(t) * E + e] += off;
+  // each (tile, expert) entry becomes its first row: expert base + run base
+  // + the counts of the earlier tiles of the run
+  if (active) {
+    int32_t run = base[e] + run_sum[seg * E + e];
+    for (int t = t0; t < t1; t += 8) {
+      int32_t v[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        v[j] = (t + j < t1) ? __ldcg(tile_counts + static_cast<size_t>(t + j) * E + e) : 0;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        if (t + j < t1) tile_counts[static_cast<size_t>(t + j) * E + e] = run;
+        run += v[j];
+      }
+    }
   }
 }
 
@@ -197,7 +231,8 @@ cudaError_t launch_permute(const int32_t* idx, int T, int K, int E, const uint16
   cudaError_t err;
   count_kernel<<<n_tiles, kTile, E * sizeof(int32_t), s>>>(idx, R, E, tile_counts, status);
   if ((err = cudaGetLastError()) != cudaSuccess) return err;
-  scan_kernel<<<1, 1024, E * sizeof(int32_t), s>>>(tile_counts, n_tiles, E, offsets);
+  scan_kernel<<<1, 1024, (1024 / E + 1) * E * sizeof(int32_t), s>>>(tile_counts, n_tiles, E,
+                                                                    offsets);
   if ((err = cudaGetLastError()) != cudaSuccess) return err;
   const size_t rank_smem = static_cast<size_t>(kTileWarps) * E * sizeof(int32_t);
   static bool attr_set[64] = {false};
