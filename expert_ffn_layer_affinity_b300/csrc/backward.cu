@@ -14,6 +14,7 @@
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 #include <cstdint>
+#include <type_traits>
 
 #include "internal.h"
 
@@ -52,6 +53,7 @@ __global__ void __launch_bounds__(256) combine_bwd_kernel(
       const uint4* yr = y_perm + static_cast<size_t>(r) * chunks;
       uint4* dr = dy_perm + static_cast<size_t>(r) * chunks;
       float acc = 0.0f;
+#pragma unroll 4
       for (int c = lane; c < chunks; c += 32) {
         const uint4 a = __ldg(dyr + c);
         const uint4 b = __ldcs(yr + c);
@@ -73,33 +75,54 @@ __global__ void __launch_bounds__(256) combine_bwd_kernel(
 
 // Elementwise SwiGLU backward: per row, dac = [da | dc] (2I columns) and the
 // recomputed h = silu(a) c (I columns; skipped when h is null), from dh, a,
-// c (I columns each).
+// c (I columns each).  8 columns (16 bytes of each input) per thread when
+// I % 8 == 0, else 2.
+template <int V>
 __global__ void __launch_bounds__(256) swiglu_bwd_kernel(
-    const uint32_t* __restrict__ dh, const uint32_t* __restrict__ a, const uint32_t* __restrict__ c,
-    long long R, int I, uint32_t* __restrict__ dac, uint32_t* __restrict__ h) {
-  const int half = I / 2;  // bf16 pairs per row
-  const long long n = R * half;
+    const uint16_t* __restrict__ dh, const uint16_t* __restrict__ a,
+    const uint16_t* __restrict__ c, long long R, int I, uint16_t* __restrict__ dac,
+    uint16_t* __restrict__ h) {
+  using Vec = typename std::conditional<V == 8, uint4, uint32_t>::type;
+  constexpr int W = V / 2;  // 32-bit words per vector
+  const int per_row = I / V;
+  const long long n = R * per_row;
   for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < n;
        i += static_cast<long long>(gridDim.x) * blockDim.x) {
-    const long long r = i / half;
-    const int j = static_cast<int>(i - r * half);
-    const uint32_t vh = __ldcs(dh + i), va = __ldcs(a + i), vc = __ldcs(c + i);
-    float da[2], dc[2], hh[2];
+    const long long r = i / per_row;
+    const int j = static_cast<int>(i - r * per_row) * V;  // first column
+    const size_t src = static_cast<size_t>(r) * I + j;
+    const Vec vh = __ldcs(reinterpret_cast<const Vec*>(dh + src));
+    const Vec va = __ldcs(reinterpret_cast<const Vec*>(a + src));
+    const Vec vc = __ldcs(reinterpret_cast<const Vec*>(c + src));
+    const uint32_t* wh = reinterpret_cast<const uint32_t*>(&vh);
+    const uint32_t* wa = reinterpret_cast<const uint32_t*>(&va);
+    const uint32_t* wc = reinterpret_cast<const uint32_t*>(&vc);
+    Vec oda, odc, oh;
+    uint32_t* pda = reinterpret_cast<uint32_t*>(&oda);
+    uint32_t* pdc = reinterpret_cast<uint32_t*>(&odc);
+    uint32_t* ph = reinterpret_cast<uint32_t*>(&oh);
 #pragma unroll
-    for (int e = 0; e < 2; ++e) {
-      const float g = e ? bf_hi(vh) : bf_lo(vh);
-      const float x = e ? bf_hi(va) : bf_lo(va);
-      const float u = e ? bf_hi(vc) : bf_lo(vc);
-      const float sig = 1.0f / (1.0f + expf(-x));
-      const float silu = x * sig;
-      da[e] = g * u * (sig * (1.0f + x * (1.0f - sig)));
-      dc[e] = g * silu;
-      hh[e] = silu * u;
+    for (int w = 0; w < W; ++w) {
+      float da[2], dc[2], hh[2];
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const float g = e ? bf_hi(wh[w]) : bf_lo(wh[w]);
+        const float x = e ? bf_hi(wa[w]) : bf_lo(wa[w]);
+        const float u = e ? bf_hi(wc[w]) : bf_lo(wc[w]);
+        const float sig = 1.0f / (1.0f + expf(-x));
+        const float silu = x * sig;
+        da[e] = g * u * (sig * (1.0f + x * (1.0f - sig)));
+        dc[e] = g * silu;
+        hh[e] = silu * u;
+      }
+      pda[w] = pack_bf2(da[0], da[1]);
+      pdc[w] = pack_bf2(dc[0], dc[1]);
+      ph[w] = pack_bf2(hh[0], hh[1]);
     }
-    uint32_t* drow = dac + r * I;  // 2I bf16 = I pairs per row
-    __stcs(drow + j, pack_bf2(da[0], da[1]));
-    __stcs(drow + half + j, pack_bf2(dc[0], dc[1]));
-    if (h) __stcs(h + i, pack_bf2(hh[0], hh[1]));
+    uint16_t* drow = dac + static_cast<size_t>(r) * 2 * I;
+    __stcs(reinterpret_cast<Vec*>(drow + j), oda);
+    __stcs(reinterpret_cast<Vec*>(drow + I + j), odc);
+    if (h) __stcs(reinterpret_cast<Vec*>(h + src), oh);
   }
 }
 
@@ -153,22 +176,35 @@ __global__ void __launch_bounds__(256) router_bwd_token_kernel(
 }
 
 // dw_r[e, c] = sum over the rows r of expert e (ascending) of du[row] x[tok_of[r], c].
-// One block per (expert, 256-column chunk); du_row[r] is du of the
-// (token, slot) that row r came from.
+// One block per (expert, 2048-column chunk), 8 columns (one 16-byte load of a
+// token row) per thread; du_row[r] is du of the (token, slot) that row r came
+// from.
 __global__ void __launch_bounds__(256) router_bwd_weight_kernel(
     const float* __restrict__ du_row, const int32_t* __restrict__ tok_of,
     const int32_t* __restrict__ offsets, const uint16_t* __restrict__ x, int d, int E,
     float* __restrict__ dw_r) {
   const int e = blockIdx.y;
-  const int c = blockIdx.x * blockDim.x + threadIdx.x;
+  const int c = (blockIdx.x * blockDim.x + threadIdx.x) * 8;
   if (e >= E || c >= d) return;
   const int r0 = offsets[e], r1 = offsets[e + 1];
-  float acc = 0.0f;
+  float acc[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) acc[j] = 0.0f;
+#pragma unroll 4
   for (int r = r0; r < r1; ++r) {
     const int t = __ldg(tok_of + r);
-    acc = fmaf(__ldg(du_row + r), __uint_as_float(static_cast<uint32_t>(__ldg(x + static_cast<size_t>(t) * d + c)) << 16), acc);
+    const float u = __ldg(du_row + r);
+    const uint4 v = __ldg(reinterpret_cast<const uint4*>(x + static_cast<size_t>(t) * d + c));
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      acc[2 * j] = fmaf(u, bf_lo(w[j]), acc[2 * j]);
+      acc[2 * j + 1] = fmaf(u, bf_hi(w[j]), acc[2 * j + 1]);
+    }
   }
-  dw_r[static_cast<size_t>(e) * d + c] = acc;
+  float4* out = reinterpret_cast<float4*>(dw_r + static_cast<size_t>(e) * d + c);
+  out[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+  out[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
 }
 
 // du by row of the dispatch order: du_row[row_of[t,k]] = du[t,k].
@@ -247,11 +283,16 @@ cudaError_t launch_combine_backward(const uint16_t* dy, const uint16_t* y_perm,
 cudaError_t launch_swiglu_backward(const uint16_t* dh, const uint16_t* a, const uint16_t* c, int R,
                                    int I, uint16_t* dac, uint16_t* h, cudaStream_t s) {
   if (R == 0) return cudaSuccess;
-  const long long n = static_cast<long long>(R) * (I / 2);
-  swiglu_bwd_kernel<<<grid_cap(n, 256, 16), 256, 0, s>>>(
-      reinterpret_cast<const uint32_t*>(dh), reinterpret_cast<const uint32_t*>(a),
-      reinterpret_cast<const uint32_t*>(c), R, I, reinterpret_cast<uint32_t*>(dac),
-      reinterpret_cast<uint32_t*>(h));
+  const bool wide = I % 8 == 0 && ((reinterpret_cast<uintptr_t>(dh) | reinterpret_cast<uintptr_t>(a) |
+                                     reinterpret_cast<uintptr_t>(c) | reinterpret_cast<uintptr_t>(dac) |
+                                     reinterpret_cast<uintptr_t>(h)) & 15u) == 0;
+  if (wide) {
+    const long long n = static_cast<long long>(R) * (I / 8);
+    swiglu_bwd_kernel<8><<<grid_cap(n, 256, 16), 256, 0, s>>>(dh, a, c, R, I, dac, h);
+  } else {
+    const long long n = static_cast<long long>(R) * (I / 2);
+    swiglu_bwd_kernel<2><<<grid_cap(n, 256, 16), 256, 0, s>>>(dh, a, c, R, I, dac, h);
+  }
   return cudaGetLastError();
 }
 
@@ -269,8 +310,8 @@ cudaError_t launch_router_backward(const float* dgate, const int32_t* idx, int l
   const long long n = static_cast<long long>(T) * K;
   scatter_rows_kernel<<<grid_cap(n, 256, 8), 256, 0, s>>>(du, row_of, n, du_row);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  router_bwd_weight_kernel<<<dim3((d + 255) / 256, E), 256, 0, s>>>(du_row, tok_of, offsets, x, d,
-                                                                     E, dw_r);
+  router_bwd_weight_kernel<<<dim3((d / 8 + 255) / 256, E), 256, 0, s>>>(du_row, tok_of, offsets, x,
+                                                                         d, E, dw_r);
   return cudaGetLastError();
 }
 

@@ -368,7 +368,8 @@ moe_status moe_router_backward(const float* dgate, const int32_t* topk_idx, int 
   if (!dw_r || (T > 0 && (!dgate || !topk_idx || !affinity || !w_r || !x_bf16 || !row_of ||
                           !tok_of || !expert_offsets || !du || !du_row)))
     return MOE_ERR_INVALID_ARG;
-  if (E > 65535) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (E > 65535 || d % 8 || !aligned16(dw_r) || (T > 0 && !aligned16(x_bf16)))
+    return MOE_ERR_UNSUPPORTED_SHAPE;
   return cuda_status(launch_router_backward(
       dgate, topk_idx, ldk, affinity, w_r, static_cast<const uint16_t*>(x_bf16), row_of, tok_of,
       expert_offsets, T, d, E, K, route_scale, du, du_row, dx_router, dw_r,

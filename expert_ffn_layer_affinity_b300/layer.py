@@ -238,6 +238,7 @@ class MoELayer:
         T = x.shape[0]
         K = self.K_slots
         R = T * K
+        self._fwd_T = T                               # what a backward call differentiates
         main = torch.cuda.current_stream() if stream is None else stream
 
         def mark(name, i, s=main):
@@ -425,6 +426,10 @@ class MoELayer:
         E, d, I, K, nI = c.E, c.d, c.I, c.K, c.n_shared * c.I
         T = x.shape[0]
         R = T * K
+        if getattr(self, "_fwd_T", None) != T:
+            raise ValueError("backward(x, dy) must follow forward(x) on the same tokens")
+        if dy.shape != x.shape or dy.dtype != torch.bfloat16 or not dy.is_contiguous():
+            raise ValueError("dy must be a contiguous bf16 tensor shaped like x")
         if getattr(self, "bwd", None) is None or self.bwd["T"] < T:
             self._alloc_backward(T)
         b = self.bwd

@@ -351,7 +351,8 @@ moe_status moe_grouped_gemm_wgrad(const void* a_bf16, const void* b_bf16,
  * affinities fp32 [T, E]; dx_router fp32 [T, d] = du . w_r (or NULL);
  * dw_r fp32 [E, d] = du^T x, summed per expert over its rows of the dispatch
  * order (row_of [T, K], tok_of [T*K], expert_offsets [E+1] from moe_permute).
- * du_row fp32 [T*K]: scratch.  x bf16 [T, d], w_r fp32 [E, d]. */
+ * du_row fp32 [T*K]: scratch.  x bf16 [T, d], w_r fp32 [E, d]; d % 8 == 0,
+ * x and dw_r 16-byte aligned. */
 moe_status moe_router_backward(const float* dgate, const int32_t* topk_idx, int ldk,
                                const float* affinity, const float* w_r, const void* x_bf16,
                                const int32_t* row_of, const int32_t* tok_of,

@@ -386,3 +386,17 @@ def test_forward_keeps_pre_activations():
     ws1, ws3, _ = host.shared()
     _close(bf16_to_np64(lt.pre_a_sh[:cfg.T]), x64 @ ws1.T, 2.0 ** -8, 1e-4)
     _close(bf16_to_np64(lt.pre_c_sh[:cfg.T]), x64 @ ws3.T, 2.0 ** -8, 1e-4)
+
+
+@pytest.mark.parametrize("R,I", [(37, 70), (129, 8), (1, 2)])
+def test_swiglu_backward_narrow_and_small(R, I):
+    """Widths that are not a multiple of 8 take the two-column path."""
+    dh, a, c = _bf16((R, I), 51), _bf16((R, I), 52, 3.0), _bf16((R, I), 53)
+    dac = torch.empty(R, 2 * I, dtype=torch.bfloat16, device="cuda")
+    moe.moe_swiglu_backward(dh.cuda(), a.cuda(), c.cuda(), R, I, dac, None)
+    torch.cuda.synchronize()
+    dh64, a64, c64 = bf16_to_np64(dh), bf16_to_np64(a), bf16_to_np64(c)
+    got = bf16_to_np64(dac)
+    scale = 1e-6 * max(np.abs(dh64 * c64).max(), 1e-30)
+    _close(got[:, :I], dh64 * c64 * B.silu_deriv64(a64), 2.0 ** -7, scale)
+    _close(got[:, I:], dh64 * ref.silu64(a64), 2.0 ** -7, scale)
