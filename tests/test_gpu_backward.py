@@ -400,3 +400,31 @@ def test_swiglu_backward_narrow_and_small(R, I):
     scale = 1e-6 * max(np.abs(dh64 * c64).max(), 1e-30)
     _close(got[:, :I], dh64 * c64 * B.silu_deriv64(a64), 2.0 ** -7, scale)
     _close(got[:, I:], dh64 * ref.silu64(a64), 2.0 ** -7, scale)
+
+
+@pytest.mark.parametrize("T", [1, 3, 129])
+def test_layer_backward_odd_token_counts(T):
+    """Few tokens: most experts get no rows, the rest ragged tails of 1..3
+    rows; every gradient against the oracle."""
+    cfg = synth.CONFIGS["tiny"]
+    p = synth.make_params(cfg, "cpu")
+    c = _layer_case(cfg, p, T=T)
+    host = HostExperts(p)
+    want = B.moe_layer_bwd64(c["x64"], p["w_r"].numpy(), c["off"], c["idx64"], cfg.route_scale,
+                             host, host.shared(), cfg.n_shared, c["dy64"])
+    g = c["g"]
+    assert ref.rel_l2(_np(g["dx"]), want["dx"]) < 1e-2
+    assert ref.rel_l2(_np(g["dw_r"]), want["dw_r"]) < 1e-2 or not np.any(want["dw_r"])
+    I = cfg.I
+    dw13, dw2 = _np(g["dw13"]), _np(g["dw2"])
+    for e in range(cfg.E):
+        if e in want["experts"]:
+            w1, w3, w2 = want["experts"][e]
+            assert ref.rel_l2(np.concatenate([dw13[e].ravel(), dw2[e].ravel()]),
+                              np.concatenate([w1.ravel(), w3.ravel(), w2.ravel()])) < 1e-2, e
+        else:
+            assert not np.any(dw13[e]) and not np.any(dw2[e]), e
+    s1, s3, s2 = want["shared"]
+    nI = cfg.n_shared * I
+    assert ref.rel_l2(_np(g["dws13"])[:nI], s1) < 1e-2
+    assert ref.rel_l2(_np(g["dws2"]), s2) < 1e-2
