@@ -95,6 +95,9 @@ cudaError_t launch_grouped_swiglu_fp8_small(const uint8_t* a_q, int ld_as, const
                                             const CUtensorMap& th2, const CUtensorMap& tsw2,
                                             cudaStream_t s);
 
+// ---- self-test of the bounded device wait (selftest.cu)
+cudaError_t launch_wait_selftest(unsigned long long limit_ns, int32_t* status, cudaStream_t s);
+
 // ---- backward (backward.cu, gemm_wgrad.cu, gemm_tc.cu)
 cudaError_t launch_grouped_gemm_kn(const uint16_t* a, const int32_t* offsets, int G, int R, int K,
                                    int N, const uint16_t* w0, int K0, const uint16_t* w1,

@@ -281,6 +281,13 @@ moe_status moe_grouped_swiglu_fp8(const void* a_q, const float* a_s, int ld_as,
       static_cast<uint16_t*>(y_bf16), status_dev, static_cast<cudaStream_t>(stream)));
 }
 
+// ------------------------------------------------------------ self-test
+moe_status moe_wait_selftest(long long limit_ns, int32_t* status_dev, moe_stream_t stream) {
+  if (!status_dev || limit_ns < 1000 || limit_ns > 1000000000ll) return MOE_ERR_INVALID_ARG;
+  return cuda_status(launch_wait_selftest(static_cast<unsigned long long>(limit_ns), status_dev,
+                                          static_cast<cudaStream_t>(stream)));
+}
+
 // ------------------------------------------------------------------ backward
 moe_status moe_combine_backward(const void* dy_bf16, const void* y_perm_bf16,
                                 const int32_t* row_of, const float* gate, int T, int K, int d,

@@ -353,6 +353,55 @@ class MoELayer:
             T_total *= T
         stats = self.stats if stats_out is None else stats_out
         L.moe_bias_update(self.load, self.bias, T_total, c.K, c.E, c.gamma, stats, stream)
+        self.updates = getattr(self, "updates", 0) + 1
+
+    # ------------------------------------------------------------ state
+    def state_dict(self) -> dict:
+        """The layer's mutable state: the per-expert bias, the number of bias
+        updates applied, and the replica plan of a serving layout (host
+        tensors; synchronises the device)."""
+        st = {"bias": self.bias.detach().cpu().clone(), "updates": getattr(self, "updates", 0)}
+        if self.n_redundant:
+            st["slot_start"] = self.slot_start.cpu().clone()
+            st["slots"] = self.slots.cpu().clone()
+        return st
+
+    def load_state_dict(self, st: dict) -> None:
+        """Restore a state_dict(): the bias bit for bit, then the replica plan
+        (re-placing the copies' weights)."""
+        if st["bias"].shape != self.bias.shape or st["bias"].dtype != self.bias.dtype:
+            raise ValueError("bias of a different shape or type")
+        self.bias.copy_(st["bias"])
+        self.updates = int(st.get("updates", 0))
+        if self.n_redundant:
+            if "slot_start" not in st:
+                raise ValueError("state without the replica plan of this serving layout")
+            ss, sl = st["slot_start"], st["slots"]
+            E = self.cfg.E
+            owner = torch.repeat_interleave(torch.arange(E, dtype=torch.int32),
+                                            (ss[1:] - ss[:-1]).to(torch.int64))
+            used = sl[:int(ss[E])]
+            # re-place the copies exactly as recorded: copy r serves the expert
+            # whose slot range holds physical id E + r (an unused copy stays)
+            for r in range(self.n_redundant):
+                at = (used == E + r).nonzero()
+                if at.numel() == 0:
+                    continue
+                e = int(owner[int(at[0])])
+                self.w1[E + r].copy_(self.w1[e])
+                self.w3[E + r].copy_(self.w3[e])
+                self.w2[E + r].copy_(self.w2[e])
+                if self.fp8:
+                    for t in (self.w13_q, self.w13_s, self.w2_q, self.w2_s):
+                        t[E + r].copy_(t[e])
+            self.slot_start = ss.to(self.device)
+            self.slots = sl.to(self.device)
+
+    def save_state(self, path: str) -> None:
+        torch.save(self.state_dict(), path)
+
+    def load_state(self, path: str) -> None:
+        self.load_state_dict(torch.load(path, map_location="cpu", weights_only=True))
 
     def step(self, x: torch.Tensor, stream=None, group=None, marks=None,
              stats_out=None, out: torch.Tensor | None = None) -> torch.Tensor:

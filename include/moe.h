@@ -290,6 +290,13 @@ moe_status moe_grouped_swiglu_fp8(const void* a_q, const float* a_s, int ld_as,
                                   const float* w2_s, void* h_bf16, void* h_q, float* h_s,
                                   void* y_bf16, int32_t* status_dev, moe_stream_t stream);
 
+/* Failure detection self-test: one small kernel waits, with the bounded wait
+ * every pipelined kernel here uses, on a barrier nothing arrives on.  After
+ * limit_ns (1 us .. 1 s) it records MOE_DEV_TIMEOUT in status_dev (DEVICE,
+ * OR-ed in) and returns; the context stays usable.  Lets a caller check that
+ * a stalled pipeline surfaces as a status instead of a hang. */
+moe_status moe_wait_selftest(long long limit_ns, int32_t* status_dev, moe_stream_t stream);
+
 /* ---------------------------------------------------------- backward pass
  * Gradients of the layer output for a fixed choice of experts.  The bias only
  * chooses experts and never enters a gate value ("Bias 仅用于路由",

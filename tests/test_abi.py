@@ -157,3 +157,9 @@ def test_backward_calls_reject_bad_arguments():
                                    1.0, FAKE, FAKE, None, FAKE, **args) == E_ARG
     # combine_dx: d % 8
     assert moe.moe_combine_dx(FAKE, FAKE, 2, None, None, 4, 12, FAKE, **args) == E_SHAPE
+
+
+def test_wait_selftest_rejects_bad_limits():
+    assert moe.moe_wait_selftest(0, FAKE, stream=0, check=False) == moe.MOE_ERR_INVALID_ARG
+    assert moe.moe_wait_selftest(2_000_000_000, FAKE, stream=0, check=False) == moe.MOE_ERR_INVALID_ARG
+    assert moe.moe_wait_selftest(1_000_000, None, stream=0, check=False) == moe.MOE_ERR_INVALID_ARG
