@@ -4,7 +4,18 @@
 #include <cstdint>
 #include <cstring>
 
+#include <nvtx3/nvToolsExt.h>
 #include "internal.h"
+
+namespace {
+// An NVTX range around every entry point, named after it: a profiler shows
+// which call each kernel belongs to; without one attached it costs a check.
+struct Trace {
+  explicit Trace(const char* name) { nvtxRangePushA(name); }
+  ~Trace() { nvtxRangePop(); }
+};
+}  // namespace
+#define MOE_TRACE() Trace moe_trace_(__func__)
 #include "../../include/moe.h"
 
 namespace moe {
@@ -71,6 +82,7 @@ size_t moe_workspace_bytes(int T, int d, int E, int K, int I) {
 
 moe_status moe_router_prepare(const float* w_r, int E, int d, void* w_split_bf16,
                               moe_stream_t stream) {
+  MOE_TRACE();
   if (!w_r || !w_split_bf16 || E < 1 || d < 1) return MOE_ERR_INVALID_ARG;
   if (d % 64 || E > 512) return MOE_ERR_UNSUPPORTED_SHAPE;
   return cuda_status(launch_router_split(w_r, E, d, static_cast<uint16_t*>(w_split_bf16),
@@ -84,6 +96,7 @@ moe_status moe_router_topk(const void* x_bf16, const void* w_split_bf16, const f
                            int32_t* expert_load,
                            float* affinity_out, int32_t* status_dev, void* ws, size_t ws_bytes,
                            moe_stream_t stream) {
+  MOE_TRACE();
   if (!bias || !expert_load || T < 0) return MOE_ERR_INVALID_ARG;
   if (T > 0 && (!topk_idx || !topk_gate)) return MOE_ERR_INVALID_ARG;
   if (!routing_shape_ok(T, E, K, n_groups, topk_groups)) return MOE_ERR_UNSUPPORTED_SHAPE;
@@ -129,6 +142,7 @@ moe_status moe_permute(const int32_t* topk_idx, int T, int K, int E, const void*
                        int32_t* expert_offsets, int32_t* row_of, int32_t* tok_of,
                        void* x_perm_bf16, int32_t* status_dev, void* ws, size_t ws_bytes,
                        moe_stream_t stream) {
+  MOE_TRACE();
   if (T < 0 || K < 1 || E < 1 || !expert_offsets) return MOE_ERR_INVALID_ARG;
   if (T > 0 && (!topk_idx || !row_of || !tok_of)) return MOE_ERR_INVALID_ARG;
   if (E > 512 || K > 32 || static_cast<long long>(T) * K >= (1ll << 31))
@@ -152,6 +166,7 @@ moe_status moe_permute(const int32_t* topk_idx, int T, int K, int E, const void*
 moe_status moe_permute_static(const int32_t* topk_idx, int T, int K, int E, const void* x_bf16,
                               int d, int32_t* expert_offsets, int32_t* row_of, int32_t* tok_of,
                               void* x_perm_bf16, int32_t* status_dev, moe_stream_t stream) {
+  MOE_TRACE();
   if (T < 0 || K < 1 || E < 1 || !expert_offsets) return MOE_ERR_INVALID_ARG;
   if (T > 0 && (!topk_idx || !row_of || !tok_of)) return MOE_ERR_INVALID_ARG;
   if (E > 512 || K > 32 || static_cast<long long>(T) * K >= (1ll << 31))
@@ -178,6 +193,7 @@ moe_status moe_grouped_swiglu(const void* a_bf16, const int32_t* group_offsets, 
                               int R, int d, int I, const void* w1_bf16, const void* w3_bf16,
                               const void* w2_bf16, void* h_bf16, void* y_bf16,
                               int32_t* status_dev, moe_stream_t stream) {
+  MOE_TRACE();
   if (R < 0 || n_groups < 1 || d < 1 || I < 1) return MOE_ERR_INVALID_ARG;
   if (R > 0 && (!a_bf16 || !group_offsets || !w1_bf16 || !w3_bf16 || !w2_bf16 || !h_bf16 ||
                 !y_bf16))
@@ -198,6 +214,7 @@ moe_status moe_grouped_swiglu_save(const void* a_bf16, const int32_t* group_offs
                                    const void* w3_bf16, const void* w2_bf16, void* h_bf16,
                                    void* y_bf16, void* pre_a_bf16, void* pre_c_bf16,
                                    int32_t* status_dev, moe_stream_t stream) {
+  MOE_TRACE();
   if (R > 0 && (!pre_a_bf16 || !pre_c_bf16)) return MOE_ERR_INVALID_ARG;
   if (R > 0 && (!aligned16(pre_a_bf16) || !aligned16(pre_c_bf16))) return MOE_ERR_UNSUPPORTED_SHAPE;
   if (R < 0 || n_groups < 1 || d < 1 || I < 1) return MOE_ERR_INVALID_ARG;
@@ -219,6 +236,7 @@ moe_status moe_grouped_swiglu_save(const void* a_bf16, const int32_t* group_offs
 // ------------------------------------------------------------------ FP8 path
 moe_status moe_quantize_fp8(const void* x_bf16, int rows, int cols, void* q_out, float* s_out,
                             int ld_s, moe_stream_t stream) {
+  MOE_TRACE();
   if (rows < 0 || cols < 1 || ld_s < rows) return MOE_ERR_INVALID_ARG;
   if (rows > 0 && (!x_bf16 || !q_out || !s_out)) return MOE_ERR_INVALID_ARG;
   if (cols % 128) return MOE_ERR_UNSUPPORTED_SHAPE;
@@ -233,6 +251,7 @@ moe_status moe_quantize_fp8(const void* x_bf16, int rows, int cols, void* q_out,
 moe_status moe_quantize_weights_fp8(const void* w_bf16, const void* w_pair_bf16, int groups,
                                     int rows, int cols, void* q_out, float* s_out,
                                     moe_stream_t stream) {
+  MOE_TRACE();
   if (groups < 0 || rows < 1 || cols < 1) return MOE_ERR_INVALID_ARG;
   if (groups > 0 && (!w_bf16 || !q_out || !s_out)) return MOE_ERR_INVALID_ARG;
   if (rows % 128 || cols % 128) return MOE_ERR_UNSUPPORTED_SHAPE;
@@ -248,6 +267,7 @@ moe_status moe_quantize_weights_fp8(const void* w_bf16, const void* w_pair_bf16,
 moe_status moe_permute_fp8(const void* q_in, const float* s_in, int ld_in, int T, int K, int d,
                            const int32_t* row_of, void* q_perm, float* s_perm, int ld_out,
                            moe_stream_t stream) {
+  MOE_TRACE();
   if (T < 0 || K < 1 || d < 1 || ld_in < T) return MOE_ERR_INVALID_ARG;
   if (static_cast<long long>(T) * K >= (1ll << 31) || static_cast<long long>(ld_out) < 1ll * T * K)
     return MOE_ERR_INVALID_ARG;
@@ -264,6 +284,7 @@ moe_status moe_grouped_swiglu_fp8(const void* a_q, const float* a_s, int ld_as,
                                   const void* w13_q, const float* w13_s, const void* w2_q,
                                   const float* w2_s, void* h_bf16, void* h_q, float* h_s,
                                   void* y_bf16, int32_t* status_dev, moe_stream_t stream) {
+  MOE_TRACE();
   if (R < 0 || n_groups < 1 || d < 1 || I < 1 || ld_as < R) return MOE_ERR_INVALID_ARG;
   if (R > 0 && (!a_q || !a_s || !group_offsets || !w13_q || !w13_s || !w2_q || !w2_s ||
                 !h_bf16 || !h_q || !h_s || !y_bf16))
@@ -283,6 +304,7 @@ moe_status moe_grouped_swiglu_fp8(const void* a_q, const float* a_s, int ld_as,
 
 // ------------------------------------------------------------ self-test
 moe_status moe_wait_selftest(long long limit_ns, int32_t* status_dev, moe_stream_t stream) {
+  MOE_TRACE();
   if (!status_dev || limit_ns < 1000 || limit_ns > 1000000000ll) return MOE_ERR_INVALID_ARG;
   return cuda_status(launch_wait_selftest(static_cast<unsigned long long>(limit_ns), status_dev,
                                           static_cast<cudaStream_t>(stream)));
@@ -292,6 +314,7 @@ moe_status moe_wait_selftest(long long limit_ns, int32_t* status_dev, moe_stream
 moe_status moe_combine_backward(const void* dy_bf16, const void* y_perm_bf16,
                                 const int32_t* row_of, const float* gate, int T, int K, int d,
                                 void* dy_perm_bf16, float* dgate, moe_stream_t stream) {
+  MOE_TRACE();
   if (T < 0 || K < 1 || K > 32 || d < 1) return MOE_ERR_INVALID_ARG;
   if (T > 0 && (!dy_bf16 || !y_perm_bf16 || !row_of || !gate || !dy_perm_bf16 || !dgate))
     return MOE_ERR_INVALID_ARG;
@@ -305,6 +328,7 @@ moe_status moe_combine_backward(const void* dy_bf16, const void* y_perm_bf16,
 
 moe_status moe_swiglu_backward(const void* dh_bf16, const void* a_bf16, const void* c_bf16, int R,
                                int I, void* dac_bf16, void* h_bf16, moe_stream_t stream) {
+  MOE_TRACE();
   if (R < 0 || I < 1) return MOE_ERR_INVALID_ARG;
   if (R > 0 && (!dh_bf16 || !a_bf16 || !c_bf16 || !dac_bf16)) return MOE_ERR_INVALID_ARG;
   if (I % 2) return MOE_ERR_UNSUPPORTED_SHAPE;
@@ -321,6 +345,7 @@ moe_status moe_swiglu_backward(const void* dh_bf16, const void* a_bf16, const vo
 moe_status moe_grouped_gemm(const void* a_bf16, const int32_t* group_offsets, int n_groups, int R,
                             int K, int N, const void* w_bf16, void* out_bf16, int32_t* status_dev,
                             moe_stream_t stream) {
+  MOE_TRACE();
   if (R < 0 || n_groups < 1 || K < 1 || N < 1) return MOE_ERR_INVALID_ARG;
   if (R > 0 && (!a_bf16 || !group_offsets || !w_bf16 || !out_bf16)) return MOE_ERR_INVALID_ARG;
   if (K % 64 || N % 8 || n_groups > 512) return MOE_ERR_UNSUPPORTED_SHAPE;
@@ -335,6 +360,7 @@ moe_status moe_grouped_gemm(const void* a_bf16, const int32_t* group_offsets, in
 moe_status moe_grouped_gemm_kn(const void* a_bf16, const int32_t* group_offsets, int n_groups,
                                int R, int K, int N, const void* w0_bf16, const void* w1_bf16,
                                void* out_bf16, int32_t* status_dev, moe_stream_t stream) {
+  MOE_TRACE();
   if (R < 0 || n_groups < 1 || K < 1 || N < 1) return MOE_ERR_INVALID_ARG;
   if (R > 0 && (!a_bf16 || !group_offsets || !w0_bf16 || !out_bf16)) return MOE_ERR_INVALID_ARG;
   const int K0 = w1_bf16 ? K / 2 : K;
@@ -351,6 +377,7 @@ moe_status moe_grouped_gemm_kn(const void* a_bf16, const int32_t* group_offsets,
 moe_status moe_grouped_gemm_wgrad(const void* a_bf16, const void* b_bf16,
                                   const int32_t* group_offsets, int n_groups, int R, int M, int N,
                                   float* out, int32_t* status_dev, moe_stream_t stream) {
+  MOE_TRACE();
   if (R < 0 || n_groups < 1 || M < 1 || N < 1) return MOE_ERR_INVALID_ARG;
   if (!group_offsets || !out || (R > 0 && (!a_bf16 || !b_bf16))) return MOE_ERR_INVALID_ARG;
   if (M % 8 || N % 8 || n_groups > 65535) return MOE_ERR_UNSUPPORTED_SHAPE;
@@ -371,6 +398,7 @@ moe_status moe_router_backward(const float* dgate, const int32_t* topk_idx, int 
                                const int32_t* expert_offsets, int T, int d, int E, int K,
                                float route_scale, float* du, float* du_row, float* dx_router,
                                float* dw_r, moe_stream_t stream) {
+  MOE_TRACE();
   if (T < 0 || d < 1 || E < 1 || K < 1 || K > 32 || K > E || ldk < K) return MOE_ERR_INVALID_ARG;
   if (!dw_r || (T > 0 && (!dgate || !topk_idx || !affinity || !w_r || !x_bf16 || !row_of ||
                           !tok_of || !expert_offsets || !du || !du_row)))
@@ -386,6 +414,7 @@ moe_status moe_router_backward(const float* dgate, const int32_t* topk_idx, int 
 moe_status moe_combine_dx(const void* dx_perm_bf16, const int32_t* row_of, int K,
                           const void* dx_shared_bf16, const float* dx_router, int T, int d,
                           void* dx_bf16, moe_stream_t stream) {
+  MOE_TRACE();
   if (T < 0 || K < 1 || d < 1) return MOE_ERR_INVALID_ARG;
   if (T > 0 && (!dx_perm_bf16 || !row_of || !dx_bf16)) return MOE_ERR_INVALID_ARG;
   if (d % 8) return MOE_ERR_UNSUPPORTED_SHAPE;
@@ -401,6 +430,7 @@ moe_status moe_combine_dx(const void* dx_perm_bf16, const int32_t* row_of, int K
 moe_status moe_replica_plan(const int32_t* load_host, int E, int n_redundant,
                             int32_t* slot_start_host, int32_t* slots_host,
                             int32_t* expert_of_slot_host) {
+  MOE_TRACE();
   if (!load_host || !slot_start_host || !slots_host || !expert_of_slot_host || E < 1 ||
       n_redundant < 0)
     return MOE_ERR_INVALID_ARG;
@@ -413,6 +443,7 @@ moe_status moe_replica_plan(const int32_t* load_host, int E, int n_redundant,
 moe_status moe_replica_remap(const int32_t* topk_idx, int T, int K, int E, int n_redundant,
                              const int32_t* slot_start, const int32_t* slots, int32_t* phys_idx,
                              moe_stream_t stream) {
+  MOE_TRACE();
   if (T < 0 || K < 1 || E < 1 || n_redundant < 0) return MOE_ERR_INVALID_ARG;
   if (T > 0 && (!topk_idx || !slot_start || !slots || !phys_idx)) return MOE_ERR_INVALID_ARG;
   return cuda_status(launch_replica_remap(topk_idx, T, K, E, n_redundant, slot_start, slots,
@@ -422,6 +453,7 @@ moe_status moe_replica_remap(const int32_t* topk_idx, int T, int K, int E, int n
 moe_status moe_combine(const void* y_perm_bf16, const int32_t* row_of, const float* topk_gate,
                        const void* y_shared_bf16, int T, int K, int d, void* out_bf16,
                        moe_stream_t stream) {
+  MOE_TRACE();
   if (T < 0 || K < 1 || d < 1) return MOE_ERR_INVALID_ARG;
   if (T > 0 && (!y_perm_bf16 || !row_of || !topk_gate || !out_bf16)) return MOE_ERR_INVALID_ARG;
   if (d % 8 || K > 32) return MOE_ERR_UNSUPPORTED_SHAPE;
@@ -437,6 +469,7 @@ moe_status moe_combine(const void* y_perm_bf16, const int32_t* row_of, const flo
 moe_status moe_seq_balance_loss(const float* scores, const int32_t* topk_idx, int ldk,
                                 const int32_t* seq_offsets, int S, int E, int K, float alpha,
                                 float* loss_out, moe_stream_t stream) {
+  MOE_TRACE();
   if (S < 0 || E < 1 || K < 1 || ldk < K) return MOE_ERR_INVALID_ARG;
   if (S > 0 && (!scores || !topk_idx || !seq_offsets || !loss_out)) return MOE_ERR_INVALID_ARG;
   if (E > 512 || K > 32) return MOE_ERR_UNSUPPORTED_SHAPE;
@@ -446,6 +479,7 @@ moe_status moe_seq_balance_loss(const float* scores, const int32_t* topk_idx, in
 
 moe_status moe_bias_update(const int32_t* expert_load, float* bias, int T, int K, int E,
                            float gamma, float* stats_out, moe_stream_t stream) {
+  MOE_TRACE();
   if (!expert_load || !bias || T < 0 || K < 1 || E < 1) return MOE_ERR_INVALID_ARG;
   if (E > 1024) return MOE_ERR_UNSUPPORTED_SHAPE;
   return cuda_status(launch_bias_update(expert_load, bias, T, K, E, gamma, stats_out,
