@@ -32,10 +32,10 @@ CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.a
                 "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
                 "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 # DRAM bytes (read + write) per routed expert of the two expert-GEMM launches,
-# from ncu dram__bytes on the 16-expert profiling case (profiles/gemm_pair_v3e16.md),
-# scaled by the experts a launch processes.  Must be re-measured when those
-# kernels change.
-GEMM_TRAFFIC_PER_EXPERT = (1.042742e9 + 16.753152e6 + 0.497552e9 + 48.797696e6) / 16
+# from ncu dram__bytes on the 16-expert profiling case (profiles/gemm_pair_v3e16.md,
+# "Re-measured DRAM traffic"), scaled by the experts a launch processes.  Must be
+# re-measured when those kernels change.
+GEMM_TRAFFIC_PER_EXPERT = (1.042927872e9 + 16.49152e6 + 0.493063424e9 + 44.88576e6) / 16
 KERNELS_PER_STEP = 12  # router GEMM, selection, 4 permute, 2+2 grouped GEMM, combine, bias update
 # backward: combine 1; routed: dh GEMM, SwiGLU, dv GEMM, 2 weight-gradient GEMMs; shared:
 # the same 5; router 3; input gradient 1 (the forward keeps the pre-activations)
