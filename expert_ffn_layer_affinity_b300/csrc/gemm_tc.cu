@@ -134,6 +134,8 @@ struct GemmParams {
   int w_part_kb;         // DGRAD: k-blocks from tmA, the rest from tmA2
   void* out_a;           // SWIGLU: also store the pre-activations a and c (or nullptr)
   void* out_c;
+  int splits;            // ROUTER: the k-blocks of a tile split over this many CTAs (>= 1)
+  float* partial;        // ROUTER, splits > 1: raw logit sums [splits][R][ldo]
   void* out;
   int ldo;               // output row stride in elements
   const float* col_offset;  // router: per-expert logit offset or nullptr
@@ -219,7 +221,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem_base = *tmem_slot;
 
   const int NT = (p.N + C::kColTile - 1) / C::kColTile;
-  const int total = mt_prefix[G] * NT;
+  // the router may split a tile's k-blocks over `splits` work items (whole
+  // chunks of kRouterChunkKb each); item w is (tile w / splits, split w % splits)
+  const int splits = (MODE == MODE_ROUTER && p.splits > 1) ? p.splits : 1;
+  const int total = mt_prefix[G] * NT * splits;
+  const int split_kb = (MODE == MODE_ROUTER)
+                           ? ((p.num_kb + kRouterChunkKb - 1) / kRouterChunkKb + splits - 1) / splits *
+                                 kRouterChunkKb
+                           : p.num_kb;
+  auto kb_range = [&](int w, int& kb_lo, int& kb_hi) {
+    const int sp = w % splits;
+    kb_lo = sp * split_kb;
+    kb_hi = kb_lo + split_kb < p.num_kb ? kb_lo + split_kb : p.num_kb;
+  };
   const int chunk_kb = (MODE == MODE_ROUTER) ? kRouterChunkKb : p.num_kb;
   const int num_st = (p.num_kb + C::kBoxes - 1) / C::kBoxes;           // stages per tile
   const int chunk_st = (MODE == MODE_ROUTER) ? kRouterChunkKb : num_st;  // stages per TMEM unit
@@ -232,8 +246,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t it = 0;
       bool ok = true;
       for (int w = unit_id; w < total && ok; w += n_units) {
-        int g, n, m;
-        decode_work(w, NT, mt_prefix, G, g, n, m);
+        int g, n, m, kb_lo, kb_hi;
+        decode_work(w / splits, NT, mt_prefix, G, g, n, m);
+        kb_range(w, kb_lo, kb_hi);
         const int rows_g = row_start[g + 1] - row_start[g];
         int tok_row = row_start[g] + m * C::kTokTile;
         int w_row = g * p.w_rows_per_group + n * C::kColTile;
@@ -241,7 +256,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tok_row += static_cast<int>(rank) * (tile_n(rows_g - m * C::kTokTile, C::kTokTile) / 2);
           w_row += static_cast<int>(rank) * (MODE == MODE_SWIGLU ? 64 : 128);
         }
-        for (int st = 0; st < num_st; ++st, ++it) {
+        for (int st = kb_lo; st < kb_hi; ++st, ++it) {
           const int s = static_cast<int>(it % S);
           const uint32_t ph = (it / S) & 1u;
           if (!mbar_wait(empty_bar(s), ph ^ 1u, abort_flag, p.status)) {
@@ -301,8 +316,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t it = 0, unit = 0;
       bool ok = true, issued = false;
       for (int w = unit_id; w < total && ok; w += n_units) {
-        int g, n, m;
-        decode_work(w, NT, mt_prefix, G, g, n, m);
+        int g, n, m, kb_lo, kb_hi;
+        decode_work(w / splits, NT, mt_prefix, G, g, n, m);
+        kb_range(w, kb_lo, kb_hi);
         uint32_t idesc;
         if (MODE == MODE_ROUTER) {
           idesc = umma_idesc_bf16(128, C::kColTile);
@@ -311,7 +327,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           idesc = umma_idesc_bf16(256, tile_n(rows_g - m * C::kTokTile, C::kTokTile)) |
                   (MODE == MODE_DGRAD ? (1u << 15) : 0u);  // A (weights) MN-major
         }
-        for (int st0 = 0; st0 < num_st && ok; st0 += chunk_st, ++unit) {
+        for (int st0 = kb_lo; st0 < kb_hi && ok; st0 += chunk_st, ++unit) {
           const int b = static_cast<int>(unit % NB);
           const uint32_t bph = (unit / NB) & 1u;
           if (!mbar_wait(acce_bar(b), bph ^ 1u, abort_flag, p.status)) {
@@ -320,7 +336,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tc_fence_after();
           const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(b * C::kBufCols);
-          const int st1 = (st0 + chunk_st < num_st) ? st0 + chunk_st : num_st;
+          const int st1 = (st0 + chunk_st < kb_hi) ? st0 + chunk_st : kb_hi;
           for (int st = st0; st < st1; ++st, ++it) {
             const int s = static_cast<int>(it % S);
             const uint32_t ph = (it / S) & 1u;
@@ -371,15 +387,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t unit = 0, xchunk = 0;
     bool ok = true;
     for (int w = unit_id; w < total && ok; w += n_units) {
-      int g, n, m;
-      decode_work(w, NT, mt_prefix, G, g, n, m);
+      int g, n, m, kb_lo, kb_hi;
+      decode_work(w / splits, NT, mt_prefix, G, g, n, m);
+      kb_range(w, kb_lo, kb_hi);
       const int rows_g = row_start[g + 1] - row_start[g];
       const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
       if (MODE == MODE_ROUTER) {
         float acc[128];
 #pragma unroll
         for (int i = 0; i < 128; ++i) acc[i] = 0.0f;
-        for (int kb0 = 0; kb0 < p.num_kb; kb0 += chunk_kb, ++unit) {
+        for (int kb0 = kb_lo; kb0 < kb_hi; kb0 += chunk_kb, ++unit) {
           const int b = static_cast<int>(unit % NB);
           const uint32_t bph = (unit / NB) & 1u;
           ok = __all_sync(0xFFFFFFFFu, mbar_wait(accf_bar(b), bph, abort_flag, p.status));
@@ -400,15 +417,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok) break;
         const int row_local = m * 128 + q * 32 + lane;
         if (row_local < rows_g && row_local < p.R) {
-          float* out = reinterpret_cast<float*>(p.out) + static_cast<long long>(row_local) * p.ldo;
           const int col0 = n * 128;
+          if (splits > 1) {
+            // this split's sum of its chunk partials; router_finish adds the
+            // splits in order, then the offset and the sigmoid
+            float* out = p.partial + (static_cast<long long>(w % splits) * p.R + row_local) * p.ldo;
 #pragma unroll
-          for (int i = 0; i < 128; ++i) {
-            const int cc = col0 + i;
-            if (cc < p.N) {
-              float u = acc[i];
-              if (p.col_offset) u = __fadd_rn(u, p.col_offset[cc]);
-              out[cc] = 1.0f / (1.0f + expf(-u));
+            for (int i = 0; i < 128; ++i)
+              if (col0 + i < p.N) out[col0 + i] = acc[i];
+          } else {
+            float* out = reinterpret_cast<float*>(p.out) + static_cast<long long>(row_local) * p.ldo;
+#pragma unroll
+            for (int i = 0; i < 128; ++i) {
+              const int cc = col0 + i;
+              if (cc < p.N) {
+                float u = acc[i];
+                if (p.col_offset) u = __fadd_rn(u, p.col_offset[cc]);
+                out[cc] = 1.0f / (1.0f + expf(-u));
+              }
             }
           }
         }
@@ -659,9 +685,35 @@ cudaError_t launch_grouped_gemm_kn(const uint16_t* a, const int32_t* offsets, in
   return launch_gemm<MODE_DGRAD>(tw0, tw1, ta, p, mt * ((N + 255) / 256), s);
 }
 
+namespace {
+// scores[t, e] = sigmoid(sum over the splits, in order, of partial[s, t, e] + o[e])
+__global__ void __launch_bounds__(256) router_finish_kernel(const float* __restrict__ partial,
+                                                            int splits, long long n, int E,
+                                                            const float* __restrict__ offset,
+                                                            float* __restrict__ scores) {
+  for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < n;
+       i += static_cast<long long>(gridDim.x) * blockDim.x) {
+    float u = partial[i];
+    for (int sp = 1; sp < splits; ++sp) u = __fadd_rn(u, partial[sp * n + i]);
+    if (offset) u = __fadd_rn(u, offset[i % E]);
+    scores[i] = 1.0f / (1.0f + expf(-u));
+  }
+}
+}  // namespace
+
+int router_splits(int T, int d, int E, int sms) {
+  const int units = ((T + 127) / 128) * ((E + 127) / 128);
+  const int chunks = (3 * d / BK + kRouterChunkKb - 1) / kRouterChunkKb;
+  int sp = units >= sms ? 1 : sms / units;
+  if (sp > chunks) sp = chunks;
+  if (sp < 1) sp = 1;
+  const int per = (chunks + sp - 1) / sp;  // no empty split
+  return (chunks + per - 1) / per;
+}
+
 cudaError_t launch_router_gemm(const uint16_t* x, const uint16_t* w_split, const float* offset,
                                int T, int d, int E, float* scores, int32_t* status,
-                               cudaStream_t s) {
+                               cudaStream_t s, float* partial, size_t partial_bytes) {
   if (T == 0) return cudaSuccess;
   CUtensorMap ta, tb;
   if (!make_map(&ta, x, d, T, 128) || !make_map(&tb, w_split, 3ull * d, E, 128))
@@ -679,8 +731,21 @@ cudaError_t launch_router_gemm(const uint16_t* x, const uint16_t* w_split, const
   p.ldo = E;
   p.col_offset = offset;
   p.status = status;
-  const int works = ((T + 127) / 128) * ((E + 127) / 128);
-  return launch_gemm<MODE_ROUTER>(ta, ta, tb, p, works, s);
+  // small batches fill the GPU by splitting each tile's reduction
+  int splits = router_splits(T, d, E, sm_count());
+  const size_t need = static_cast<size_t>(splits) * T * E * sizeof(float);
+  if (splits > 1 && (partial == nullptr || partial_bytes < need)) splits = 1;
+  p.splits = splits;
+  p.partial = splits > 1 ? partial : nullptr;
+  const int works = ((T + 127) / 128) * ((E + 127) / 128) * splits;
+  cudaError_t e = launch_gemm<MODE_ROUTER>(ta, ta, tb, p, works, s);
+  if (e != cudaSuccess || splits == 1) return e;
+  const long long n = static_cast<long long>(T) * E;
+  long long blocks = (n + 255) / 256;
+  if (blocks > 148 * 8) blocks = 148 * 8;
+  router_finish_kernel<<<static_cast<int>(blocks), 256, 0, s>>>(partial, splits, n, E, offset,
+                                                                 scores);
+  return cudaGetLastError();
 }
 
 }  // namespace moe

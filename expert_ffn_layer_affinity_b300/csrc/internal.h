@@ -59,9 +59,12 @@ cudaError_t launch_seq_balance(const float* scores, const int32_t* idx, int ldk,
 // ---- tensor-core GEMMs (gemm_tc.cu)
 // Router logits + sigmoid: s[t, e] = sigmoid(sum_j x[t,j] w[e,j] + o[e]) with
 // w given as the exact bf16 split [E, 3d].
+// Router GEMM; with `partial` (a caller scratch of partial_bytes) small batches
+// split each tile's reduction over several CTAs (router_splits of them).
+int router_splits(int T, int d, int E, int sms);
 cudaError_t launch_router_gemm(const uint16_t* x, const uint16_t* w_split, const float* offset,
                                int T, int d, int E, float* scores, int32_t* status,
-                               cudaStream_t s);
+                               cudaStream_t s, float* partial = nullptr, size_t partial_bytes = 0);
 // Grouped SwiGLU experts (GEMM1 + fused SwiGLU, then GEMM2).
 cudaError_t launch_grouped_swiglu(const uint16_t* a, const int32_t* offsets, int G, int R, int d,
                                   int I, const uint16_t* w1, const uint16_t* w3,

@@ -48,6 +48,19 @@ moe_status cuda_status(cudaError_t e) {
 // Workspace layout: [router scores T*E fp32][permute tile counts].
 size_t ws_router_bytes(int T, int E) { return align_up(static_cast<size_t>(T) * E * sizeof(float)); }
 
+// Scratch of the router GEMM's split reduction (small batches): at most
+// splits * T * E floats with splits * ceil(T/128) * ceil(E/128) <= the SM
+// count (bounded by 160 here) and splits <= the 4-k-block chunks of 3d.  It
+// shares the workspace region after the scores with the permute's counts:
+// the router's reduction is finished before the permute runs.
+size_t ws_router_partial_bound(int T, int d, int E) {
+  if (d < 64) return 0;
+  const long long chunks = (3ll * d / 64 + 3) / 4;
+  long long n = 160ll * 128 * 128;
+  if (chunks * T * E < n) n = chunks * T * E;
+  return align_up(static_cast<size_t>(n) * sizeof(float));
+}
+
 bool routing_shape_ok(int T, int E, int K, int G, int M) {
   if (T < 0 || E < 1 || E > 512 || K < 1 || K > E || K > 32) return false;
   if (G < 1 || M < 1 || M > G || E % G) return false;
@@ -74,10 +87,11 @@ extern "C" {
 int moe_abi_version(void) { return 1; }
 
 size_t moe_workspace_bytes(int T, int d, int E, int K, int I) {
-  (void)d;
   (void)I;
   if (T < 0 || E < 1 || K < 1) return 0;
-  return ws_router_bytes(T, E) + align_up(permute_ws_bytes(T, K, E));
+  const size_t perm = align_up(permute_ws_bytes(T, K, E));
+  const size_t part = ws_router_partial_bound(T, d, E);
+  return ws_router_bytes(T, E) + (perm > part ? perm : part);
 }
 
 moe_status moe_router_prepare(const float* w_r, int E, int d, void* w_split_bf16,
@@ -113,9 +127,18 @@ moe_status moe_router_topk(const void* x_bf16, const void* w_split_bf16, const f
       if (!ws || ws_bytes < ws_router_bytes(T, E)) return MOE_ERR_WORKSPACE;
       buf = static_cast<float*>(ws);
     }
+    // the split reduction's scratch follows the scores region (when the
+    // workspace has room; otherwise the GEMM runs unsplit)
+    float* partial = nullptr;
+    size_t partial_bytes = 0;
+    if (ws && ws_bytes > ws_router_bytes(T, E)) {
+      partial = reinterpret_cast<float*>(static_cast<char*>(ws) + ws_router_bytes(T, E));
+      partial_bytes = ws_bytes - ws_router_bytes(T, E);
+    }
     const cudaError_t e = launch_router_gemm(static_cast<const uint16_t*>(x_bf16),
                                              static_cast<const uint16_t*>(w_split_bf16),
-                                             logit_offset, T, d, E, buf, status_dev, s);
+                                             logit_offset, T, d, E, buf, status_dev, s, partial,
+                                             partial_bytes);
     if (e != cudaSuccess) return cuda_status(e);
     scores = buf;
   } else if (scores_in == nullptr && T > 0) {

@@ -65,7 +65,9 @@ int moe_abi_version(void);
 
 /* Bytes of device workspace the calls below need for a layer of this shape
  * (the caller allocates it once; 256-byte aligned).  Covers the router's
- * affinity buffer (T*E fp32) and the permute's per-tile expert counts. */
+ * affinity buffer (T*E fp32), then, in one shared region, the router GEMM's
+ * split-reduction scratch (small T: each output tile's reduction spread over
+ * several CTAs) and the permute's per-tile expert counts. */
 size_t moe_workspace_bytes(int T, int d, int E, int K, int I);
 
 /* One-time router weight preparation: splits fp32 w_r [E, d] exactly into
@@ -102,7 +104,9 @@ moe_status moe_router_prepare(const float* w_r, int E, int d, void* w_split_bf16
  * Fp32 rule (bit-exact against a reference fed the same s): z = s + b; group
  *  score = top1 + top2 (+ ...); denom = s_1 + s_2 + ... in rank order;
  *  g = (s_k / denom) * scale, each one IEEE fp32 operation.
- * Workspace: `ws` of `ws_bytes` >= moe_workspace_bytes(...). */
+ * Workspace: `ws` of `ws_bytes` >= moe_workspace_bytes(...); with x given and
+ *  a smaller workspace (or none next to affinity_out) the router GEMM runs
+ *  without splitting its reduction. */
 moe_status moe_router_topk(const void* x_bf16, const void* w_split_bf16,
                            const float* scores_in, const float* logit_offset,
                            const float* bias, int T, int d, int E, int K,
