@@ -81,6 +81,13 @@ def load_config(name):
     return synth.CONFIGS[name]
 
 
+def router_extra(cfg):
+    """1 when the router GEMM splits its reduction (a small kernel then adds
+    the splits), else 0."""
+    from expert_ffn_layer_affinity_b300 import _lib as L
+    return 1 if L.moe_router_splits(cfg.T, cfg.d, cfg.E) > 1 else 0
+
+
 def peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -419,7 +426,7 @@ def run_ours(args):
         "hbm_kernels": {n: {"gbs": kernels[n]["gbs"],
                             "frac": round(kernels[n]["gbs"] / pk["hbm"], 4)}
                         for n in ("permute", "combine")},
-        "gpu_launches": (KERNELS_PER_STEP + 3 * fp8
+        "gpu_launches": (KERNELS_PER_STEP + router_extra(cfg) + 3 * fp8
                          - (3 if fp8 else 2) * bool(args.shared_as_routed)
                          + bool(args.redundant)) * args.steps,
         "device_status": status,
@@ -602,7 +609,7 @@ def run_train(args):
                      "peak_kind": f"HBM copy, {pk['src']}",
                      "bytes_per_launch_pair": wg_bytes},
         "kernels": kernels,
-        "gpu_launches": (KERNELS_PER_STEP + KERNELS_PER_BACKWARD) * args.steps,
+        "gpu_launches": (KERNELS_PER_STEP + router_extra(cfg) + KERNELS_PER_BACKWARD) * args.steps,
         "device_status": status,
         "clocks": clk,
         "e2e": e2e,

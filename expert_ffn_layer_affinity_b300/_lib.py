@@ -52,6 +52,7 @@ SIGNATURES = {
     "moe_grouped_swiglu_fp8": (I, [P, P, I, P, I, I, I, I, P, P, P, P, P, P, P, P, P, P]),
     "moe_grouped_swiglu_save": (I, [P, P, I, I, I, I, P, P, P, P, P, P, P, P, P]),
     "moe_wait_selftest": (I, [LL, P, P]),
+    "moe_router_splits": (I, [I, I, I]),
     "moe_combine_backward": (I, [P, P, P, P, I, I, I, P, P, P]),
     "moe_swiglu_backward": (I, [P, P, P, I, I, P, P, P]),
     "moe_grouped_gemm": (I, [P, P, I, I, I, I, P, P, P, P]),
@@ -293,3 +294,7 @@ def moe_combine_dx(dx_perm, row_of, K, dx_shared, dx_router, T, d, dx, stream=No
 def moe_wait_selftest(limit_ns, status_dev, stream=None, check=True):
     r = lib().moe_wait_selftest(int(limit_ns), _ptr(status_dev), _stream(stream))
     return _check("moe_wait_selftest", r) if check else r
+
+
+def moe_router_splits(T, d, E):
+    return int(lib().moe_router_splits(T, d, E))

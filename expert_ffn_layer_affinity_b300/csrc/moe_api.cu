@@ -94,6 +94,11 @@ size_t moe_workspace_bytes(int T, int d, int E, int K, int I) {
   return ws_router_bytes(T, E) + (perm > part ? perm : part);
 }
 
+int moe_router_splits(int T, int d, int E) {
+  if (T < 1 || d < 64 || E < 1) return 1;
+  return router_splits(T, d, E, sm_count());
+}
+
 moe_status moe_router_prepare(const float* w_r, int E, int d, void* w_split_bf16,
                               moe_stream_t stream) {
   MOE_TRACE();

@@ -70,6 +70,11 @@ int moe_abi_version(void);
  * several CTAs) and the permute's per-tile expert counts. */
 size_t moe_workspace_bytes(int T, int d, int E, int K, int I);
 
+/* How many CTAs share each output tile's reduction in the router GEMM of
+ * moe_router_topk on the current device (1: no split; above 1 one more small
+ * kernel adds the splits).  Host-only query. */
+int moe_router_splits(int T, int d, int E);
+
 /* One-time router weight preparation: splits fp32 w_r [E, d] exactly into
  * three bf16 parts hi + mid + lo (each the bf16 rounding of the remainder),
  * stored side by side as w_split [E, 3*d] bf16, so the tensor-core router
