@@ -63,7 +63,8 @@ R8  Sequence-wise balance loss (the pages keep "a tiny-weight sequence-wise
     them); the pins fix the function against this reading.
 
 Function-level parity status: every function below is pinned by the CPU test
-suite (brute force, closed forms, invariants).  seq_balance_loss follows a
+suite (brute force, closed forms, invariants, hand-worked cases: load_stats
+and both branches of near_tie_tokens included).  seq_balance_loss follows a
 reading (R8) whose formula the pages do not print: parity unpinned against
 the pages, pinned against the reading.
 """
@@ -248,7 +249,10 @@ def seq_balance_loss(s, idx, seq_offsets, K, alpha):
 
 
 def load_stats(load):
-    """(max, mean, max/mean, coefficient of variation) of the loads."""
+    """(max, mean, max/mean, coefficient of variation) of the loads, taken
+    over all E experts (untouched ones count as load 0).  The coefficient of
+    variation is the population standard deviation (divide by E) over the
+    mean; with no load at all every statistic is 0."""
     l = np.asarray(load, dtype=F64)
     mean = l.mean()
     mx = l.max()

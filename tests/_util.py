@@ -8,8 +8,10 @@ from oracle import moe_ref as ref
 
 
 def bf16_to_np64(t: torch.Tensor) -> np.ndarray:
-    """Exact float64 values of a bf16 tensor."""
-    return ref.bf16_to_f64(t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16))
+    """Exact float64 values of a bf16 tensor (widening bf16 to float64 is
+    exact; tests/test_util_pins.py checks this against the oracle's
+    bit-pattern decoding)."""
+    return t.detach().cpu().to(torch.float64).numpy()
 
 
 def f32_bits(a) -> np.ndarray:
@@ -47,9 +49,11 @@ class HostExperts:
         return f8ref.quantize_expert(*self.shared())
 
 
-def check_pass(cfg, p, x, layer, out, sample=None, bias=None, fp8=False):
-    """Compare one pass: routing on every token, output on `sample` tokens
-    (against the FP8 reading of the experts when fp8=True)."""
+def route_check(cfg, p, x, layer, bias=None):
+    """The GPU's expert choice for every token of the pass against the
+    oracle's fp64 routing (with the bias the GPU used).  Returns the oracle's
+    x64, idx64, gate64, the near-tie masks kth / grp, the mismatch mask and
+    `bad`: mismatched tokens that are not near-tie (must be empty)."""
     T = x.shape[0]
     x64 = bf16_to_np64(x)
     off = p["logit_offset"].cpu().numpy() if p["logit_offset"] is not None else None
@@ -60,7 +64,18 @@ def check_pass(cfg, p, x, layer, out, sample=None, bias=None, fp8=False):
     kth, grp = ref.near_tie_tokens(s64, b, cfg.K, cfg.n_groups, cfg.topk_groups)
     gidx = layer.idx[:T, :cfg.K].cpu().numpy()
     mism = np.any(np.sort(gidx, 1) != np.sort(idx64, 1), axis=1)
-    assert not np.any(mism & ~(kth | grp)), np.nonzero(mism & ~(kth | grp))[0][:10]
+    return dict(x64=x64, idx64=idx64, gate64=gate64, kth=kth, grp=grp, mism=mism,
+                bad=np.nonzero(mism & ~(kth | grp))[0])
+
+
+def check_pass(cfg, p, x, layer, out, sample=None, bias=None, fp8=False):
+    """Compare one pass: routing on every token, output on `sample` tokens
+    (against the FP8 reading of the experts when fp8=True)."""
+    T = x.shape[0]
+    rc = route_check(cfg, p, x, layer, bias)
+    x64, idx64, gate64 = rc["x64"], rc["idx64"], rc["gate64"]
+    kth, grp, mism = rc["kth"], rc["grp"], rc["mism"]
+    assert len(rc["bad"]) == 0, rc["bad"][:10]
     tokens = np.arange(T) if sample is None else sample
     tokens = tokens[~mism[tokens]]
     host = HostExperts(p)
@@ -73,7 +88,44 @@ def check_pass(cfg, p, x, layer, out, sample=None, bias=None, fp8=False):
     err = ref.rel_l2(got, want)
     assert err < 1e-2, err
     return dict(rel_l2=err, mismatched_tokens=int(mism.sum()), near_tie=int((kth | grp).sum()),
-                idx64=idx64)
+                near_tie_kth=int(kth.sum()), near_tie_grp=int(grp.sum()),
+                mismatched_kth=int((mism & kth).sum()), mismatched_grp_only=int((mism & grp & ~kth).sum()),
+                checked_tokens=int(len(tokens)), idx64=idx64)
+
+
+def output_sample(rc, n, seed):
+    """Tokens whose layer output is checked: `n` seeded-random tokens of the
+    pass plus every near-tie token (K-th gap or group gap below 1e-5 in the
+    oracle's fp64 scores), minus the tokens whose experts differ (a counted
+    near-tie flip: the GPU then ran other experts for them)."""
+    T = len(rc["mism"])
+    rnd = np.random.default_rng(seed).choice(T, min(n, T), replace=False)
+    tok = np.union1d(rnd, np.nonzero(rc["kth"] | rc["grp"])[0])
+    return tok[~rc["mism"][tok]]
+
+
+def oracle_outputs(requests, host, n_shared):
+    """The oracle's layer output (reading R6) for several passes that share
+    one set of expert weights, in ONE call of the oracle on the stacked token
+    rows (rows are independent, so this equals one call per pass; each
+    expert's weights are then fetched once).  requests: list of
+    (x64 rows, idx64 rows, gate64 rows).  Returns one array per request."""
+    X = np.concatenate([r[0] for r in requests], axis=0)
+    IDX = np.concatenate([r[1] for r in requests], axis=0)
+    GATE = np.concatenate([r[2] for r in requests], axis=0)
+    Y = ref.moe_output64(X, IDX, GATE, host, host.shared(), n_shared)
+    out, a = [], 0
+    for r in requests:
+        out.append(Y[a:a + len(r[0])])
+        a += len(r[0])
+    return out
+
+
+def describe(r) -> str:
+    return (f"rel_l2={r['rel_l2']:.3e} checked={r['checked_tokens']} "
+            f"near_tie kth={r['near_tie_kth']} grp={r['near_tie_grp']} "
+            f"mismatched={r['mismatched_tokens']} (kth {r['mismatched_kth']}, "
+            f"group-gap only {r['mismatched_grp_only']})")
 
 
 def sign_rule_holds(load, b_before, b_after, T, K, E, gamma) -> bool:
@@ -101,6 +153,8 @@ class Trajectory:
         self.b = np.asarray(bias0, dtype=np.float32).copy()
         self.diverged_at = None
         self.near_tie_mismatches = 0
+        self.mismatches_kth = 0
+        self.mismatches_grp_only = 0
 
     def step(self, step, T, s64, gpu_idx, gpu_load, gpu_b_before, gpu_b_after):
         c = self.cfg
@@ -113,6 +167,8 @@ class Trajectory:
         mism = np.any(np.sort(gpu_idx, 1) != np.sort(idx64, 1), axis=1)
         assert not np.any(mism & ~(kth | grp)), np.nonzero(mism & ~(kth | grp))[0][:10]
         self.near_tie_mismatches += int(mism.sum())
+        self.mismatches_kth += int((mism & kth).sum())
+        self.mismatches_grp_only += int((mism & grp & ~kth).sum())
         load = ref.expert_load(idx64, c.E)
         new_b = ref.bias_update(load, self.b, T, c.K, c.E, c.gamma)
         if np.array_equal(load, np.asarray(gpu_load)):

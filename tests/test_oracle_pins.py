@@ -314,6 +314,73 @@ def test_near_tie_detection():
     assert not kth[0]
 
 
+# Hand-built biased scores z for the group-limited rule with E = 12 experts in
+# G = 4 groups of 3, M = 2 groups kept, K = 4 (so a group's score is the sum of
+# its 2 largest z, reading R1).  Every value is dyadic, so each sum and gap
+# below is exact in fp64 and the group scores are worked out by hand:
+#   token 0  group scores 0.75, 0.1875, 1.8125, 0.75 - 2^-18 -> 2nd vs 3rd
+#            group gap 2^-18 (< 1e-5): group near-tie.  The kept groups are 2
+#            and 0; among their experts the 4th and 5th z are 0.25 and 0.125.
+#   token 1  the same with the gap 2^-15 (> 1e-5): no group near-tie, although
+#            the two groups' LARGEST members tie exactly (0.5 and 0.5).
+#   token 2  kept groups 0 and 1; 4th vs 5th among their experts 0.5 vs
+#            0.0625, while the best expert of a DROPPED group (group 2) is
+#            0.5 - 2^-18: that candidate must not count as the (K+1)-th.
+#   token 3  4th vs 5th among the kept groups' experts 0.5 vs 0.5 - 2^-18.
+_NT_Z = np.array([
+    [0.5, 0.25, 0.125, 0.125, 0.0625, 0.03125, 0.9375, 0.875, 0.0625,
+     0.5, 0.25 - 2.0**-18, 0.0078125],
+    [0.5, 0.25, 0.0, 0.125, 0.0625, 0.03125, 0.9375, 0.875, 0.0,
+     0.5, 0.25 - 2.0**-15, 0.0],
+    [0.9375, 0.875, 0.0625, 0.75, 0.5, 0.0, 0.5 - 2.0**-18, 0.125, 0.0,
+     0.25, 0.125, 0.0],
+    [0.9375, 0.875, 0.0625, 0.75, 0.5, 0.5 - 2.0**-18, 0.25, 0.125, 0.0,
+     0.125, 0.0625, 0.0],
+])
+
+
+def test_near_tie_group_gap_and_eligible_kth_gap():
+    """The group-gap branch and the K-th gap among eligible experts only
+    (node-limited routing: at most M groups per token -- chenshi221 notes,
+    "Auxiliary-loss-free 负载均衡")."""
+    want_grp = [True, False, False, False]
+    want_kth = [False, False, False, True]
+    kth, grp = ref.near_tie_tokens(_NT_Z, np.zeros(12), 4, n_groups=4, topk_groups=2)
+    assert grp.tolist() == want_grp
+    assert kth.tolist() == want_kth
+    # the masks look at z = s + b: a dyadic bias moved into s gives the same z
+    b = np.tile(np.array([0.03125, -0.0625, 0.0]), 4)
+    kth_b, grp_b = ref.near_tie_tokens(_NT_Z - b[None, :], b.astype(np.float32), 4,
+                                       n_groups=4, topk_groups=2)
+    assert grp_b.tolist() == want_grp and kth_b.tolist() == want_kth
+    # the kept groups of tokens 0 and 2 are the hand-worked ones
+    idx, _ = ref.select_experts(_NT_Z, np.zeros(12), 4, 4, 2, precision="fp64")
+    assert sorted({int(e) // 3 for e in idx[0]}) == [0, 2]
+    assert sorted({int(e) // 3 for e in idx[2]}) == [0, 1]
+    # without a group limit only the plain K-th gap exists: for token 2 the
+    # 5th-best z overall is the 0.5 - 2^-18 that the group limit had excluded
+    kth1, grp1 = ref.near_tie_tokens(_NT_Z, np.zeros(12), 4)
+    assert kth1[2] and not grp1.any()
+
+
+def test_load_stats_handworked():
+    """max, mean, max/mean and the coefficient of variation (population
+    standard deviation over the mean, over ALL experts, untouched ones too)
+    of per-expert loads."""
+    # [0, 2, 2, 4]: mean 2, max 4, deviations -2, 0, 0, 2 -> variance 8/4 = 2
+    np.testing.assert_allclose(ref.load_stats([0, 2, 2, 4]),
+                               [4.0, 2.0, 2.0, math.sqrt(2.0) / 2.0], rtol=0, atol=1e-15)
+    # all load on one of E experts: mean 3/E, max/mean = E, CV = sqrt(E - 1)
+    for E in (2, 6, 256):
+        load = np.zeros(E, dtype=np.int32)
+        load[E // 2] = 3
+        np.testing.assert_allclose(ref.load_stats(load), [3.0, 3.0 / E, E, math.sqrt(E - 1)],
+                                   rtol=1e-14, atol=0)
+    # perfectly even loads: max/mean 1, CV 0; no load at all: zeros, not NaN
+    np.testing.assert_array_equal(ref.load_stats([5, 5, 5]), [5.0, 5.0, 1.0, 0.0])
+    np.testing.assert_array_equal(ref.load_stats([0, 0, 0, 0]), [0.0, 0.0, 0.0, 0.0])
+
+
 def test_seq_balance_loss_closed_forms():
     rng = np.random.default_rng(13)
     E, K, alpha = 8, 2, 1e-4
