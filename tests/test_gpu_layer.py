@@ -8,7 +8,8 @@ import torch
 from expert_ffn_layer_affinity_b300 import synth
 from expert_ffn_layer_affinity_b300.layer import MoELayer
 from oracle import moe_ref as ref
-from _util import Trajectory, bf16_to_np64, check_pass, f32_bits, sign_rule_holds
+from _util import (Trajectory, bf16_to_np64, check_pass, describe, f32_bits, output_sample,
+                   route_check, sign_rule_holds)
 
 pytestmark = pytest.mark.gpu
 
@@ -76,22 +77,41 @@ def test_mid_layer_one_pass_sampled(mid):
     check_pass(cfg, p, x, layer, out, sample=sample)
 
 
+MID_OUTPUT_STEPS = (0, 25, 49)
+
+
 def test_mid_layer_feedback_steps(mid):
-    """Several bias-feedback steps with fresh tokens: the GPU's routing, loads
-    and bias against the oracle's own trajectory (see Trajectory)."""
+    """All 50 bias-feedback steps of the mid workload (Zipf-skewed router,
+    fresh tokens every step) through the full layer: the GPU's routing, loads
+    and bias against the oracle's own trajectory (see Trajectory) on every
+    step, and the layer output on 256 + near-tie tokens at steps 0, 25 and 49
+    (with the bias the GPU used at that step)."""
     cfg, p = mid
     layer = MoELayer(cfg, p)
     traj = Trajectory(cfg, p["bias"].numpy())
-    ratios = []
-    for step in range(6):
+    ratios, checks = [], []
+    for step in range(cfg.steps):
         x = synth.make_tokens(cfg, step, "cpu")
-        b_before = layer.bias.cpu().numpy().copy()
-        layer.forward(x.cuda())
+        b_before = layer.bias.clone()
+        out = layer.forward(x.cuda())
+        if step in MID_OUTPUT_STEPS:
+            out = out.clone()
         layer.bias_update(cfg.T)
         torch.cuda.synchronize()
+        assert layer.device_status() == 0
         s64 = ref.router_affinity64(bf16_to_np64(x), p["w_r"].numpy(), p["logit_offset"].numpy())
-        traj.step(step, cfg.T, s64, layer.idx.cpu().numpy(), layer.load.cpu().numpy(), b_before,
-                  layer.bias.cpu().numpy())
+        traj.step(step, cfg.T, s64, layer.idx.cpu().numpy(), layer.load.cpu().numpy(),
+                  b_before.cpu().numpy(), layer.bias.cpu().numpy())
         ratios.append(float(layer.stats[2].item()))
-    assert layer.device_status() == 0
+        if step in MID_OUTPUT_STEPS:
+            rc = route_check(cfg, p, x, layer, bias=b_before)
+            sample = output_sample(rc, 256, step)
+            r = check_pass(cfg, p, x, layer, out, sample=sample, bias=b_before)
+            checks.append((step, describe(r)))
+    for step, d in checks:
+        print(f"mid step {step}: {d}")
+    print(f"mid max/mean first {ratios[0]:.4f} last {ratios[-1]:.4f}; near-tie mismatches "
+          f"{traj.near_tie_mismatches} (kth {traj.mismatches_kth}); trajectories parted at "
+          f"{traj.diverged_at}")
+    assert len(ratios) == 50
     assert ratios[0] > 1.5          # the Zipf offset skews the start
