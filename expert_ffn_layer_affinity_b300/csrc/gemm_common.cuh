@@ -6,6 +6,7 @@
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
+#include <atomic>
 #include <cstdint>
 
 #include "ptx.cuh"
@@ -107,15 +108,21 @@ __device__ __forceinline__ void build_tile_prefix(int G, int tok_tile, int lane,
 }
 
 // ------------------------------------------------------------------ host side
+// The driver's tensor-map encoder, looked up on first use (and again after a
+// failed lookup); an atomic, so threads making their first calls together
+// are safe.
 inline PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::atomic<PFN_cuTensorMapEncodeTiled_v12000> cached{nullptr};
+  PFN_cuTensorMapEncodeTiled_v12000 fn = cached.load(std::memory_order_acquire);
   if (!fn) {
     void* ptr = nullptr;
     cudaDriverEntryPointQueryResult q;
     if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
                                          &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
+        q == cudaDriverEntryPointSuccess) {
       fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+      cached.store(fn, std::memory_order_release);
+    }
   }
   return fn;
 }

@@ -459,21 +459,20 @@ template <int MODE>
 cudaError_t launch_fp8(const CUtensorMap& w, const CUtensorMap& x, const CUtensorMap& sa1,
                        const CUtensorMap& sa2, const CUtensorMap& sw, const Fp8Params& p,
                        int max_units, cudaStream_t s) {
-  static bool attr_done[64] = {false};
+  static DeviceOnce once;
   int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev < 64 && !attr_done[dev]) {
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  err = once_per_device(once, dev, []() {
     // The register split (setmaxnreg) must fit what the CTA is launched with,
     // or the increasing warps would wait for registers that never come.
     cudaFuncAttributes fa;
     cudaError_t e = cudaFuncGetAttributes(&fa, fp8_gemm_kernel<MODE>);
     if (e != cudaSuccess) return e;
     if (fa.numRegs * kThreads < kSplitRegs) return cudaErrorInvalidConfiguration;
-    e = cudaFuncSetAttribute(fp8_gemm_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kSmem);
-    if (e != cudaSuccess) return e;
-    attr_done[dev] = true;
-  }
+    return cudaFuncSetAttribute(fp8_gemm_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+  });
+  if (err != cudaSuccess) return err;
   int units = sm_count() / 2;
   if (max_units < units) units = max_units;
   if (units < 1) units = 1;

@@ -40,6 +40,15 @@
 //   warp 1      TMEM allocator; lane 0 issues tcgen05.mma and commits (in a
 //               pair, only the even CTA issues; its commits reach both CTAs)
 //   warps 2..5  epilogue: tcgen05.ld from TMEM, activation, global stores
+//
+// The MMA issuer is the critical path: a tcgen05.mma of the pair costs the
+// issuing thread about the same whatever N is, so a k-block of a ragged tile
+// takes as long as a full one.  The issuer's loop keeps only the barrier
+// wait, four MMAs and the commit per k-block (ring slot and parity stepped,
+// descriptors offset from slot 0), and the epilogue warps, which share the
+// SM sub-partitions with the issuer and the producer, poll their
+// accumulator barrier with short sleeps instead of spinning (measured on the
+// V3 routed call: about 20% fewer cycles, outputs bit-identical).
 // Work items are (group, token tile, column tile), group-major and column
 // tile fastest (see decode_work), handed out with a fixed stride.
 #include <cuda.h>
@@ -313,8 +322,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issuer
     if (lane == 0 && rank == 0) {
-      uint32_t it = 0, unit = 0;
+      uint32_t unit = 0;
+      int slot = 0;        // ring slot of the next stage
+      uint32_t fph = 0;    // parity of that slot's full barrier
       bool ok = true, issued = false;
+      // shared-memory descriptors of slot 0; slot s starts s * kStageBytes
+      // further on (the start-address field counts 16-byte units)
+      static_assert(C::kBoxes == 1, "one 64-deep k-block per stage");
+      const uint64_t a_desc0 =
+          MODE == MODE_DGRAD ? umma_sdesc_mn_sw128(tiles) : umma_sdesc_sw128(tiles);
+      const uint64_t b_desc0 = umma_sdesc_sw128(tiles + C::kA);
+      constexpr uint64_t kSlotStep = C::kStageBytes >> 4;
+      // the next 16 of K: 32 bytes along a K-major row, or 16 128-byte rows
+      // of an MN-major chunk
+      constexpr uint64_t a_step = MODE == MODE_DGRAD ? (16 * 128) >> 4 : 2;
       for (int w = unit_id; w < total && ok; w += n_units) {
         int g, n, m, kb_lo, kb_hi;
         decode_work(w / splits, NT, mt_prefix, G, g, n, m);
@@ -337,36 +358,29 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_after();
           const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(b * C::kBufCols);
           const int st1 = (st0 + chunk_st < kb_hi) ? st0 + chunk_st : kb_hi;
-          for (int st = st0; st < st1; ++st, ++it) {
-            const int s = static_cast<int>(it % S);
-            const uint32_t ph = (it / S) & 1u;
-            if (!mbar_wait(full_bar(s), ph, abort_flag, p.status)) {
+          uint32_t acc = 0u;  // the unit's first MMA overwrites its accumulator
+          for (int st = st0; st < st1; ++st) {
+            if (!mbar_wait(full_bar(slot), fph, abort_flag, p.status)) {
               ok = false;
               break;
             }
             tc_fence_after();
-            const int kb0 = st * C::kBoxes;
-            const int nbox = (p.num_kb - kb0) < C::kBoxes ? p.num_kb - kb0 : C::kBoxes;
-            const uint32_t sa = tiles + s * C::kStageBytes;
-            for (int j = 0; j < nbox; ++j) {
-              const uint64_t adesc = MODE == MODE_DGRAD
-                                         ? umma_sdesc_mn_sw128(sa + static_cast<uint32_t>(j * C::kA))
-                                         : umma_sdesc_sw128(sa + static_cast<uint32_t>(j * C::kA));
-              const uint64_t bdesc =
-                  umma_sdesc_sw128(sa + static_cast<uint32_t>(C::kBoxes * C::kA + j * C::kB));
-              // the next 16 of K: 32 bytes along a K-major row, or 16
-              // 128-byte rows of an MN-major chunk
-              constexpr uint64_t a_step = MODE == MODE_DGRAD ? (16 * 128) >> 4 : 2;
+            const uint64_t soff = static_cast<uint64_t>(slot) * kSlotStep;
+            const uint64_t adesc = a_desc0 + soff;
+            const uint64_t bdesc = b_desc0 + soff;
 #pragma unroll
-              for (int k = 0; k < BK / UMMA_K; ++k) {
-                const uint32_t acc = (st > st0 || j > 0 || k > 0) ? 1u : 0u;
-                if (PAIR) umma_bf16_pair(d_tmem, adesc + a_step * k, bdesc + 2ull * k, idesc, acc);
-                else umma_bf16(d_tmem, adesc + a_step * k, bdesc + 2ull * k, idesc, acc);
-              }
+            for (int k = 0; k < BK / UMMA_K; ++k) {
+              if (PAIR) umma_bf16_pair(d_tmem, adesc + a_step * k, bdesc + 2ull * k, idesc, acc);
+              else umma_bf16(d_tmem, adesc + a_step * k, bdesc + 2ull * k, idesc, acc);
+              acc = 1u;
             }
             issued = true;
-            if (PAIR) umma_commit_pair_mc(empty_bar(s), 0x3);
-            else umma_commit(empty_bar(s));
+            if (PAIR) umma_commit_pair_mc(empty_bar(slot), 0x3);
+            else umma_commit(empty_bar(slot));
+            if (++slot == S) {
+              slot = 0;
+              fph ^= 1u;
+            }
           }
           if (!ok) break;
           if (PAIR) umma_commit_pair_mc(accf_bar(b), 0x3);
@@ -399,7 +413,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int kb0 = kb_lo; kb0 < kb_hi; kb0 += chunk_kb, ++unit) {
           const int b = static_cast<int>(unit % NB);
           const uint32_t bph = (unit / NB) & 1u;
-          ok = __all_sync(0xFFFFFFFFu, mbar_wait(accf_bar(b), bph, abort_flag, p.status));
+          ok = __all_sync(0xFFFFFFFFu, mbar_wait_nap(accf_bar(b), bph, abort_flag, p.status));
           if (!ok) break;
           tc_fence_after();
           const uint32_t taddr = tmem_base + lane_base + static_cast<uint32_t>(b * C::kBufCols);
@@ -442,7 +456,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int b = static_cast<int>(unit % NB);
         const uint32_t bph = (unit / NB) & 1u;
         ++unit;
-        ok = __all_sync(0xFFFFFFFFu, mbar_wait(accf_bar(b), bph, abort_flag, p.status));
+        ok = __all_sync(0xFFFFFFFFu, mbar_wait_nap(accf_bar(b), bph, abort_flag, p.status));
         if (!ok) break;
         tc_fence_after();
         const int tok0 = m * C::kTokTile;
@@ -555,15 +569,15 @@ template <int MODE>
 cudaError_t launch_gemm(const CUtensorMap& a, const CUtensorMap& a2, const CUtensorMap& b,
                         const GemmParams& p, int max_units, cudaStream_t s) {
   using C = Cfg<MODE>;
-  static bool attr_done[64] = {false};
+  static DeviceOnce once;
   int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev < 64 && !attr_done[dev]) {
-    const cudaError_t e = cudaFuncSetAttribute(gemm_kernel<MODE>,
-                                               cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
-    if (e != cudaSuccess) return e;
-    attr_done[dev] = true;
-  }
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  err = once_per_device(once, dev, []() {
+    return cudaFuncSetAttribute(gemm_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                C::kSmem);
+  });
+  if (err != cudaSuccess) return err;
   const int per_unit = C::kPair ? 2 : 1;
   int units = sm_count() / per_unit;
   if (max_units < units) units = max_units;

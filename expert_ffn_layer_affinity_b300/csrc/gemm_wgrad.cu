@@ -330,7 +330,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       int b = 0;
       if (!zero) {
         b = static_cast<int>(unit & 1u);
-        ok = __all_sync(0xFFFFFFFFu, mbar_wait(accf_bar(b), (unit >> 1) & 1u, abort_flag, p.status));
+        // a long wait: poll with short sleeps, leaving issue slots to the
+        // producer and the MMA issuer on the shared sub-partitions
+        ok = __all_sync(0xFFFFFFFFu,
+                        mbar_wait_nap(accf_bar(b), (unit >> 1) & 1u, abort_flag, p.status));
         if (!ok) break;
         ++unit;
         tc_fence_after();
@@ -422,15 +425,14 @@ cudaError_t launch_grouped_wgrad(const uint16_t* a, const uint16_t* b, const int
       !gemm::make_map_sw128(&tb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, b, N, rows, BK) ||
       !make_out_map(&to, out, G, M, N))
     return cudaErrorInvalidValue;
-  static bool attr_done[64] = {false};
+  static DeviceOnce once;
   int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev < 64 && !attr_done[dev]) {
-    const cudaError_t e =
-        cudaFuncSetAttribute(wgrad_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
-    if (e != cudaSuccess) return e;
-    attr_done[dev] = true;
-  }
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  err = once_per_device(once, dev, []() {
+    return cudaFuncSetAttribute(wgrad_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+  });
+  if (err != cudaSuccess) return err;
   WgradParams p{};
   p.offsets = offsets;
   p.G = G;

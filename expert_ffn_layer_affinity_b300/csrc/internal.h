@@ -2,12 +2,36 @@
 #pragma once
 #include <cuda.h>
 #include <cuda_runtime.h>
+#include <atomic>
 #include <cstddef>
 #include <cstdint>
+#include <mutex>
 
 namespace moe {
 
 int sm_count();  // SMs of the current device (cached per device)
+
+// One-time set-up per device (a kernel attribute, a looked-up address, a
+// device property), safe when several host threads make their first calls
+// at the same time: the first caller on a device runs `init` under a lock
+// and marks the device done only when `init` succeeded; later callers see
+// the mark (acquire) without locking.  Devices beyond kMaxDevices run
+// `init` on every call.
+constexpr int kMaxDevices = 64;
+struct DeviceOnce {
+  std::atomic<bool> done[kMaxDevices] = {};
+  std::mutex lock;
+};
+template <typename F>
+cudaError_t once_per_device(DeviceOnce& once, int dev, F&& init) {
+  if (dev < 0 || dev >= kMaxDevices) return init();
+  if (once.done[dev].load(std::memory_order_acquire)) return cudaSuccess;
+  std::lock_guard<std::mutex> guard(once.lock);
+  if (once.done[dev].load(std::memory_order_relaxed)) return cudaSuccess;
+  const cudaError_t e = init();
+  if (e == cudaSuccess) once.done[dev].store(true, std::memory_order_release);
+  return e;
+}
 
 // ---- router selection (router_topk.cu)
 struct TopkArgs {

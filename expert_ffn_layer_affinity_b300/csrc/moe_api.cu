@@ -21,15 +21,19 @@ struct Trace {
 namespace moe {
 
 int sm_count() {
-  static int cached[64] = {0};
+  static DeviceOnce once;
+  static int cached[kMaxDevices] = {0};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 148;
-  if (dev >= 0 && dev < 64 && cached[dev] > 0) return cached[dev];
   int n = 0;
-  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
-    n = 148;
-  if (dev >= 0 && dev < 64) cached[dev] = n;
-  return n;
+  const cudaError_t e = once_per_device(once, dev, [&]() {
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+      n = 148;
+    if (dev >= 0 && dev < kMaxDevices) cached[dev] = n;
+    return cudaSuccess;
+  });
+  if (e != cudaSuccess) return 148;
+  return (dev >= 0 && dev < kMaxDevices) ? cached[dev] : n;
 }
 
 namespace {

@@ -200,18 +200,21 @@ static __device__ __align__(256) int32_t g_permute_scratch[kPermuteStaticScratch
 
 cudaError_t permute_static_scratch(int32_t** ptr) {
   // In host code the symbol is only a host-side stand-in; the device address
-  // is looked up once per device, with that device current.
-  static int32_t* cached[64] = {nullptr};
+  // is looked up once per device, with that device current (several host
+  // threads making their first call at once look it up once).
+  static DeviceOnce once;
+  static int32_t* cached[kMaxDevices] = {nullptr};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  if (cached[dev] == nullptr) {
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  e = once_per_device(once, dev, [&]() {
     void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_permute_scratch);
-    if (e != cudaSuccess) return e;
-    cached[dev] = static_cast<int32_t*>(p);
-  }
+    const cudaError_t r = cudaGetSymbolAddress(&p, g_permute_scratch);
+    if (r == cudaSuccess) cached[dev] = static_cast<int32_t*>(p);
+    return r;
+  });
+  if (e != cudaSuccess) return e;
   *ptr = cached[dev];
   return cudaSuccess;
 }
@@ -235,14 +238,15 @@ cudaError_t launch_permute(const int32_t* idx, int T, int K, int E, const uint16
                                                                     offsets);
   if ((err = cudaGetLastError()) != cudaSuccess) return err;
   const size_t rank_smem = static_cast<size_t>(kTileWarps) * E * sizeof(int32_t);
-  static bool attr_set[64] = {false};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (rank_smem > 48 * 1024 && dev < 64 && !attr_set[dev]) {
-    err = cudaFuncSetAttribute(rank_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               32 * 512 * static_cast<int>(sizeof(int32_t)));
+  if (rank_smem > 48 * 1024) {
+    static DeviceOnce once;
+    int dev = 0;
+    if ((err = cudaGetDevice(&dev)) != cudaSuccess) return err;
+    err = once_per_device(once, dev, []() {
+      return cudaFuncSetAttribute(rank_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  32 * 512 * static_cast<int>(sizeof(int32_t)));
+    });
     if (err != cudaSuccess) return err;
-    attr_set[dev] = true;
   }
   rank_kernel<<<n_tiles, kTile, rank_smem, s>>>(idx, R, K, E, tile_counts, row_of, tok_of);
   if ((err = cudaGetLastError()) != cudaSuccess) return err;

@@ -70,6 +70,28 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
   }
 }
 
+// mbar_wait for long waits (an epilogue waiting for its next accumulator):
+// polls with a short sleep in between, so the waiting warps leave the issue
+// slots of their SM sub-partitions to the MMA issuer and the TMA producer.
+// Same limits and abort behaviour as mbar_wait.
+__device__ __forceinline__ bool mbar_wait_nap(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                              int32_t* status, unsigned nap_ns = 64) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = globaltimer_ns();
+  for (uint32_t i = 1;; ++i) {
+    __nanosleep(nap_ns);
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 15u) == 0) {
+      if (*abort_flag) return false;
+      if (globaltimer_ns() - t0 > kWaitLimitNs) {
+        *abort_flag = 1;
+        if (status) atomicOr(reinterpret_cast<unsigned int*>(status), MOE_DEV_TIMEOUT);
+        return false;
+      }
+    }
+  }
+}
+
 // ----------------------------------------------------------------------- TMA
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
