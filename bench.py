@@ -11,6 +11,12 @@ One step = one pass of the whole path over one batch of T tokens plus the
 bias update.  For N > 1 (launched with torch.distributed.run), every rank
 runs a replica on its own T tokens; the per-expert loads are summed over the
 ranks before the bias update (scaling "weak").  Prints one JSON line on rank 0.
+
+The headline is the V3-shaped layer (T=8192).  At N=1 the same line also
+carries "workloads": every other synthetic workload measured in the same run
+(tiny; mid, 50 bias-feedback steps; decode at T=64/256/1024; the drifting
+100-step run), each with tokens/s, ms/step and its roofline fraction
+(--no-workloads skips them).
 """
 from __future__ import annotations
 
@@ -32,10 +38,15 @@ CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.a
                 "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
                 "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 # DRAM bytes (read + write) per routed expert of the two expert-GEMM launches,
-# from ncu dram__bytes on the 16-expert profiling case (profiles/gemm_pair_v3e16.md,
-# "Re-measured DRAM traffic"), scaled by the experts a launch processes.  Must be
-# re-measured when those kernels change.
+# from ncu dram__bytes on the 16-expert V3-shaped profiling case (d=7168,
+# I=2048, ~256 rows per expert), scaled by the experts a launch processes.
+# Must be re-measured whenever those kernels change.
 GEMM_TRAFFIC_PER_EXPERT = (1.042927872e9 + 16.49152e6 + 0.493063424e9 + 44.88576e6) / 16
+# The timed region's length decides which measured tensor peak a fraction is
+# taken against: a region shorter than this runs at burst clocks (the peak of
+# a kernel timed alone); a longer one settles at the power-capped clock (the
+# sustained peak).
+SUSTAINED_AFTER_S = 1.0
 KERNELS_PER_STEP = 12  # router GEMM, selection, 4 permute, 2+2 grouped GEMM, combine, bias update
 # backward: combine 1; routed: dh GEMM, SwiGLU, dv GEMM, 2 weight-gradient GEMMs; shared:
 # the same 5; router 3; input gradient 1 (the forward keeps the pre-activations)
@@ -70,6 +81,8 @@ def parse():
     ap.add_argument("--pass", dest="pass_", choices=["forward", "train"], default="forward",
                     help="train: each step is the forward pass, the backward pass (all "
                          "gradients) and the bias update")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="skip the other workloads measured next to the headline (N=1)")
     return ap.parse_args()
 
 
@@ -249,6 +262,197 @@ def cpu_baseline(cfg, layer, x, n_tokens, fp8=False):
                       f"load count, bias update); {dt:.1f} s"}
 
 
+def tensor_peak(pk, timed_s, fp8=False):
+    """(peak TFLOP/s, description) for a tensor-bound fraction: the burst
+    figure when the timed region is shorter than SUSTAINED_AFTER_S (clocks
+    still at burst), else the sustained one; E4M3 counts 2 x bf16 (the
+    nominal dense ratio, 4.5 / 2.25 PFLOP/s)."""
+    burst = timed_s < SUSTAINED_AFTER_S
+    peak = (pk["bf16"] if burst else pk["bf16_sust"]) * (2.0 if fp8 else 1.0)
+    kind = (f"{'E4M3 = 2 x ' if fp8 else ''}bf16 {'burst' if burst else 'sustained'}, {pk['src']} "
+            f"(timed region {timed_s:.3f} s {'<' if burst else '>='} {SUSTAINED_AFTER_S} s)")
+    return peak, kind
+
+
+def timed_steps(layer, cfg, xs, steps, warmup, names, group=None, local=0, redundant=0):
+    """W warm-up steps, then `steps` timed steps of the whole path (route ->
+    permute -> routed and shared experts -> combine -> bias update), each on
+    the next batch of `xs`, bracketed by a barrier and a synchronize; per-call
+    CUDA events on the launching stream.  The timed trajectory starts from the
+    layer's initial bias."""
+    import torch
+    import torch.distributed as dist
+    stream = torch.cuda.current_stream()
+    bias0 = layer.bias.clone()
+
+    def barrier():
+        if group is not None:
+            dist.barrier(device_ids=[local])
+
+    for i in range(warmup):
+        layer.step(xs[i % len(xs)], group=group)
+    torch.cuda.synchronize()
+    if layer.device_status() != 0:
+        raise RuntimeError(f"device status {layer.device_status()} during warm-up")
+    if redundant:
+        layer.plan_replicas(layer.load.cpu())    # copies placed from the warm-up loads
+    touched = int((layer.load > 0).sum().item())
+    layer.bias.copy_(bias0)
+    stats_hist = torch.zeros(steps, 4, dtype=torch.float32, device="cuda")
+    marks = [{n: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for n in names} for _ in range(steps)]
+    clocks = ClockSampler(local)
+    barrier()
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks.mark_start()
+    ev0.record(stream)
+    for i in range(steps):
+        layer.step(xs[i % len(xs)], group=group, marks=marks[i], stats_out=stats_hist[i])
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    clocks.mark_stop()
+    barrier()
+    clk = clocks.stop()
+    ms = ev0.elapsed_time(ev1)
+    if group is not None:
+        t = torch.tensor([ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    per = {n: statistics.mean(m[n][0].elapsed_time(m[n][1]) for m in marks) for n in names}
+    return dict(ms=ms, per=per, stats=stats_hist.cpu().numpy(), clocks=clk, touched=touched,
+                status=layer.device_status())
+
+
+def workload_name(cfg):
+    return (f"{cfg.name}: T={cfg.T} d={cfg.d} E={cfg.E} K={cfg.K} shared={cfg.n_shared} I={cfg.I} "
+            f"groups={cfg.n_groups}/{cfg.topk_groups} scale={cfg.route_scale}")
+
+
+def feedback_summary(cfg, stats):
+    return {"steps": int(stats.shape[0]), "gamma": cfg.gamma,
+            "max_over_mean_per_step": [round(float(v), 4) for v in stats[:, 2]],
+            "cv_per_step": [round(float(v), 4) for v in stats[:, 3]],
+            "first": round(float(stats[0, 2]), 4), "last": round(float(stats[-1, 2]), 4),
+            "min": round(float(stats[:, 2].min()), 4), "max": round(float(stats[:, 2].max()), 4)}
+
+
+def roofline_entry(cfg, res, steps, pk, fp8=False):
+    """The dominant call's roofline: expert-weight streaming against HBM for
+    the decode sizes, the routed expert GEMMs against the tensor peak
+    otherwise, and none for the tiny layer (a launch-latency-bound pass of
+    microseconds, where a fraction means nothing)."""
+    per = res["per"]
+    touched = res["touched"]
+    timed_s = res["ms"] / 1e3
+    if cfg.name == "tiny":
+        return {"bound": "launch", "achieved": None, "peak": None, "unit": None, "frac": None,
+                "traffic": None, "note": "launch-latency-bound microsecond pass: no roofline "
+                                         "fraction is meaningful at this size"}
+    if cfg.name == "v3_decode":
+        # decode: the expert GEMMs stream the weights of the touched experts
+        wbytes = 3.0 * (touched + cfg.n_shared) * cfg.I * cfg.d * (1 if fp8 else 2)
+        gbs = wbytes / ((per["routed"] + per.get("shared", 0.0)) * 1e-3) / 1e9
+        return {"bound": "hbm", "achieved": round(gbs, 1), "peak": pk["hbm"], "unit": "GB/s",
+                "frac": round(gbs / pk["hbm"], 4), "traffic": None,
+                "kernel": "moe_grouped_swiglu routed + shared (expert-weight streaming)",
+                "peak_kind": f"HBM copy, {pk['src']}", "weight_bytes_per_step": wbytes}
+    alg = algorithmic(cfg, touched, fp8)
+    routed_tf = alg["routed"]["flops"] / (per["routed"] * 1e-3) / 1e12
+    peak, kind = tensor_peak(pk, timed_s, fp8)
+    tc_burst, tc_sust = (tensor_peak(pk, 0.0, fp8)[0], tensor_peak(pk, 1e9, fp8)[0])
+    return {"bound": "tensor", "achieved": round(routed_tf, 1), "peak": peak, "unit": "TFLOP/s",
+            "frac": round(routed_tf / peak, 4),
+            "traffic": (GEMM_TRAFFIC_PER_EXPERT * touched
+                        if cfg.d == 7168 and cfg.I == 2048 and not fp8 else None),
+            "kernel": ("moe_grouped_swiglu_fp8 (routed experts: GEMM1+SwiGLU, h quantization, "
+                       "GEMM2 launches)" if fp8 else
+                       "moe_grouped_swiglu (routed experts: GEMM1+SwiGLU and GEMM2 launches)"),
+            "peak_kind": kind, "frac_of_burst": round(routed_tf / tc_burst, 4),
+            "frac_of_sustained": round(routed_tf / tc_sust, 4)}
+
+
+def layer_fraction(cfg, ms_step, timed_s, pk, fp8=False):
+    """Whole-layer tensor fraction: the routed + shared expert FLOPs of a step
+    over the step time."""
+    tf = cfg.expert_flops() / (ms_step * 1e-3) / 1e12
+    peak, kind = tensor_peak(pk, timed_s, fp8)
+    return {"expert_tflops": round(tf, 1), "frac": round(tf / peak, 4), "peak": peak,
+            "peak_kind": kind, "frac_of_burst": round(tf / tensor_peak(pk, 0.0, fp8)[0], 4),
+            "frac_of_sustained": round(tf / tensor_peak(pk, 1e9, fp8)[0], 4)}
+
+
+def kernel_table(cfg, res, fp8=False):
+    alg = algorithmic(cfg, res["touched"], fp8)
+    kernels = {}
+    for n, ms in res["per"].items():
+        a = alg[n]
+        k = {"ms": round(ms, 4)}
+        if ms > 0:
+            if a["flops"]:
+                k["tflops"] = round(a["flops"] / (ms * 1e-3) / 1e12, 2)
+            k["gbs"] = round(a["bytes"] / (ms * 1e-3) / 1e9, 1)
+        kernels[n] = k
+    return kernels
+
+
+def run_workloads(args, v3_layer, pk):
+    """The other synthetic workloads, measured in the same run as the
+    headline (N=1): tiny, mid (its 50 bias-feedback steps), decode at
+    T = 64 / 256 / 1024 and the drifting 100-step run (both on the V3
+    layer's weights, as the workloads define them)."""
+    import torch
+    from expert_ffn_layer_affinity_b300 import synth
+    from expert_ffn_layer_affinity_b300.layer import MoELayer
+    names = ["route", "permute", "routed", "shared", "combine"]
+    out = {}
+
+    def one(cfg, layer, xs, steps, warmup):
+        res = timed_steps(layer, cfg, xs, steps, warmup, names)
+        ms_step = res["ms"] / steps
+        entry = {"workload": workload_name(cfg), "steps": steps, "warmup": warmup,
+                 "value": round(cfg.T * steps / (res["ms"] / 1e3), 1), "unit": "tokens/s",
+                 "ms_per_step": round(ms_step, 4),
+                 "roofline": roofline_entry(cfg, res, steps, pk),
+                 "kernels": kernel_table(cfg, res), "experts_touched": res["touched"],
+                 "gpu_launches": (KERNELS_PER_STEP + router_extra(cfg)) * steps,
+                 "device_status": res["status"], "clocks": res["clocks"]}
+        if cfg.name not in ("tiny", "v3_decode"):
+            entry["layer_tensor_frac"] = layer_fraction(cfg, ms_step, res["ms"] / 1e3, pk)
+        if cfg.steps > 1:
+            entry["feedback"] = feedback_summary(cfg, res["stats"])
+        return entry
+
+    for name in ("tiny", "mid"):
+        cfg = synth.CONFIGS[name]
+        p = synth.make_params(cfg, "cuda")
+        layer = MoELayer(cfg, p)
+        del p
+        n_batches = cfg.steps if cfg.steps > 1 else 2
+        xs = [synth.make_tokens(cfg, step=i, device="cuda") for i in range(n_batches)]
+        out[name] = one(cfg, layer, xs, cfg.steps if cfg.steps > 1 else 50, 5)
+        del layer, xs
+        torch.cuda.empty_cache()
+    # decode sizes and the drifting run share the V3 layer's weights
+    v3_cfg, bias0 = v3_layer.cfg, v3_layer.bias.clone()
+    for T in synth.DECODE_T:
+        cfg = synth.CONFIGS["v3_decode"].with_T(T)
+        v3_layer.cfg = cfg
+        v3_layer.bias.copy_(bias0)
+        xs = [synth.make_tokens(cfg, step=i, device="cuda", seed=100 + T) for i in range(2)]
+        out[f"v3_decode:{T}"] = one(cfg, v3_layer, xs, 20, 5)
+    cfg = synth.CONFIGS["v3_drift"]
+    v3_layer.cfg = cfg
+    v3_layer.bias.copy_(bias0)
+    xs = [synth.make_tokens(cfg, step=i, device="cuda") for i in range(cfg.steps)]
+    out["v3_drift"] = one(cfg, v3_layer, xs, cfg.steps, 3)
+    del xs
+    v3_layer.cfg = v3_cfg
+    v3_layer.bias.copy_(bias0)
+    torch.cuda.empty_cache()
+    return out
+
+
 # --------------------------------------------------------------------------
 def run_ours(args):
     import torch
@@ -270,7 +474,6 @@ def run_ours(args):
     layer = MoELayer(cfg, p, device=f"cuda:{local}", shared_stream=args.shared_stream,
                      shared_as_routed=args.shared_as_routed, n_redundant=args.redundant,
                      precision=args.precision)
-    bias0 = layer.bias.clone()
     del p
     feedback = cfg.steps > 1                     # mid / drift: a bias-feedback run
     if feedback:
@@ -282,46 +485,17 @@ def run_ours(args):
     xs = [synth.make_tokens(cfg, step=i, device="cuda", seed=cfg.seed + 7777 * rank)
           for i in range(n_batches)]
     stream = torch.cuda.current_stream()
+    names = ["route", "permute", "routed", "combine"]
+    if not args.shared_as_routed:
+        names.insert(3, "shared")
 
     def barrier():
         if group is not None:
             dist.barrier(device_ids=[local])
 
-    for i in range(args.warmup):
-        layer.step(xs[i % n_batches], group=group)
-    torch.cuda.synchronize()
-    if layer.device_status() != 0:
-        raise RuntimeError(f"device status {layer.device_status()} during warm-up")
-    if args.redundant:
-        layer.plan_replicas(layer.load.cpu())    # copies placed from the warm-up loads
-    layer.bias.copy_(bias0)                      # the timed trajectory starts from the initial bias
-    stats_hist = torch.zeros(args.steps, 4, dtype=torch.float32, device="cuda")
-    names = ["route", "permute", "routed", "combine"]
-    if not args.shared_as_routed:
-        names.insert(3, "shared")
-    marks = [{n: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-              for n in names} for _ in range(args.steps)]
-    touched = int((layer.load > 0).sum().item())
-    clocks = ClockSampler(local)
-    barrier()
-    torch.cuda.synchronize()
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    clocks.mark_start()
-    ev0.record(stream)
-    for i in range(args.steps):
-        layer.step(xs[i % n_batches], group=group, marks=marks[i], stats_out=stats_hist[i])
-    ev1.record(stream)
-    torch.cuda.synchronize()
-    clocks.mark_stop()
-    barrier()
-    clk = clocks.stop()
-    ms = ev0.elapsed_time(ev1)
-    if group is not None:
-        t = torch.tensor([ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
-    status = layer.device_status()
-    per = {n: statistics.mean(m[n][0].elapsed_time(m[n][1]) for m in marks) for n in names}
+    res = timed_steps(layer, cfg, xs, args.steps, args.warmup, names, group=group, local=local,
+                      redundant=args.redundant)
+    ms = res["ms"]
     ms_step = ms / args.steps
     value = cfg.T * world * args.steps / (ms / 1e3)
 
@@ -364,52 +538,16 @@ def run_ours(args):
             dist.destroy_process_group()
         return
     pk = peaks()
-    alg = algorithmic(cfg, touched, fp8)
-    # E4M3 dense peak: the measured bf16 figures times the nominal dense ratio
-    # (4.5 / 2.25 PFLOP/s)
-    tc_sust, tc_burst = (2 * pk["bf16_sust"], 2 * pk["bf16"]) if fp8 else (pk["bf16_sust"], pk["bf16"])
-    tc_kind = (f"E4M3 = 2 x bf16 sustained, {pk['src']} (nominal dense ratio)" if fp8
-               else f"bf16 sustained, {pk['src']}")
-    kernels = {}
-    if "shared" not in per:
-        per["shared"] = 0.0                       # inside the routed call in the serving layout
-    for n in names:
-        a = alg[n]
-        k = {"ms": round(per[n], 4)}
-        if a["flops"]:
-            k["tflops"] = round(a["flops"] / (per[n] * 1e-3) / 1e12, 2)
-        k["gbs"] = round(a["bytes"] / (per[n] * 1e-3) / 1e9, 1)
-        kernels[n] = k
-    routed_tf = alg["routed"]["flops"] / (per["routed"] * 1e-3) / 1e12
-    if cfg.name == "v3_decode":
-        # decode: the expert GEMMs stream the weights of the touched experts
-        wbytes = 3.0 * (touched + cfg.n_shared) * cfg.I * cfg.d * (1 if fp8 else 2)
-        gbs = wbytes / ((per["routed"] + per["shared"]) * 1e-3) / 1e9
-        roofline = {"bound": "hbm", "achieved": round(gbs, 1), "peak": pk["hbm"], "unit": "GB/s",
-                    "frac": round(gbs / pk["hbm"], 4), "traffic": None,
-                    "kernel": "moe_grouped_swiglu routed + shared (expert-weight streaming)",
-                    "peak_kind": f"HBM copy, {pk['src']}",
-                    "weight_bytes_per_step": wbytes}
-    else:
-        roofline = {"bound": "tensor", "achieved": round(routed_tf, 1), "peak": tc_sust,
-                    "unit": "TFLOP/s", "frac": round(routed_tf / tc_sust, 4),
-                    "traffic": (GEMM_TRAFFIC_PER_EXPERT * touched
-                                if cfg.d == 7168 and not fp8 else None),
-                    "kernel": ("moe_grouped_swiglu_fp8 (routed experts: GEMM1+SwiGLU, h "
-                               "quantization, GEMM2 launches)" if fp8 else
-                               "moe_grouped_swiglu (routed experts: GEMM1+SwiGLU and GEMM2 launches)"),
-                    "peak_kind": tc_kind,
-                    "frac_of_burst": round(routed_tf / tc_burst, 4)}
-    layer_tf = cfg.expert_flops() / (ms_step * 1e-3) / 1e12
+    if "shared" not in res["per"]:
+        res["per"]["shared"] = 0.0                # inside the routed call in the serving layout
+    kernels = kernel_table(cfg, res, fp8)
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "e4m3 expert GEMMs (fp32 promotion), bf16 activations" if fp8 else "bf16",
         "data": "synthetic (seeded N(0,1) tokens, N(0,0.02) weights, random-init)",
-        "config": {"workload": f"{cfg.name}: T={cfg.T} d={cfg.d} E={cfg.E} K={cfg.K} "
-                               f"shared={cfg.n_shared} I={cfg.I} groups={cfg.n_groups}/"
-                               f"{cfg.topk_groups} scale={cfg.route_scale}",
+        "config": {"workload": workload_name(cfg),
                    "tokens_per_rank": cfg.T, "parallelism": f"dp{world} (replicas, load all-reduce)",
                    "l2": "inputs larger than L2: 22.6 GB of expert weights streamed per step"
                    if cfg.d == 7168 else "two alternating token batches",
@@ -417,32 +555,28 @@ def run_ours(args):
                    "shared_as_routed": bool(args.shared_as_routed),
                    "redundant_experts": args.redundant,
                    "precision": args.precision},
-        "roofline": roofline,
-        "layer_tensor_frac": {"expert_tflops": round(layer_tf, 1),
-                              "frac_of_sustained": round(layer_tf / tc_sust, 4),
-                              "frac_of_burst": round(layer_tf / tc_burst, 4)},
+        "roofline": roofline_entry(cfg, res, args.steps, pk, fp8),
+        "layer_tensor_frac": layer_fraction(cfg, ms_step, ms / 1e3, pk, fp8),
         "kernels": kernels,
-        "experts_touched": touched,
+        "experts_touched": res["touched"],
         "hbm_kernels": {n: {"gbs": kernels[n]["gbs"],
                             "frac": round(kernels[n]["gbs"] / pk["hbm"], 4)}
-                        for n in ("permute", "combine")},
+                        for n in ("route", "permute", "combine")},
         "gpu_launches": (KERNELS_PER_STEP + router_extra(cfg) + 3 * fp8
                          - (3 if fp8 else 2) * bool(args.shared_as_routed)
                          + bool(args.redundant)) * args.steps,
-        "device_status": status,
-        "clocks": clk,
+        "device_status": res["status"],
+        "clocks": res["clocks"],
         "e2e": e2e,
     }
     if feedback:
-        h = stats_hist.cpu().numpy()
-        line["feedback"] = {"steps": args.steps, "gamma": cfg.gamma,
-                            "max_over_mean_per_step": [round(float(v), 4) for v in h[:, 2]],
-                            "cv_per_step": [round(float(v), 4) for v in h[:, 3]],
-                            "first": round(float(h[0, 2]), 4), "last": round(float(h[-1, 2]), 4),
-                            "min": round(float(h[:, 2].min()), 4),
-                            "max": round(float(h[:, 2].max()), 4)}
+        line["feedback"] = feedback_summary(cfg, res["stats"])
     if not args.no_cpu_baseline and world == 1:
         line["cpu_baseline"] = cpu_baseline(cfg, layer, xs[0], args.cpu_sample, fp8)
+    if (world == 1 and not args.no_workloads and args.config == "v3" and not fp8
+            and not args.shared_as_routed and not args.redundant and not args.shared_stream):
+        del xs
+        line["workloads"] = run_workloads(args, layer, pk)
     print(json.dumps(line), flush=True)
     if group is not None:
         dist.destroy_process_group()

@@ -276,7 +276,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else if (warp == 2) {
     // ----------------------------------------------------------- tail fixer
-    // A group's last k-block: rows valid .. 63 hold the next group's tokens
+    // A group's last k-block: rows valid .. BK-1 hold the next group's tokens
     // (or the fill past the tensor); zero them in every chunk of both
     // operands in this CTA.  A token row is one 128-byte line of a chunk
     // whatever the swizzle, so whole lines are cleared.

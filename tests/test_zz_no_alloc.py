@@ -59,9 +59,20 @@ def test_static_permute_matches_workspace_permute_on_two_calls(T, K, E, d):
 
 
 def test_static_permute_refuses_shapes_beyond_its_array():
+    """A shape whose per-tile counts exceed the fixed array is refused before
+    anything is launched.  Every buffer is a real device tensor of the right
+    size, so a weakened size check would give a wrong answer, not a fault."""
     dev = "cuda"
     T, K, E = 40000, 8, 256            # ceil(320000 / 1024) * 256 = 80128 counts > 65536
-    offs = torch.zeros(E + 1, dtype=torch.int32, device=dev)
-    r = moe.moe_permute_static(1 << 20, T, K, E, None, 0, offs, 1 << 20, 1 << 20, None, None,
+    idx = torch.zeros(T, K, dtype=torch.int32, device=dev)
+    offs = torch.full((E + 1,), -7, dtype=torch.int32, device=dev)
+    row_of = torch.full((T, K), -7, dtype=torch.int32, device=dev)
+    tok_of = torch.full((T * K,), -7, dtype=torch.int32, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    r = moe.moe_permute_static(idx, T, K, E, None, 0, offs, row_of, tok_of, None, status,
                                check=False)
+    torch.cuda.synchronize()
     assert r == moe.MOE_ERR_SCRATCH_LIMIT
+    for t in (offs, row_of, tok_of):
+        assert bool(torch.all(t == -7))
+    assert int(status.item()) == 0
