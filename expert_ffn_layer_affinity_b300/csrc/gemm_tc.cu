@@ -20,12 +20,11 @@
 // Expert modes run on CTA PAIRS (clusters of two, tcgen05 .cta_group::2).
 // The pair puts 256 WEIGHT rows on the MMA's M side (128 in each CTA) and up
 // to 256 of the group's TOKENS on the N side (half staged in each CTA), with
-// N chosen per tile as the tokens left rounded up to 32.  Each CTA thus
+// N chosen per tile as the tokens left rounded up to 16.  Each CTA thus
 // stages 16 KB of weights and 16 KB of tokens per 64-deep k-block for a
 // 256 x 256 x 64 MMA step: a third less shared-memory fill traffic per FLOP
-// than one CTA can reach, which is what the L2 -> SM path limits.  Padding
-// with N rounded to 32 costs about 6% at the V3 loads (23% with 128-row token
-// tiles).  The epilogue reads the [weight row x token] accumulator of its
+// than one CTA can reach.  Padding with N rounded to 16 costs about 3% of the
+// MMA work at the V3 loads (6% at 32, 23% with 128-row token tiles).  The epilogue reads the [weight row x token] accumulator of its
 // own CTA, transposes it through shared memory and writes token-major rows.
 //
 // Router mode keeps tokens on M (128) and experts on N (128).  Its K loop is
@@ -70,9 +69,17 @@ constexpr int kThreads = 192;
 using gemm::kMaxGroups;
 using gemm::decode_work;
 using gemm::wait_plain;
-using gemm::tile_n;
 using gemm::store_block_transposed;
 constexpr int kRouterChunkKb = 4;
+
+// Tokens of a pair tile the MMA covers: the rows left, at most tok_tile,
+// rounded up to 16 (8 staged in each CTA of the pair, one swizzle atom; the
+// MMA's N is a multiple of 16).  Rows past the group's end are computed and
+// never stored.
+__device__ __forceinline__ int tile_n(int rows_left, int tok_tile) {
+  const int n = rows_left < tok_tile ? rows_left : tok_tile;
+  return (n + 15) & ~15;
+}
 
 enum Mode : int { MODE_SWIGLU = 0, MODE_DOWN = 1, MODE_ROUTER = 2, MODE_DGRAD = 3 };
 

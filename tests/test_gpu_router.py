@@ -206,3 +206,43 @@ def test_router_gemm_affinity_and_routing(T, d, E, K, G, M, scale, zipf):
     gg = np.take_along_axis(gg, np.argsort(gi, 1), 1)
     og = np.take_along_axis(og, np.argsort(oi, 1), 1)
     np.testing.assert_allclose(gg, og, rtol=2e-5, atol=1e-6)
+
+
+@pytest.mark.parametrize("T,d,E,K,G,M,scale", [
+    (4096, 2048, 64, 6, 1, 1, 1.0),        # mid layer shape: the reduction is split
+    (64, 7168, 256, 8, 8, 4, 2.5),         # decode size of the V3 layer
+])
+def test_router_split_and_unsplit_reductions_agree(T, d, E, K, G, M, scale):
+    """Small batches split each router tile's reduction over several CTAs;
+    a workspace with room for the scores only forces the unsplit path.  The
+    two sum the same exact products in different orders, so the affinities
+    may differ in the last bits (router scores are not batch-invariant
+    across split counts), but both stay within the oracle's error bound and
+    the chosen experts agree on every token that is not a near tie."""
+    assert moe.moe_router_splits(T, d, E) > 1
+    g = torch.Generator().manual_seed(T + d + 1)
+    x = torch.randn(T, d, generator=g).to(torch.bfloat16)
+    w = (torch.randn(E, d, generator=g) * 0.02).float()
+    b = (torch.randn(E, generator=g) * 0.01).float()
+    dev = "cuda"
+    w_split = torch.empty(E, 3 * d, dtype=torch.bfloat16, device=dev)
+    moe.moe_router_prepare(w.to(dev), E, d, w_split)
+    scores_only = (T * E * 4 + 255) // 256 * 256
+    out = {}
+    for name, ws_b in (("split", moe.moe_workspace_bytes(T, d, E, K, 64)), ("unsplit", scores_only)):
+        idx = torch.empty(T, K, dtype=torch.int32, device=dev)
+        gate = torch.empty(T, K, device=dev)
+        load = torch.empty(E, dtype=torch.int32, device=dev)
+        aff = torch.empty(T, E, device=dev)
+        status = torch.zeros(1, dtype=torch.int32, device=dev)
+        ws = torch.empty(ws_b, dtype=torch.uint8, device=dev)
+        moe.moe_router_topk(x.to(dev), w_split, None, None, b.to(dev), T, d, E, K, G, M, scale,
+                            idx, gate, load, aff, status, ws, ws_b)
+        assert sync_status(status) == 0
+        out[name] = (idx.cpu().numpy(), aff.cpu().numpy().astype(np.float64))
+    s64 = ref.router_affinity64(bf16_to_np64(x), w.numpy())
+    for name in out:
+        assert np.abs(out[name][1] - s64).max() < 4e-6, name
+    kth, grp = ref.near_tie_tokens(s64, b.numpy(), K, G, M)
+    diff = np.any(np.sort(out["split"][0], 1) != np.sort(out["unsplit"][0], 1), axis=1)
+    assert not np.any(diff & ~(kth | grp)), np.nonzero(diff & ~(kth | grp))[0][:10]
