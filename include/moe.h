@@ -396,7 +396,9 @@ moe_status moe_combine_dx(const void* dx_perm_bf16, const int32_t* row_of, int K
  *   bias[e] = bias[e] + gamma  if E*load[e] < T*K   (underloaded)
  *   unchanged                  if equal
  * each one fp32 operation.  stats_out [4] fp32 (max load, mean load,
- * max/mean, coefficient of variation) or NULL. */
+ * max/mean, coefficient of variation = population standard deviation over
+ * the mean; all taken over the E experts, untouched ones as load 0; all 0
+ * when no load was counted) or NULL. */
 moe_status moe_bias_update(const int32_t* expert_load, float* bias, int T, int K, int E,
                            float gamma, float* stats_out, moe_stream_t stream);
 
