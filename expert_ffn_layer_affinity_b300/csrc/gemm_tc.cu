@@ -93,7 +93,7 @@ struct Tr;
 template <>
 struct Tr<MODE_SWIGLU> {
   static constexpr bool kPair = true;
-  static constexpr int kTokTile = 256, kColTile = 128, kStages = 6, kBoxes = 1, kBufs = 2,
+  static constexpr int kTokTile = 256, kColTile = 128, kStages = 3, kBoxes = 2, kBufs = 2,
                        kBufCols = 256;
   static constexpr int kA = 128 * BK * 2, kB = 128 * BK * 2;  // per CTA and 64-wide k-block
 };
@@ -101,7 +101,7 @@ struct Tr<MODE_SWIGLU> {
 template <>
 struct Tr<MODE_DOWN> {
   static constexpr bool kPair = true;
-  static constexpr int kTokTile = 256, kColTile = 256, kStages = 6, kBoxes = 1, kBufs = 2,
+  static constexpr int kTokTile = 256, kColTile = 256, kStages = 3, kBoxes = 2, kBufs = 2,
                        kBufCols = 256;
   static constexpr int kA = 128 * BK * 2, kB = 128 * BK * 2;
 };
@@ -121,10 +121,11 @@ template <int MODE>
 struct Cfg : Tr<MODE> {
   using T = Tr<MODE>;
   // A stage holds kBoxes consecutive 64-wide k-blocks of both operands, laid
-  // out [A_0 .. A_{n-1}][B_0 .. B_{n-1}].  (Measured on the V3 shape: one box
-  // per stage with 6 stages beats two boxes with 3 stages; HBM itself streams
-  // these boxes at ~6.6 TB/s, and the shared-memory fill from L2 is bound by
-  // the bytes in flight per SM.)
+  // out [A_0 .. A_{n-1}][B_0 .. B_{n-1}].  The expert modes take two boxes
+  // per stage in three stages: the MMA issuer then waits and commits once
+  // per 128 of K (eight MMAs) instead of once per 64 (measured on the V3
+  // routed call: 3% fewer SM cycles, 1.7% shorter steps from a cold start,
+  // outputs bit-identical).
   static constexpr int kStageBytes = T::kBoxes * (T::kA + T::kB);
   static constexpr int kTmemCols = T::kBufs * T::kBufCols;
   static constexpr int kNumBars = 2 * T::kStages + 2 * T::kBufs + 1;
@@ -253,6 +254,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int chunk_kb = (MODE == MODE_ROUTER) ? kRouterChunkKb : p.num_kb;
   const int num_st = (p.num_kb + C::kBoxes - 1) / C::kBoxes;           // stages per tile
   const int chunk_st = (MODE == MODE_ROUTER) ? kRouterChunkKb : num_st;  // stages per TMEM unit
+  static_assert(MODE != MODE_ROUTER || C::kBoxes == 1, "router chunks count k-blocks");
+  // the stages of item w: its k-blocks kBoxes at a time (the last stage may
+  // hold fewer boxes)
+  auto st_range = [&](int w, int& st_lo, int& st_hi) {
+    int kb_lo, kb_hi;
+    kb_range(w, kb_lo, kb_hi);
+    st_lo = kb_lo / C::kBoxes;
+    st_hi = (kb_hi + C::kBoxes - 1) / C::kBoxes;
+  };
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -262,9 +272,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t it = 0;
       bool ok = true;
       for (int w = unit_id; w < total && ok; w += n_units) {
-        int g, n, m, kb_lo, kb_hi;
+        int g, n, m, st_lo, st_hi;
         decode_work(w / splits, NT, mt_prefix, G, g, n, m);
-        kb_range(w, kb_lo, kb_hi);
+        st_range(w, st_lo, st_hi);
         const int rows_g = row_start[g + 1] - row_start[g];
         int tok_row = row_start[g] + m * C::kTokTile;
         int w_row = g * p.w_rows_per_group + n * C::kColTile;
@@ -272,7 +282,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tok_row += static_cast<int>(rank) * (tile_n(rows_g - m * C::kTokTile, C::kTokTile) / 2);
           w_row += static_cast<int>(rank) * (MODE == MODE_SWIGLU ? 64 : 128);
         }
-        for (int st = kb_lo; st < kb_hi; ++st, ++it) {
+        for (int st = st_lo; st < st_hi; ++st, ++it) {
           const int s = static_cast<int>(it % S);
           const uint32_t ph = (it / S) & 1u;
           if (!mbar_wait(empty_bar(s), ph ^ 1u, abort_flag, p.status)) {
@@ -335,18 +345,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true, issued = false;
       // shared-memory descriptors of slot 0; slot s starts s * kStageBytes
       // further on (the start-address field counts 16-byte units)
-      static_assert(C::kBoxes == 1, "one 64-deep k-block per stage");
       const uint64_t a_desc0 =
           MODE == MODE_DGRAD ? umma_sdesc_mn_sw128(tiles) : umma_sdesc_sw128(tiles);
-      const uint64_t b_desc0 = umma_sdesc_sw128(tiles + C::kA);
+      const uint64_t b_desc0 = umma_sdesc_sw128(tiles + C::kBoxes * C::kA);
       constexpr uint64_t kSlotStep = C::kStageBytes >> 4;
       // the next 16 of K: 32 bytes along a K-major row, or 16 128-byte rows
       // of an MN-major chunk
       constexpr uint64_t a_step = MODE == MODE_DGRAD ? (16 * 128) >> 4 : 2;
       for (int w = unit_id; w < total && ok; w += n_units) {
-        int g, n, m, kb_lo, kb_hi;
+        int g, n, m, st_lo, st_hi;
         decode_work(w / splits, NT, mt_prefix, G, g, n, m);
-        kb_range(w, kb_lo, kb_hi);
+        st_range(w, st_lo, st_hi);
         uint32_t idesc;
         if (MODE == MODE_ROUTER) {
           idesc = umma_idesc_bf16(128, C::kColTile);
@@ -355,7 +364,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           idesc = umma_idesc_bf16(256, tile_n(rows_g - m * C::kTokTile, C::kTokTile)) |
                   (MODE == MODE_DGRAD ? (1u << 15) : 0u);  // A (weights) MN-major
         }
-        for (int st0 = kb_lo; st0 < kb_hi && ok; st0 += chunk_st, ++unit) {
+        for (int st0 = st_lo; st0 < st_hi && ok; st0 += chunk_st, ++unit) {
           const int b = static_cast<int>(unit % NB);
           const uint32_t bph = (unit / NB) & 1u;
           if (!mbar_wait(acce_bar(b), bph ^ 1u, abort_flag, p.status)) {
@@ -364,7 +373,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tc_fence_after();
           const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(b * C::kBufCols);
-          const int st1 = (st0 + chunk_st < kb_hi) ? st0 + chunk_st : kb_hi;
+          const int st1 = (st0 + chunk_st < st_hi) ? st0 + chunk_st : st_hi;
           uint32_t acc = 0u;  // the unit's first MMA overwrites its accumulator
           for (int st = st0; st < st1; ++st) {
             if (!mbar_wait(full_bar(slot), fph, abort_flag, p.status)) {
@@ -373,13 +382,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             tc_fence_after();
             const uint64_t soff = static_cast<uint64_t>(slot) * kSlotStep;
-            const uint64_t adesc = a_desc0 + soff;
-            const uint64_t bdesc = b_desc0 + soff;
+            const int nbox = C::kBoxes == 1 ? 1
+                             : (p.num_kb - st * C::kBoxes < C::kBoxes ? p.num_kb - st * C::kBoxes
+                                                                        : C::kBoxes);
 #pragma unroll
-            for (int k = 0; k < BK / UMMA_K; ++k) {
-              if (PAIR) umma_bf16_pair(d_tmem, adesc + a_step * k, bdesc + 2ull * k, idesc, acc);
-              else umma_bf16(d_tmem, adesc + a_step * k, bdesc + 2ull * k, idesc, acc);
-              acc = 1u;
+            for (int j = 0; j < C::kBoxes; ++j) {
+              if (j >= nbox) break;
+              const uint64_t adesc = a_desc0 + soff + static_cast<uint64_t>((j * C::kA) >> 4);
+              const uint64_t bdesc = b_desc0 + soff + static_cast<uint64_t>((j * C::kB) >> 4);
+#pragma unroll
+              for (int k = 0; k < BK / UMMA_K; ++k) {
+                if (PAIR) umma_bf16_pair(d_tmem, adesc + a_step * k, bdesc + 2ull * k, idesc, acc);
+                else umma_bf16(d_tmem, adesc + a_step * k, bdesc + 2ull * k, idesc, acc);
+                acc = 1u;
+              }
             }
             issued = true;
             if (PAIR) umma_commit_pair_mc(empty_bar(slot), 0x3);
