@@ -112,7 +112,7 @@ struct Tr<MODE_DGRAD> : Tr<MODE_DOWN> {};
 template <>
 struct Tr<MODE_ROUTER> {
   static constexpr bool kPair = false;
-  static constexpr int kTokTile = 128, kColTile = 128, kStages = 6, kBoxes = 1, kBufs = 4,
+  static constexpr int kTokTile = 128, kColTile = 128, kStages = 3, kBoxes = 2, kBufs = 4,
                        kBufCols = 128;
   static constexpr int kA = 128 * BK * 2, kB = 128 * BK * 2;      // token tile, w_split tile
 };
@@ -121,11 +121,11 @@ template <int MODE>
 struct Cfg : Tr<MODE> {
   using T = Tr<MODE>;
   // A stage holds kBoxes consecutive 64-wide k-blocks of both operands, laid
-  // out [A_0 .. A_{n-1}][B_0 .. B_{n-1}].  The expert modes take two boxes
-  // per stage in three stages: the MMA issuer then waits and commits once
-  // per 128 of K (eight MMAs) instead of once per 64 (measured on the V3
-  // routed call: 3% fewer SM cycles, 1.7% shorter steps from a cold start,
-  // outputs bit-identical).
+  // out [A_0 .. A_{n-1}][B_0 .. B_{n-1}].  Every mode takes two boxes per
+  // stage in three stages: the MMA issuer then waits and commits once per 128
+  // of K (eight MMAs) instead of once per 64 (measured on the V3 shape: the
+  // routed call 3% fewer SM cycles and 1.7% shorter steps from a cold start,
+  // the route call 5% faster; outputs bit-identical).
   static constexpr int kStageBytes = T::kBoxes * (T::kA + T::kB);
   static constexpr int kTmemCols = T::kBufs * T::kBufCols;
   static constexpr int kNumBars = 2 * T::kStages + 2 * T::kBufs + 1;
@@ -253,8 +253,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   };
   const int chunk_kb = (MODE == MODE_ROUTER) ? kRouterChunkKb : p.num_kb;
   const int num_st = (p.num_kb + C::kBoxes - 1) / C::kBoxes;           // stages per tile
-  const int chunk_st = (MODE == MODE_ROUTER) ? kRouterChunkKb : num_st;  // stages per TMEM unit
-  static_assert(MODE != MODE_ROUTER || C::kBoxes == 1, "router chunks count k-blocks");
+  // stages per TMEM unit (a router chunk holds whole stages)
+  const int chunk_st = (MODE == MODE_ROUTER) ? kRouterChunkKb / C::kBoxes : num_st;
+  static_assert(kRouterChunkKb % C::kBoxes == 0, "router chunks hold whole stages");
   // the stages of item w: its k-blocks kBoxes at a time (the last stage may
   // hold fewer boxes)
   auto st_range = [&](int w, int& st_lo, int& st_hi) {
@@ -296,8 +297,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t bytes = static_cast<uint32_t>(nbox * (C::kA + C::kB));
           if (MODE == MODE_ROUTER) {
             mbar_arrive_expect_tx(full_bar(s), bytes);
-            tma_load_2d(sa, &tmA, full_bar(s), (kb0 % p.a_k_wrap_kb) * BK, tok_row, pol_tok);
-            tma_load_2d(sb, &tmB, full_bar(s), kb0 * BK, w_row, pol_w);
+            for (int j = 0; j < nbox; ++j) {
+              tma_load_2d(sa + static_cast<uint32_t>(j * C::kA), &tmA, full_bar(s),
+                          ((kb0 + j) % p.a_k_wrap_kb) * BK, tok_row, pol_tok);
+              tma_load_2d(sb + static_cast<uint32_t>(j * C::kB), &tmB, full_bar(s), (kb0 + j) * BK,
+                          w_row, pol_w);
+            }
           } else {
             // both CTAs' copies complete on the even CTA's barrier
             if (rank == 0) mbar_arrive_expect_tx(full_bar(s), 2 * bytes);
