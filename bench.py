@@ -81,6 +81,9 @@ def parse():
     ap.add_argument("--pass", dest="pass_", choices=["forward", "train"], default="forward",
                     help="train: each step is the forward pass, the backward pass (all "
                          "gradients) and the bias update")
+    ap.add_argument("--standard-weights", action="store_true",
+                    help="run the expert GEMMs on the [rows, cols] weight layout instead of the "
+                         "box-contiguous copies (same results)")
     ap.add_argument("--no-workloads", action="store_true",
                     help="skip the other workloads measured next to the headline (N=1)")
     return ap.parse_args()
@@ -473,7 +476,8 @@ def run_ours(args):
     fp8 = args.precision == "fp8"
     layer = MoELayer(cfg, p, device=f"cuda:{local}", shared_stream=args.shared_stream,
                      shared_as_routed=args.shared_as_routed, n_redundant=args.redundant,
-                     precision=args.precision)
+                     precision=args.precision,
+                     tiled_weights=False if args.standard_weights else None)
     del p
     feedback = cfg.steps > 1                     # mid / drift: a bias-feedback run
     if feedback:
@@ -554,7 +558,8 @@ def run_ours(args):
                    "shared_stream": bool(args.shared_stream),
                    "shared_as_routed": bool(args.shared_as_routed),
                    "redundant_experts": args.redundant,
-                   "precision": args.precision},
+                   "precision": args.precision,
+                   "expert_weight_layout": "box-contiguous" if layer.tiled else "rows"},
         "roofline": roofline_entry(cfg, res, args.steps, pk, fp8),
         "layer_tensor_frac": layer_fraction(cfg, ms_step, ms / 1e3, pk, fp8),
         "kernels": kernels,

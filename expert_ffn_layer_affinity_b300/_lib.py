@@ -41,6 +41,8 @@ SIGNATURES = {
     "moe_permute": (I, [P, I, I, I, P, I, P, P, P, P, P, P, Z, P]),
     "moe_permute_static": (I, [P, I, I, I, P, I, P, P, P, P, P, P]),
     "moe_grouped_swiglu": (I, [P, P, I, I, I, I, P, P, P, P, P, P, P]),
+    "moe_tile_expert_weights": (I, [P, P, P, I, I, I, P, P, P]),
+    "moe_grouped_swiglu_tiled": (I, [P, P, I, I, I, I, P, P, P, P, P, P]),
     "moe_combine": (I, [P, P, P, P, I, I, I, P, P]),
     "moe_replica_plan": (I, [P, I, I, P, P, P]),
     "moe_replica_remap": (I, [P, I, I, I, I, P, P, P, P]),
@@ -151,6 +153,22 @@ def moe_permute_static(topk_idx, T, K, E, x, d, expert_offsets, row_of, tok_of, 
                                  _ptr(row_of), _ptr(tok_of), _ptr(x_perm), _ptr(status_dev),
                                  _stream(stream))
     return _check("moe_permute_static", r) if check else r
+
+
+def moe_tile_expert_weights(w1, w3, w2, n_groups, I, d, w13_tiled, w2_tiled, stream=None,
+                            check=True):
+    """Box-contiguous copies of the expert weights (see include/moe.h)."""
+    r = lib().moe_tile_expert_weights(_ptr(w1), _ptr(w3), _ptr(w2), n_groups, I, d,
+                                      _ptr(w13_tiled), _ptr(w2_tiled), _stream(stream))
+    return _check("moe_tile_expert_weights", r) if check else r
+
+
+def moe_grouped_swiglu_tiled(a, group_offsets, n_groups, R, d, I, w13_tiled, w2_tiled, h, y,
+                             status_dev, stream=None, check=True):
+    r = lib().moe_grouped_swiglu_tiled(_ptr(a), _ptr(group_offsets), n_groups, R, d, I,
+                                       _ptr(w13_tiled), _ptr(w2_tiled), _ptr(h), _ptr(y),
+                                       _ptr(status_dev), _stream(stream))
+    return _check("moe_grouped_swiglu_tiled", r) if check else r
 
 
 def moe_grouped_swiglu(a, group_offsets, n_groups, R, d, I, w1, w3, w2, h, y, status_dev,

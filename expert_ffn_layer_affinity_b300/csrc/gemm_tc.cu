@@ -158,6 +158,7 @@ struct GemmParams {
   const float* col_offset;  // router: per-expert logit offset or nullptr
   int w13_3d;               // SwiGLU: tmA is a 3-D map fetching w1 and w3 rows in one box
   int32_t* status;
+  int w_tiled;  // expert modes: weights in the box-contiguous layout (see tile_expert_weights)
 };
 
 __device__ __forceinline__ int group_offset(const GemmParams& p, int g) {
@@ -310,7 +311,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int j = 0; j < nbox; ++j) {
               const uint32_t aj = sa + static_cast<uint32_t>(j * C::kA);
               const int kx = (kb0 + j) * BK;
-              if (MODE == MODE_SWIGLU && p.w13_3d) {
+              if ((MODE == MODE_SWIGLU || MODE == MODE_DOWN) && p.w_tiled) {
+                // box-contiguous weights: box (group, row tile of this CTA,
+                // k-block) is 128 rows of 128 B at row (index * 128) of a
+                // [boxes * 128, 64] view; SwiGLU row tiles are 64 w1 rows
+                // followed by the same 64 w3 rows
+                const int row_tiles = MODE == MODE_SWIGLU ? p.N / 64 : p.N / 128;
+                const long long box =
+                    (static_cast<long long>(g) * row_tiles + n * 2 + static_cast<int>(rank)) *
+                        p.num_kb + (kb0 + j);
+                tma_load_2d_pair(aj, &tmA, fb, 0, static_cast<int>(box * 128), pol_w);
+              } else if (MODE == MODE_SWIGLU && p.w13_3d) {
                 tma_load_3d_pair(aj, &tmA, fb, kx, w_row, 0, pol_w);  // w1 rows, then w3 rows
               } else if (MODE == MODE_SWIGLU) {
                 tma_load_2d_pair(aj, &tmA, fb, kx, w_row, pol_w);
@@ -664,6 +675,99 @@ cudaError_t launch_grouped_swiglu(const uint16_t* a, const int32_t* offsets, int
   GemmParams p2 = p1;
   p2.out_a = p2.out_c = nullptr;
   p2.w13_3d = 0;
+  p2.N = d;
+  p2.num_kb = I / BK;
+  p2.a_k_wrap_kb = I / BK;
+  p2.w_rows_per_group = d;
+  p2.out = y;
+  p2.ldo = d;
+  const int mt2 = (R + C2::kTokTile - 1) / C2::kTokTile + G;
+  return launch_gemm<MODE_DOWN>(tw2, tw2, th, p2, mt2 * ((d + 255) / 256), s);
+}
+
+namespace {
+// out = the box-contiguous copy of a weight tensor (see launch_tile_expert_weights):
+// 16-byte chunk q of the output holds source row `src_row`, columns
+// kb*64 + c8*8 .. +7.
+__global__ void __launch_bounds__(256) tile_weights_kernel(const uint4* __restrict__ w1,
+                                                           const uint4* __restrict__ w3,
+                                                           long long G, int rows, int cols,
+                                                           int tile_rows, uint4* __restrict__ out) {
+  const int kbs = cols / 64;
+  const int tiles = rows / tile_rows;  // row tiles per group (SwiGLU: 64 rows of w1 and of w3)
+  const int box_rows = w3 ? 2 * tile_rows : tile_rows;
+  const long long n = G * tiles * kbs * box_rows * 8;
+  for (long long q = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; q < n;
+       q += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const int c8 = static_cast<int>(q & 7);
+    long long t = q >> 3;
+    const int r = static_cast<int>(t % box_rows);
+    t /= box_rows;
+    const int kb = static_cast<int>(t % kbs);
+    t /= kbs;
+    const int tile = static_cast<int>(t % tiles);
+    const long long g = t / tiles;
+    const bool second = w3 != nullptr && r >= tile_rows;
+    const long long src_row = g * rows + static_cast<long long>(tile) * tile_rows +
+                              (second ? r - tile_rows : r);
+    const uint4* src = second ? w3 : w1;
+    out[q] = src[src_row * (cols / 8) + kb * 8 + c8];
+  }
+}
+}  // namespace
+
+// Box-contiguous copies of the expert weights, so that every 128-row x
+// 64-column box the grouped GEMM stages is 16 KB of consecutive memory (one
+// DRAM stream per box instead of 128 strided rows):
+//   w13_tiled [G][I/64][d/64][128][64]: rows 0..63 of a box are w1 rows
+//     t*64 .. t*64+63 of group g, rows 64..127 the same rows of w3, columns
+//     kb*64 .. kb*64+63;
+//   w2_tiled  [G][d/128][I/64][128][64]: rows t*128 .. t*128+127 of w2[g].
+cudaError_t launch_tile_expert_weights(const uint16_t* w1, const uint16_t* w3, const uint16_t* w2,
+                                       int G, int I, int d, uint16_t* w13_tiled,
+                                       uint16_t* w2_tiled, cudaStream_t s) {
+  const int blocks = sm_count() * 8;
+  if (w1 && w3 && w13_tiled)
+    tile_weights_kernel<<<blocks, 256, 0, s>>>(reinterpret_cast<const uint4*>(w1),
+                                               reinterpret_cast<const uint4*>(w3), G, I, d, 64,
+                                               reinterpret_cast<uint4*>(w13_tiled));
+  if (w2 && w2_tiled)
+    tile_weights_kernel<<<blocks, 256, 0, s>>>(reinterpret_cast<const uint4*>(w2), nullptr, G, d,
+                                               I, 128, reinterpret_cast<uint4*>(w2_tiled));
+  return cudaGetLastError();
+}
+
+// The grouped SwiGLU experts on box-contiguous weights (same arithmetic and
+// order as launch_grouped_swiglu, so bit-identical outputs).
+cudaError_t launch_grouped_swiglu_tiled(const uint16_t* a, const int32_t* offsets, int G, int R,
+                                        int d, int I, const uint16_t* w13_tiled,
+                                        const uint16_t* w2_tiled, uint16_t* h, uint16_t* y,
+                                        int32_t* status, cudaStream_t s) {
+  if (R == 0 || G == 0) return cudaSuccess;
+  if (G > kMaxGroups) return cudaErrorInvalidValue;
+  using C1 = Cfg<MODE_SWIGLU>;
+  using C2 = Cfg<MODE_DOWN>;
+  CUtensorMap tw13, tx, tw2, th;
+  if (!make_map(&tw13, w13_tiled, 64, static_cast<uint64_t>(G) * (I / 64) * (d / 64) * 128, 128) ||
+      !make_map(&tw2, w2_tiled, 64, static_cast<uint64_t>(G) * (d / 128) * (I / 64) * 128, 128) ||
+      !make_map(&tx, a, d, R, 128) || !make_map(&th, h, I, R, 128))
+    return cudaErrorInvalidValue;
+  GemmParams p1{};
+  p1.w_tiled = 1;
+  p1.group_offsets = offsets;
+  p1.G = G;
+  p1.N = I;
+  p1.R = R;
+  p1.num_kb = d / BK;
+  p1.a_k_wrap_kb = d / BK;
+  p1.w_rows_per_group = I;
+  p1.out = h;
+  p1.ldo = I;
+  p1.status = status;
+  const int mt1 = (R + C1::kTokTile - 1) / C1::kTokTile + G;
+  cudaError_t e = launch_gemm<MODE_SWIGLU>(tw13, tw13, tx, p1, mt1 * ((I + 127) / 128), s);
+  if (e != cudaSuccess) return e;
+  GemmParams p2 = p1;
   p2.N = d;
   p2.num_kb = I / BK;
   p2.a_k_wrap_kb = I / BK;

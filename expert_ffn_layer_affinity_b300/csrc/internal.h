@@ -96,6 +96,15 @@ cudaError_t launch_grouped_swiglu(const uint16_t* a, const int32_t* offsets, int
                                   cudaStream_t s, uint16_t* a_out = nullptr,
                                   uint16_t* c_out = nullptr);
 
+// Box-contiguous expert weights and the grouped SwiGLU reading them.
+cudaError_t launch_tile_expert_weights(const uint16_t* w1, const uint16_t* w3, const uint16_t* w2,
+                                       int G, int I, int d, uint16_t* w13_tiled,
+                                       uint16_t* w2_tiled, cudaStream_t s);
+cudaError_t launch_grouped_swiglu_tiled(const uint16_t* a, const int32_t* offsets, int G, int R,
+                                        int d, int I, const uint16_t* w13_tiled,
+                                        const uint16_t* w2_tiled, uint16_t* h, uint16_t* y,
+                                        int32_t* status, cudaStream_t s);
+
 // ---- FP8 path (quant_fp8.cu, gemm_fp8.cu)
 cudaError_t launch_quantize_rows(const uint16_t* in, int rows, int cols, uint8_t* q, float* s,
                                  int ld_s, cudaStream_t st);

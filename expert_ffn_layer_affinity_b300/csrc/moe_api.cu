@@ -221,6 +221,46 @@ moe_status moe_permute_static(const int32_t* topk_idx, int T, int K, int E, cons
                                     static_cast<cudaStream_t>(stream)));
 }
 
+moe_status moe_tile_expert_weights(const void* w1_bf16, const void* w3_bf16, const void* w2_bf16,
+                                   int n_groups, int I, int d, void* w13_tiled_bf16,
+                                   void* w2_tiled_bf16, moe_stream_t stream) {
+  MOE_TRACE();
+  if (n_groups < 1 || I < 1 || d < 1) return MOE_ERR_INVALID_ARG;
+  const bool has13 = w1_bf16 || w3_bf16 || w13_tiled_bf16;
+  const bool has2 = w2_bf16 || w2_tiled_bf16;
+  if (!has13 && !has2) return MOE_ERR_INVALID_ARG;
+  if (has13 && (!w1_bf16 || !w3_bf16 || !w13_tiled_bf16)) return MOE_ERR_INVALID_ARG;
+  if (has2 && (!w2_bf16 || !w2_tiled_bf16)) return MOE_ERR_INVALID_ARG;
+  if (d % 128 || I % 64 || n_groups > 512) return MOE_ERR_UNSUPPORTED_SHAPE;
+  for (const void* q : {w1_bf16, w3_bf16, w2_bf16, static_cast<const void*>(w13_tiled_bf16),
+                        static_cast<const void*>(w2_tiled_bf16)})
+    if (q && !aligned16(q)) return MOE_ERR_UNSUPPORTED_SHAPE;
+  return cuda_status(launch_tile_expert_weights(
+      static_cast<const uint16_t*>(w1_bf16), static_cast<const uint16_t*>(w3_bf16),
+      static_cast<const uint16_t*>(w2_bf16), n_groups, I, d, static_cast<uint16_t*>(w13_tiled_bf16),
+      static_cast<uint16_t*>(w2_tiled_bf16), static_cast<cudaStream_t>(stream)));
+}
+
+moe_status moe_grouped_swiglu_tiled(const void* a_bf16, const int32_t* group_offsets,
+                                    int n_groups, int R, int d, int I, const void* w13_tiled_bf16,
+                                    const void* w2_tiled_bf16, void* h_bf16, void* y_bf16,
+                                    int32_t* status_dev, moe_stream_t stream) {
+  MOE_TRACE();
+  if (R < 0 || n_groups < 1 || d < 1 || I < 1) return MOE_ERR_INVALID_ARG;
+  if (R > 0 && (!a_bf16 || !group_offsets || !w13_tiled_bf16 || !w2_tiled_bf16 || !h_bf16 ||
+                !y_bf16))
+    return MOE_ERR_INVALID_ARG;
+  if (d % 128 || I % 64 || n_groups > 512) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (R > 0 && (!aligned16(a_bf16) || !aligned16(w13_tiled_bf16) || !aligned16(w2_tiled_bf16) ||
+                !aligned16(h_bf16) || !aligned16(y_bf16)))
+    return MOE_ERR_UNSUPPORTED_SHAPE;
+  return cuda_status(launch_grouped_swiglu_tiled(
+      static_cast<const uint16_t*>(a_bf16), group_offsets, n_groups, R, d, I,
+      static_cast<const uint16_t*>(w13_tiled_bf16), static_cast<const uint16_t*>(w2_tiled_bf16),
+      static_cast<uint16_t*>(h_bf16), static_cast<uint16_t*>(y_bf16), status_dev,
+      static_cast<cudaStream_t>(stream)));
+}
+
 moe_status moe_grouped_swiglu(const void* a_bf16, const int32_t* group_offsets, int n_groups,
                               int R, int d, int I, const void* w1_bf16, const void* w3_bf16,
                               const void* w2_bf16, void* h_bf16, void* y_bf16,

@@ -15,6 +15,13 @@ Serving layouts from the report's deployment (qwbw.cn essay, "9个专家",
                     are spread over its copies.
 Physical expert weights are then laid out [E experts][copies][shared].
 
+tiled_weights (default: on whenever it applies, i.e. a bf16 forward layer in
+the standard layout with d % 128 == 0 and I % 64 == 0) keeps box-contiguous
+copies of the routed and shared expert weights (moe_tile_expert_weights) and
+runs the expert GEMMs on them (moe_grouped_swiglu_tiled): the same arithmetic
+in the same order, so bit-identical outputs, with every staged weight box one
+run of consecutive memory.
+
 precision="fp8" runs the expert GEMMs in E4M3 with fine-grained scaling
 (qwbw.cn essay on the report, the FP8 training passage; weigao.cc section
 "6. FP8 Training"): weights are quantized once per 128 x 128 block when the
@@ -40,7 +47,8 @@ class MoELayer:
     def __init__(self, cfg: LayerConfig, params: dict, max_T: int | None = None,
                  device: str = "cuda", keep_affinity: bool = False,
                  shared_stream: bool = False, shared_as_routed: bool = False,
-                 n_redundant: int = 0, precision: str = "bf16", training: bool = False):
+                 n_redundant: int = 0, precision: str = "bf16", training: bool = False,
+                 tiled_weights: bool | None = None):
         if precision not in ("bf16", "fp8"):
             raise ValueError(f"precision must be 'bf16' or 'fp8', not {precision!r}")
         if training and (precision != "bf16" or shared_as_routed or n_redundant):
@@ -103,6 +111,25 @@ class MoELayer:
             self.slots = torch.arange(E + n_redundant, dtype=torch.int32, device=dev)
         self.w_split = torch.empty(E, 3 * d, dtype=torch.bfloat16, device=dev)
         L.moe_router_prepare(self.w_r, E, d, self.w_split)
+        # box-contiguous copies of the expert weights for the forward GEMMs
+        # (moe_tile_expert_weights): the standard layout, whose boxes are
+        # strided rows, stays for the backward pass and the other layouts
+        can_tile = (d % 128 == 0 and I % 64 == 0 and not self.fp8 and not shared_as_routed
+                    and not n_redundant and not training)
+        self.tiled = can_tile if tiled_weights is None else bool(tiled_weights)
+        if self.tiled and not can_tile:
+            raise ValueError("tiled weights need bf16, the standard layout, d % 128 == 0 and "
+                             "I % 64 == 0")
+        if self.tiled:
+            bf = torch.bfloat16
+            self.w13_t = torch.empty(E, I // 64, d // 64, 128, 64, dtype=bf, device=dev)
+            self.w2_t = torch.empty(E, d // 128, I // 64, 128, 64, dtype=bf, device=dev)
+            L.moe_tile_expert_weights(self.w1, self.w3, self.w2, E, I, d, self.w13_t, self.w2_t)
+            nI = ns * I
+            self.ws13_t = torch.empty(1, nI // 64, d // 64, 128, 64, dtype=bf, device=dev)
+            self.ws2_t = torch.empty(1, d // 128, nI // 64, 128, 64, dtype=bf, device=dev)
+            L.moe_tile_expert_weights(self.ws1, self.ws3, self.ws2, 1, nI, d, self.ws13_t,
+                                      self.ws2_t)
         if self.fp8:
             self._quantize_weights()
         self.keep_affinity = keep_affinity
@@ -266,6 +293,10 @@ class MoELayer:
                 L.moe_grouped_swiglu_save(x, self.shared_offsets, 1, T, c.d, c.n_shared * c.I,
                                           self.ws1, self.ws3, self.ws2, self.h_sh, self.y_sh,
                                           self.pre_a_sh, self.pre_c_sh, self.status, s)
+            elif self.tiled:
+                L.moe_grouped_swiglu_tiled(x, self.shared_offsets, 1, T, c.d, c.n_shared * c.I,
+                                           self.ws13_t, self.ws2_t, self.h_sh, self.y_sh,
+                                           self.status, s)
             else:
                 L.moe_grouped_swiglu(x, self.shared_offsets, 1, T, c.d, c.n_shared * c.I, self.ws1,
                                      self.ws3, self.ws2, self.h_sh, self.y_sh, self.status, s)
@@ -280,6 +311,10 @@ class MoELayer:
             L.moe_grouped_swiglu_save(self.x_perm, self.offsets, self.E_phys, R, c.d, c.I, self.w1,
                                       self.w3, self.w2, self.h, self.y_perm, self.pre_a,
                                       self.pre_c, self.status, stream)
+        elif self.tiled:
+            L.moe_grouped_swiglu_tiled(self.x_perm, self.offsets, self.E_phys, R, c.d, c.I,
+                                       self.w13_t, self.w2_t, self.h, self.y_perm, self.status,
+                                       stream)
         else:
             L.moe_grouped_swiglu(self.x_perm, self.offsets, self.E_phys, R, c.d, c.I, self.w1,
                                  self.w3, self.w2, self.h, self.y_perm, self.status, stream)

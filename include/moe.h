@@ -183,6 +183,34 @@ moe_status moe_grouped_swiglu(const void* a_bf16, const int32_t* group_offsets, 
                               const void* w2_bf16, void* h_bf16, void* y_bf16,
                               int32_t* status_dev, moe_stream_t stream);
 
+/* Box-contiguous copies of expert weights for moe_grouped_swiglu_tiled.  The
+ * grouped GEMM stages its weights as boxes of 128 rows x 64 columns; in the
+ * [rows, cols] layout above every box is 128 strided 128-byte pieces, in
+ * these copies it is 16 KB of consecutive memory, which the GPU's memory
+ * streams more efficiently.  Same values, rearranged (a one-time copy, like
+ * moe_router_prepare; the method is unchanged):
+ *  w13_tiled [G][I/64][d/64][128][64] bf16: box (g, t, kb) holds rows
+ *    t*64 .. t*64+63 of w1[g] (box rows 0..63) and the same rows of w3[g]
+ *    (box rows 64..127), columns kb*64 .. kb*64+63;
+ *  w2_tiled  [G][d/128][I/64][128][64] bf16: box (g, t, kb) holds rows
+ *    t*128 .. t*128+127 of w2[g], columns kb*64 .. kb*64+63.
+ * w1, w3 [G, I, d] and w2 [G, d, I] as for moe_grouped_swiglu; either the
+ * w1/w3/w13_tiled triple or the w2/w2_tiled pair may be all NULL to skip it.
+ * d % 128 == 0 and I % 64 == 0, else MOE_ERR_UNSUPPORTED_SHAPE. */
+moe_status moe_tile_expert_weights(const void* w1_bf16, const void* w3_bf16, const void* w2_bf16,
+                                   int n_groups, int I, int d, void* w13_tiled_bf16,
+                                   void* w2_tiled_bf16, moe_stream_t stream);
+
+/* moe_grouped_swiglu on the box-contiguous weights of moe_tile_expert_weights:
+ * the same kernels, staging the same boxes in the same order, so h and y are
+ * bit-identical to moe_grouped_swiglu's on the same weights.  Requires
+ * d % 128 == 0 and I % 64 == 0.  Same expert FFN (weigao.cc notes, §2 table
+ * row "DeepSeekMoE"). */
+moe_status moe_grouped_swiglu_tiled(const void* a_bf16, const int32_t* group_offsets,
+                                    int n_groups, int R, int d, int I, const void* w13_tiled_bf16,
+                                    const void* w2_tiled_bf16, void* h_bf16, void* y_bf16,
+                                    int32_t* status_dev, moe_stream_t stream);
+
 /* The same call for a training step: also writes the pre-activations
  * pre_a[r] = a[r] . w1[g]^T and pre_c[r] = a[r] . w3[g]^T (bf16 [R, I] each),
  * which the backward pass needs (da = dh c silu'(a), dc = dh silu(a)), from

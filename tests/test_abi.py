@@ -84,6 +84,26 @@ def test_other_calls_reject_bad_arguments():
     assert moe.moe_router_prepare(FAKE, 16, 65, FAKE, stream=0, check=False) == moe.MOE_ERR_UNSUPPORTED_SHAPE
 
 
+def test_tiled_weight_calls_reject_bad_arguments():
+    # d must be a multiple of 128 and I of 64 (whole boxes); pointers 16-byte aligned
+    assert moe.moe_tile_expert_weights(FAKE, FAKE, FAKE, 4, 128, 192, FAKE, FAKE, stream=0,
+                                       check=False) == moe.MOE_ERR_UNSUPPORTED_SHAPE
+    assert moe.moe_tile_expert_weights(FAKE, FAKE, FAKE, 4, 96, 256, FAKE, FAKE, stream=0,
+                                       check=False) == moe.MOE_ERR_UNSUPPORTED_SHAPE
+    assert moe.moe_tile_expert_weights(FAKE, None, FAKE, 4, 128, 256, FAKE, FAKE, stream=0,
+                                       check=False) == moe.MOE_ERR_INVALID_ARG
+    assert moe.moe_tile_expert_weights(None, None, None, 4, 128, 256, None, None, stream=0,
+                                       check=False) == moe.MOE_ERR_INVALID_ARG
+    assert moe.moe_tile_expert_weights(FAKE + 8, FAKE, None, 4, 128, 256, FAKE, None, stream=0,
+                                       check=False) == moe.MOE_ERR_UNSUPPORTED_SHAPE
+    assert moe.moe_grouped_swiglu_tiled(FAKE, FAKE, 4, 128, 192, 128, FAKE, FAKE, FAKE, FAKE,
+                                        None, stream=0, check=False) == moe.MOE_ERR_UNSUPPORTED_SHAPE
+    assert moe.moe_grouped_swiglu_tiled(None, FAKE, 4, 128, 256, 128, FAKE, FAKE, FAKE, FAKE,
+                                        None, stream=0, check=False) == moe.MOE_ERR_INVALID_ARG
+    assert moe.moe_grouped_swiglu_tiled(FAKE, FAKE, 4, 128, 256, 128, FAKE + 8, FAKE, FAKE, FAKE,
+                                        None, stream=0, check=False) == moe.MOE_ERR_UNSUPPORTED_SHAPE
+
+
 def test_binding_raises_on_error():
     with pytest.raises(moe.MoEError):
         moe.moe_combine(None, FAKE, FAKE, None, 4, 2, 16, FAKE, stream=0)

@@ -151,3 +151,70 @@ def test_grouped_swiglu_w1_w3_in_one_allocation(sizes, d, I):
     assert sync_status(status) == 0 and st1 == 0
     assert torch.equal(h.cpu().view(torch.int16), h_sep.view(torch.int16))
     assert torch.equal(y.cpu().view(torch.int16), y_sep.view(torch.int16))
+
+
+def tiled_reference(w1, w3, w2):
+    """The box-contiguous arrangement of include/moe.h, written with torch
+    reshapes (w1, w3 [G, I, d]; w2 [G, d, I])."""
+    G, I, d = w1.shape
+    a = w1.reshape(G, I // 64, 64, d // 64, 64).permute(0, 1, 3, 2, 4)
+    c = w3.reshape(G, I // 64, 64, d // 64, 64).permute(0, 1, 3, 2, 4)
+    w13t = torch.cat([a, c], dim=3).contiguous()
+    w2t = w2.reshape(G, d // 128, 128, I // 64, 64).permute(0, 1, 3, 2, 4).contiguous()
+    return w13t, w2t
+
+
+def run_tiled(a, offsets, w1, w3, w2):
+    R, d = a.shape
+    G, I, _ = w1.shape
+    dev = "cuda"
+    w13t = torch.empty(G, I // 64, d // 64, 128, 64, dtype=torch.bfloat16, device=dev)
+    w2t = torch.empty(G, d // 128, I // 64, 128, 64, dtype=torch.bfloat16, device=dev)
+    moe.moe_tile_expert_weights(w1.to(dev), w3.to(dev), w2.to(dev), G, I, d, w13t, w2t)
+    h = torch.zeros(R, I, dtype=torch.bfloat16, device=dev)
+    y = torch.zeros(R, d, dtype=torch.bfloat16, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    moe.moe_grouped_swiglu_tiled(a.to(dev), offsets.to(dev), G, R, d, I, w13t, w2t, h, y, status)
+    st = sync_status(status)
+    return h.cpu(), y.cpu(), st, w13t.cpu(), w2t.cpu()
+
+
+@pytest.mark.parametrize("sizes,d,I", [
+    ([128], 256, 128),
+    ([1], 256, 128),
+    ([0, 129, 0, 127, 1, 256, 300], 256, 128),
+    ([200, 57, 0, 513], 512, 192),           # I % 128 == 64: column tail in GEMM1
+    ([300, 17], 384, 128),                   # d % 256 == 128: column tail in GEMM2
+    (list(range(1, 257, 8)) + [256 + 9, 256 + 100, 256 + 255, 512 + 16], 256, 128),
+])
+def test_grouped_swiglu_tiled_bit_identical(sizes, d, I):
+    """Box-contiguous weights: the layout is the one include/moe.h states, and
+    h and y equal the standard-layout call's bit for bit (same boxes, same
+    order), which the oracle tests above pin."""
+    G = len(sizes)
+    offsets = torch.tensor([0] + list(np.cumsum(sizes)), dtype=torch.int32)
+    R = int(offsets[-1])
+    a = synth.make_ffn_rows(R, d, seed=R + d + 1)
+    w1, w3, w2 = weights(G, I, d, seed=G + I + 1)
+    h0, y0, st0 = run_grouped(a, offsets, w1, w3, w2)
+    h1, y1, st1, w13t, w2t = run_tiled(a, offsets, w1, w3, w2)
+    assert st0 == 0 and st1 == 0
+    r13, r2 = tiled_reference(w1, w3, w2)
+    assert torch.equal(w13t.view(torch.int16), r13.view(torch.int16))
+    assert torch.equal(w2t.view(torch.int16), r2.view(torch.int16))
+    assert torch.equal(h1.view(torch.int16), h0.view(torch.int16))
+    assert torch.equal(y1.view(torch.int16), y0.view(torch.int16))
+
+
+def test_grouped_swiglu_tiled_v3_shape():
+    """One V3-shaped expert (d=7168, I=2048) with 300 rows and an empty group:
+    tiled equals standard bit for bit."""
+    d, I = 7168, 2048
+    offsets = torch.tensor([0, 0, 300], dtype=torch.int32)
+    a = synth.make_ffn_rows(300, d, seed=3)
+    w1, w3, w2 = weights(2, I, d, seed=5, std=0.02)
+    h0, y0, st0 = run_grouped(a, offsets, w1, w3, w2)
+    h1, y1, st1, _, _ = run_tiled(a, offsets, w1, w3, w2)
+    assert st0 == 0 and st1 == 0
+    assert torch.equal(h1.view(torch.int16), h0.view(torch.int16))
+    assert torch.equal(y1.view(torch.int16), y0.view(torch.int16))

@@ -47,6 +47,23 @@ def test_tiny_layer_deterministic():
     assert torch.equal(a.view(torch.int16), b.view(torch.int16))
 
 
+def test_layer_tiled_weights_bit_identical():
+    """The forward layer's default box-contiguous expert weights give the
+    standard layout's output bit for bit (mid shapes: two shared experts,
+    I = 1408)."""
+    cfg = synth.CONFIGS["mid"]
+    p = synth.make_params(cfg, "cpu")
+    x = synth.make_tokens(cfg, 0, "cuda")
+    a = MoELayer(cfg, p)
+    b = MoELayer(cfg, p, tiled_weights=False)
+    assert a.tiled and not b.tiled
+    ya = a.forward(x).clone()
+    yb = b.forward(x).clone()
+    torch.cuda.synchronize()
+    assert a.device_status() == 0 and b.device_status() == 0
+    assert torch.equal(ya.view(torch.int16), yb.view(torch.int16))
+
+
 def test_tiny_layer_odd_token_counts():
     cfg = synth.CONFIGS["tiny"]
     p = synth.make_params(cfg, "cpu")
