@@ -314,8 +314,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               if ((MODE == MODE_SWIGLU || MODE == MODE_DOWN) && p.w_tiled) {
                 // box-contiguous weights: box (group, row tile of this CTA,
                 // k-block) is 128 rows of 128 B at row (index * 128) of a
-                // [boxes * 128, 64] view; SwiGLU row tiles are 64 w1 rows
-                // followed by the same 64 w3 rows
+                // [boxes * 128, 64] view; SwiGLU boxes alternate w1 and w3 rows
                 const int row_tiles = MODE == MODE_SWIGLU ? p.N / 64 : p.N / 128;
                 const long long box =
                     (static_cast<long long>(g) * row_tiles + n * 2 + static_cast<int>(rank)) *
@@ -516,7 +515,33 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (valid > 32) valid = 32;
           const long long last = row0 + c + valid;
           if (last > p.R) valid -= static_cast<int>(last - p.R);
-          if (MODE == MODE_SWIGLU) {
+          if (MODE == MODE_SWIGLU && p.w_tiled) {
+            // box-contiguous weights interleave the rows: TMEM lane 2i holds
+            // the gate (w1 row i) and lane 2i + 1 the up value (w3 row i) of
+            // output column i, so a lane pair of this warp owns 16 columns;
+            // the even lane finishes tokens 0..15 of the chunk, the odd lane
+            // tokens 16..31, after swapping halves with one shuffle each
+            const bool odd = (lane & 1) != 0;
+            const int tcol = n * C::kColTile + 64 * static_cast<int>(rank) + 16 * q;
+            __nv_bfloat16* st = reinterpret_cast<__nv_bfloat16*>(xp);  // [32 tokens][16 columns]
+#pragma unroll
+            for (int k = 0; k < 16; ++k) {
+              const float mine = __uint_as_float(odd ? v[k] : v[16 + k]);
+              const float other = __shfl_xor_sync(0xFFFFFFFFu, mine, 1);
+              const float gate = odd ? other : __uint_as_float(v[k]);
+              const float up = odd ? __uint_as_float(v[16 + k]) : other;
+              const float hv = gate * __frcp_rn(1.0f + __expf(-gate)) * up;
+              st[((odd ? 16 : 0) + k) * 16 + (lane >> 1)] = __float2bfloat16_rn(hv);
+            }
+            __syncwarp();
+            if (tcol < p.N && lane < valid) {
+              const uint4* src = reinterpret_cast<const uint4*>(xp + lane * 32);
+              uint4* dst = reinterpret_cast<uint4*>(out + (row0 + c + lane) * p.ldo + tcol);
+              dst[0] = src[0];
+              dst[1] = src[1];
+            }
+            __syncwarp();
+          } else if (MODE == MODE_SWIGLU) {
             // pair (q, q + 2): lanes 64..127 (up) hand over to lanes 0..63 (gate)
             const int pr = q & 1, xb = static_cast<int>(xchunk & 1u);
             const uint32_t xph = (xchunk >> 1) & 1u;
@@ -707,9 +732,10 @@ __global__ void __launch_bounds__(256) tile_weights_kernel(const uint4* __restri
     t /= kbs;
     const int tile = static_cast<int>(t % tiles);
     const long long g = t / tiles;
-    const bool second = w3 != nullptr && r >= tile_rows;
+    // SwiGLU boxes alternate the rows: row 2i is w1 row i, row 2i + 1 is w3 row i
+    const bool second = w3 != nullptr && (r & 1);
     const long long src_row = g * rows + static_cast<long long>(tile) * tile_rows +
-                              (second ? r - tile_rows : r);
+                              (w3 != nullptr ? (r >> 1) : r);
     const uint4* src = second ? w3 : w1;
     out[q] = src[src_row * (cols / 8) + kb * 8 + c8];
   }
@@ -719,9 +745,10 @@ __global__ void __launch_bounds__(256) tile_weights_kernel(const uint4* __restri
 // Box-contiguous copies of the expert weights, so that every 128-row x
 // 64-column box the grouped GEMM stages is 16 KB of consecutive memory (one
 // DRAM stream per box instead of 128 strided rows):
-//   w13_tiled [G][I/64][d/64][128][64]: rows 0..63 of a box are w1 rows
-//     t*64 .. t*64+63 of group g, rows 64..127 the same rows of w3, columns
-//     kb*64 .. kb*64+63;
+//   w13_tiled [G][I/64][d/64][128][64]: row 2i of a box is w1 row t*64 + i of
+//     group g and row 2i + 1 the same row of w3 (so the gate and up values of
+//     an output column land in neighbouring TMEM lanes of one epilogue warp),
+//     columns kb*64 .. kb*64+63;
 //   w2_tiled  [G][d/128][I/64][128][64]: rows t*128 .. t*128+127 of w2[g].
 cudaError_t launch_tile_expert_weights(const uint16_t* w1, const uint16_t* w3, const uint16_t* w2,
                                        int G, int I, int d, uint16_t* w13_tiled,

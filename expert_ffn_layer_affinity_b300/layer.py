@@ -20,7 +20,7 @@ the standard layout with d % 128 == 0 and I % 64 == 0) keeps box-contiguous
 copies of the routed and shared expert weights (moe_tile_expert_weights) and
 runs the expert GEMMs on them (moe_grouped_swiglu_tiled): the same arithmetic
 in the same order, so bit-identical outputs, with every staged weight box one
-run of consecutive memory.
+run of consecutive memory and the SwiGLU finished inside each epilogue warp.
 
 precision="fp8" runs the expert GEMMs in E4M3 with fine-grained scaling
 (qwbw.cn essay on the report, the FP8 training passage; weigao.cc section

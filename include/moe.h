@@ -190,8 +190,8 @@ moe_status moe_grouped_swiglu(const void* a_bf16, const int32_t* group_offsets, 
  * streams more efficiently.  Same values, rearranged (a one-time copy, like
  * moe_router_prepare; the method is unchanged):
  *  w13_tiled [G][I/64][d/64][128][64] bf16: box (g, t, kb) holds rows
- *    t*64 .. t*64+63 of w1[g] (box rows 0..63) and the same rows of w3[g]
- *    (box rows 64..127), columns kb*64 .. kb*64+63;
+ *    t*64 .. t*64+63 of w1[g] and of w3[g], alternating (box row 2i is w1
+ *    row t*64+i, box row 2i+1 is w3 row t*64+i), columns kb*64 .. kb*64+63;
  *  w2_tiled  [G][d/128][I/64][128][64] bf16: box (g, t, kb) holds rows
  *    t*128 .. t*128+127 of w2[g], columns kb*64 .. kb*64+63.
  * w1, w3 [G, I, d] and w2 [G, d, I] as for moe_grouped_swiglu; either the
@@ -202,8 +202,12 @@ moe_status moe_tile_expert_weights(const void* w1_bf16, const void* w3_bf16, con
                                    void* w2_tiled_bf16, moe_stream_t stream);
 
 /* moe_grouped_swiglu on the box-contiguous weights of moe_tile_expert_weights:
- * the same kernels, staging the same boxes in the same order, so h and y are
- * bit-identical to moe_grouped_swiglu's on the same weights.  Requires
+ * the same kernels and the same arithmetic in the same order, so h and y are
+ * bit-identical to moe_grouped_swiglu's on the same weights.  The alternating
+ * w1/w3 rows put each output column's gate and up values in neighbouring
+ * lanes of one epilogue warp, which finishes the SwiGLU with a register
+ * shuffle instead of a shared-memory exchange between warps (faster where
+ * the reduction is short: the mid layer's d = 2048).  Requires
  * d % 128 == 0 and I % 64 == 0.  Same expert FFN (weigao.cc notes, §2 table
  * row "DeepSeekMoE"). */
 moe_status moe_grouped_swiglu_tiled(const void* a_bf16, const int32_t* group_offsets,

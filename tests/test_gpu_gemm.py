@@ -159,7 +159,8 @@ def tiled_reference(w1, w3, w2):
     G, I, d = w1.shape
     a = w1.reshape(G, I // 64, 64, d // 64, 64).permute(0, 1, 3, 2, 4)
     c = w3.reshape(G, I // 64, 64, d // 64, 64).permute(0, 1, 3, 2, 4)
-    w13t = torch.cat([a, c], dim=3).contiguous()
+    # box row 2i = w1 row i, row 2i + 1 = w3 row i
+    w13t = torch.stack([a, c], dim=4).reshape(G, I // 64, d // 64, 128, 64).contiguous()
     w2t = w2.reshape(G, d // 128, 128, I // 64, 64).permute(0, 1, 3, 2, 4).contiguous()
     return w13t, w2t
 
