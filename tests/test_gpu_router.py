@@ -167,6 +167,11 @@ def test_router_split_is_exact():
     (300, 7168, 256, 8, 8, 4, 2.5, None),
     (129, 512, 8, 3, 4, 2, 2.5, None),
     (1, 1024, 128, 4, 1, 1, 1.0, None),
+    # ragged last token tile with four expert tiles; a split V3-width
+    # batch; the V3 batch itself (one split)
+    (3000, 1024, 512, 8, 8, 4, 2.5, None),
+    (2048, 7168, 256, 8, 8, 4, 2.5, None),
+    (8192, 7168, 256, 8, 8, 4, 2.5, None),
 ])
 def test_router_gemm_affinity_and_routing(T, d, E, K, G, M, scale, zipf):
     """Tensor-core router logits (exact products, fp32 accumulation) + sigmoid
@@ -211,6 +216,7 @@ def test_router_gemm_affinity_and_routing(T, d, E, K, G, M, scale, zipf):
 @pytest.mark.parametrize("T,d,E,K,G,M,scale", [
     (4096, 2048, 64, 6, 1, 1, 1.0),        # mid layer shape: the reduction is split
     (64, 7168, 256, 8, 8, 4, 2.5),         # decode size of the V3 layer
+    (2048, 7168, 256, 8, 8, 4, 2.5),       # 32 tiles at V3 width, each split over 4 CTAs
 ])
 def test_router_split_and_unsplit_reductions_agree(T, d, E, K, G, M, scale):
     """Small batches split each router tile's reduction over several CTAs;
