@@ -327,6 +327,32 @@ def timed_steps(layer, cfg, xs, steps, warmup, names, group=None, local=0, redun
                 status=layer.device_status())
 
 
+def graphed_steps(layer, xs, steps, bias0):
+    """The trajectory timed_steps times, from the same initial bias, with each
+    step replayed from a CUDA graph captured beforehand for its batch (one
+    host call per step instead of one per kernel).  Returns the time of the
+    `steps` replays and their per-step load statistics."""
+    import torch
+    stats_hist = torch.zeros(steps, 4, dtype=torch.float32, device="cuda")
+    graphs = [layer.capture_step(xs[i % len(xs)], stats_out=stats_hist[i]) for i in range(steps)]
+    for _ in range(3):                       # warm-up replays, then back to the initial bias
+        graphs[0].replay()
+    layer.bias.copy_(bias0)
+    stream = torch.cuda.current_stream()
+    clocks = ClockSampler(0)
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks.mark_start()
+    ev0.record(stream)
+    for g in graphs:
+        g.replay()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    clocks.mark_stop()
+    return dict(ms=ev0.elapsed_time(ev1), stats=stats_hist.cpu().numpy(), clocks=clocks.stop(),
+                status=layer.device_status())
+
+
 def workload_name(cfg):
     return (f"{cfg.name}: T={cfg.T} d={cfg.d} E={cfg.E} K={cfg.K} shared={cfg.n_shared} I={cfg.I} "
             f"groups={cfg.n_groups}/{cfg.topk_groups} scale={cfg.route_scale}")
@@ -410,7 +436,8 @@ def run_workloads(args, v3_layer, pk):
     names = ["route", "permute", "routed", "shared", "combine"]
     out = {}
 
-    def one(cfg, layer, xs, steps, warmup):
+    def one(cfg, layer, xs, steps, warmup, graphs=False):
+        bias0 = layer.bias.clone()
         res = timed_steps(layer, cfg, xs, steps, warmup, names)
         ms_step = res["ms"] / steps
         entry = {"workload": workload_name(cfg), "steps": steps, "warmup": warmup,
@@ -424,6 +451,16 @@ def run_workloads(args, v3_layer, pk):
             entry["layer_tensor_frac"] = layer_fraction(cfg, ms_step, res["ms"] / 1e3, pk)
         if cfg.steps > 1:
             entry["feedback"] = feedback_summary(cfg, res["stats"])
+        if graphs:
+            # the same steps replayed from CUDA graphs: launch-bound steps lose
+            # the host's per-call cost; the trajectory must match bit for bit
+            g = graphed_steps(layer, xs, steps, bias0)
+            entry["graphs"] = {
+                "value": round(cfg.T * steps / (g["ms"] / 1e3), 1), "unit": "tokens/s",
+                "ms_per_step": round(g["ms"] / steps, 4),
+                "same_trajectory": bool((g["stats"] == res["stats"]).all()),
+                "gpu_launches": (KERNELS_PER_STEP + router_extra(cfg)) * steps,
+                "device_status": g["status"], "clocks": g["clocks"]}
         return entry
 
     for name in ("tiny", "mid"):
@@ -433,7 +470,7 @@ def run_workloads(args, v3_layer, pk):
         del p
         n_batches = cfg.steps if cfg.steps > 1 else 2
         xs = [synth.make_tokens(cfg, step=i, device="cuda") for i in range(n_batches)]
-        out[name] = one(cfg, layer, xs, cfg.steps if cfg.steps > 1 else 50, 5)
+        out[name] = one(cfg, layer, xs, cfg.steps if cfg.steps > 1 else 50, 5, graphs=True)
         del layer, xs
         torch.cuda.empty_cache()
     # decode sizes and the drifting run share the V3 layer's weights

@@ -444,6 +444,24 @@ class MoELayer:
         self.bias_update(x.shape[0], stream, group, stats_out)
         return y
 
+    def capture_step(self, x: torch.Tensor, stats_out=None,
+                     out: torch.Tensor | None = None) -> "StepGraph":
+        """One step (forward on x, then the bias update from its loads)
+        captured in a CUDA graph: replay() relaunches all of the step's
+        kernels with one host call, on the same x, out and stats_out buffers
+        and the layer's own buffers (the bias it reads is the one the previous
+        replay or step left).  Steps of small batches are bound by the host's
+        per-call launch cost; a replay removes it.  Run one forward pass
+        before capturing (first calls set up kernel attributes).  Single
+        process only (a process group's load all-reduce is not captured)."""
+        g = torch.cuda.CUDAGraph()
+        n = getattr(self, "updates", 0)
+        with torch.cuda.graph(g):
+            self.forward(x, out=out)
+            self.bias_update(x.shape[0], stats_out=stats_out)
+        self.updates = n                  # capturing ran nothing
+        return StepGraph(self, g, self.out[:x.shape[0]] if out is None else out)
+
     def device_status(self) -> int:
         return int(self.status.item())
 
@@ -577,6 +595,20 @@ class MoELayer:
         mark("bwd_dx", 1)
         return dict(dx=dx, dw_r=b["dw_r"], dw13=b["dw13"], dw2=b["dw2"],
                     dws13=b["dws13"][0], dws2=b["dws2"][0], dgate=b["dgate"][:T], du=b["du"][:T])
+
+
+class StepGraph:
+    """A layer step captured by MoELayer.capture_step."""
+
+    def __init__(self, layer: "MoELayer", graph: torch.cuda.CUDAGraph, out: torch.Tensor):
+        self.layer, self.graph, self.out = layer, graph, out
+
+    def replay(self) -> torch.Tensor:
+        """Runs the captured step on the current stream's device work queue;
+        returns the output buffer it writes."""
+        self.graph.replay()
+        self.layer.updates = getattr(self.layer, "updates", 0) + 1
+        return self.out
 
 
 class HostPipeline:
