@@ -47,8 +47,8 @@ constexpr int kEpiWarps = 4;
 constexpr int kThreads = (3 + kEpiWarps) * 32;
 constexpr int kStages = 12;
 constexpr int kChunk = 64 * BK * 2;              // 4 KB: 64 MN elements x 32 tokens
-constexpr int kABytes = (TM / 2 / 64) * kChunk;  // 16 KB per CTA
-constexpr int kBBytes = (TN / 2 / 64) * kChunk;  // 16 KB per CTA
+constexpr int kABytes = (TM / 2 / 64) * kChunk;  // 8 KB per CTA and k-block
+constexpr int kBBytes = (TN / 2 / 64) * kChunk;  // 8 KB per CTA and k-block
 constexpr int kStageBytes = kABytes + kBBytes;
 constexpr int kOutBuf = 32 * 32 * 4;         // one 32 x 32 fp32 block
 constexpr int kOutBytes = kEpiWarps * 2 * kOutBuf;  // 2 buffers per epilogue warp
