@@ -195,6 +195,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto xempty_bar = [&](int pr, int b) { return bars + 8u * (C::kNumBars + 4 + 2 * pr + b); };
   // epilogue row gather (down / data-gradient modes, SwiGLU on box-contiguous
   // weights): the four epilogue warps meet once per 32-token chunk
+  static_assert(kThreads == 6 * 32, "the row-gather barrier counts four epilogue warps");
   const uint32_t gather_bar = bars + 8u * C::kNumBars;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(meta + 8 * (C::kNumBars + 8));
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
