@@ -40,7 +40,8 @@ def seeded_rows(rows, cols, seed):
     return x
 
 
-@pytest.mark.parametrize("rows,cols", [(1, 128), (37, 256), (300, 384), (1024, 7168)])
+@pytest.mark.parametrize("rows,cols", [(1, 128), (37, 256), (300, 384), (1024, 7168),
+                                       (5, 1152), (65, 2048)])   # a run of 8 blocks + 1; two runs
 def test_quantize_rows_bit_exact(rows, cols):
     x = seeded_rows(rows, cols, 11 + rows)
     ld = rows + 5
