@@ -267,6 +267,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     kb_hi = kb_lo + split_kb < p.num_kb ? kb_lo + split_kb : p.num_kb;
   };
   const int chunk_kb = (MODE == MODE_ROUTER) ? kRouterChunkKb : p.num_kb;
+  // Rows per token tile of a group of rows_g rows (expert modes): the group's
+  // ceil(rows_g / 256) tiles share its rows evenly, rounded up to 16, so no
+  // tile is a sliver.  A tile's MMAs cost the issuer about the same whatever
+  // their N, so 300 rows as 160 + 144 cost less than as 256 + 48.  (The
+  // fallback to 256 guards the last tile against being empty; no group of
+  // up to 200000 rows needs it.)  Each token's arithmetic is unchanged.
+  auto tile_rows = [&](int rows_g) {
+    if (MODE == MODE_ROUTER || rows_g <= C::kTokTile) return C::kTokTile;
+    const int nt = (rows_g + C::kTokTile - 1) / C::kTokTile;
+    const int per = ((rows_g + nt - 1) / nt + 15) & ~15;
+    return (nt - 1) * per < rows_g ? per : C::kTokTile;
+  };
   const int num_st = (p.num_kb + C::kBoxes - 1) / C::kBoxes;           // stages per tile
   // stages per TMEM unit (a router chunk holds whole stages)
   const int chunk_st = (MODE == MODE_ROUTER) ? kRouterChunkKb / C::kBoxes : num_st;
@@ -292,10 +304,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         decode_work(w / splits, NT, mt_prefix, G, g, n, m);
         st_range(w, st_lo, st_hi);
         const int rows_g = row_start[g + 1] - row_start[g];
-        int tok_row = row_start[g] + m * C::kTokTile;
+        const int per = tile_rows(rows_g);
+        int tok_row = row_start[g] + m * per;
         int w_row = g * p.w_rows_per_group + n * C::kColTile;
         if (PAIR) {
-          tok_row += static_cast<int>(rank) * (tile_n(rows_g - m * C::kTokTile, C::kTokTile) / 2);
+          tok_row += static_cast<int>(rank) * (tile_n(rows_g - m * per, per) / 2);
           w_row += static_cast<int>(rank) * (MODE == MODE_SWIGLU ? 64 : 128);
         }
         for (int st = st_lo; st < st_hi; ++st, ++it) {
@@ -390,7 +403,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           idesc = umma_idesc_bf16(128, C::kColTile);
         } else {
           const int rows_g = row_start[g + 1] - row_start[g];
-          idesc = umma_idesc_bf16(256, tile_n(rows_g - m * C::kTokTile, C::kTokTile)) |
+          const int per = tile_rows(rows_g);
+          idesc = umma_idesc_bf16(256, tile_n(rows_g - m * per, per)) |
                   (MODE == MODE_DGRAD ? (1u << 15) : 0u);  // A (weights) MN-major
         }
         for (int st0 = st_lo; st0 < st_hi && ok; st0 += chunk_st, ++unit) {
@@ -511,9 +525,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = __all_sync(0xFFFFFFFFu, mbar_wait_nap(accf_bar(b), bph, abort_flag, p.status));
         if (!ok) break;
         tc_fence_after();
-        const int tok0 = m * C::kTokTile;
-        const int n_eff = tile_n(rows_g - tok0, C::kTokTile);
-        const int rows_tile = (rows_g - tok0) < C::kTokTile ? rows_g - tok0 : C::kTokTile;
+        const int per = tile_rows(rows_g);
+        const int tok0 = m * per;
+        const int n_eff = tile_n(rows_g - tok0, per);
+        const int rows_tile = (rows_g - tok0) < per ? rows_g - tok0 : per;
         const int col = n * C::kColTile +
                         (MODE == MODE_SWIGLU ? 64 * static_cast<int>(rank) + 32 * (q & 1)
                                              : 128 * static_cast<int>(rank) + 32 * q);
