@@ -41,7 +41,7 @@ CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.a
 # from ncu dram__bytes on the 16-expert V3-shaped profiling case (d=7168,
 # I=2048, ~256 rows per expert), scaled by the experts a launch processes.
 # Must be re-measured whenever those kernels change.
-GEMM_TRAFFIC_PER_EXPERT = (1.043762944e9 + 16.54784e6 + 0.499597056e9 + 49.208576e6) / 16
+GEMM_TRAFFIC_PER_EXPERT = (1.042770688e9 + 16.624128e6 + 0.504207872e9 + 49.14816e6) / 16
 # The timed region's length decides which measured tensor peak a fraction is
 # taken against: a region shorter than this runs at burst clocks (the peak of
 # a kernel timed alone); a longer one settles at the power-capped clock (the
