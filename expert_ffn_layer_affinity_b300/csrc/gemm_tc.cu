@@ -129,10 +129,9 @@ struct Cfg : Tr<MODE> {
   static constexpr int kStageBytes = T::kBoxes * (T::kA + T::kB);
   static constexpr int kTmemCols = T::kBufs * T::kBufCols;
   static constexpr int kNumBars = 2 * T::kStages + 2 * T::kBufs + 1;
-  // epilogue staging: four per-warp 32 x 80-byte blocks (SwiGLU on strided
-  // weights), or a CTA-wide [2][32 tokens][columns] tile that the four
-  // epilogue warps fill together (64 columns for SwiGLU on box-contiguous
-  // weights, inside the same bytes; 128 for the down and data-gradient modes)
+  // epilogue staging: four per-warp 32 x 80-byte blocks (SwiGLU), or a
+  // CTA-wide [2][32 tokens][128 columns] tile that the four epilogue warps
+  // fill together (down and data-gradient modes)
   static constexpr int kXposeBytes = (MODE == MODE_ROUTER) ? 0
                                      : (MODE == MODE_DOWN || MODE == MODE_DGRAD) ? 2 * 32 * 128 * 2
                                                                                  : 4 * 32 * 80;
@@ -193,8 +192,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   // SwiGLU exchange: xfull / xempty for (warp pair, buffer)
   auto xfull_bar = [&](int pr, int b) { return bars + 8u * (C::kNumBars + 2 * pr + b); };
   auto xempty_bar = [&](int pr, int b) { return bars + 8u * (C::kNumBars + 4 + 2 * pr + b); };
-  // epilogue row gather (down / data-gradient modes, SwiGLU on box-contiguous
-  // weights): the four epilogue warps meet once per 32-token chunk
+  // epilogue row gather (down and data-gradient modes): the four epilogue
+  // warps meet once per 32-token chunk
   static_assert(kThreads == 6 * 32, "the row-gather barrier counts four epilogue warps");
   const uint32_t gather_bar = bars + 8u * C::kNumBars;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(meta + 8 * (C::kNumBars + 8));
@@ -228,11 +227,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(acce_bar(b), PAIR ? 256 : 128);
       }
       mbar_init(drain_bar, 1);
-      // the first of these is the epilogue warps' row-gather barrier (one
-      // arrival per warp) wherever the SwiGLU hand-over does not use it
+      // outside SwiGLU the first of these is the epilogue warps' row-gather
+      // barrier (one arrival per warp)
       for (int i = 0; i < 8; ++i)
-        mbar_init(bars + 8u * (C::kNumBars + i),
-                  (i == 0 && (MODE != MODE_SWIGLU || p.w_tiled)) ? 4 : 1);
+        mbar_init(bars + 8u * (C::kNumBars + i), (i == 0 && MODE != MODE_SWIGLU) ? 4 : 1);
       *abort_flag = 0;
       fence_mbar_init();
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -549,12 +547,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             // the gate (w1 row i) and lane 2i + 1 the up value (w3 row i) of
             // output column i, so a lane pair of this warp owns 16 columns;
             // the even lane finishes tokens 0..15 of the chunk, the odd lane
-            // tokens 16..31, after swapping halves with one shuffle each.  The
-            // four warps fill one [32 tokens][64 columns] tile (the CTA's
-            // columns), then each writes 8 whole 128-byte token rows of it.
+            // tokens 16..31, after swapping halves with one shuffle each
             const bool odd = (lane & 1) != 0;
-            __nv_bfloat16* tile =
-                reinterpret_cast<__nv_bfloat16*>(xpose) + (xchunk & 1u) * (32 * 64);
+            const int tcol = n * C::kColTile + 64 * static_cast<int>(rank) + 16 * q;
+            __nv_bfloat16* st = reinterpret_cast<__nv_bfloat16*>(xp);  // [32 tokens][16 columns]
 #pragma unroll
             for (int k = 0; k < 16; ++k) {
               const float mine = __uint_as_float(odd ? v[k] : v[16 + k]);
@@ -562,21 +558,16 @@ __global__ void __launch_bounds__(kThreads, 1)
               const float gate = odd ? other : __uint_as_float(v[k]);
               const float up = odd ? __uint_as_float(v[16 + k]) : other;
               const float hv = gate * __frcp_rn(1.0f + __expf(-gate)) * up;
-              tile[((odd ? 16 : 0) + k) * 64 + 16 * q + (lane >> 1)] = __float2bfloat16_rn(hv);
+              st[((odd ? 16 : 0) + k) * 16 + (lane >> 1)] = __float2bfloat16_rn(hv);
             }
             __syncwarp();
-            if (lane == 0) mbar_arrive(gather_bar);
-            ok = __all_sync(0xFFFFFFFFu, mbar_wait(gather_bar, xchunk & 1u, abort_flag, p.status));
-            if (!ok) break;
-            const int cbase = n * C::kColTile + 64 * static_cast<int>(rank);
-#pragma unroll
-            for (int i = 0; i < 2; ++i) {
-              const int r = 8 * q + 4 * i + (lane >> 3);
-              const int cc = (lane & 7) * 8;
-              if (r < valid && cbase + cc < p.N)
-                *reinterpret_cast<uint4*>(out + (row0 + c + r) * p.ldo + cbase + cc) =
-                    *reinterpret_cast<const uint4*>(tile + r * 64 + cc);
+            if (tcol < p.N && lane < valid) {
+              const uint4* src = reinterpret_cast<const uint4*>(xp + lane * 32);
+              uint4* dst = reinterpret_cast<uint4*>(out + (row0 + c + lane) * p.ldo + tcol);
+              dst[0] = src[0];
+              dst[1] = src[1];
             }
+            __syncwarp();
           } else if (MODE == MODE_SWIGLU) {
             // pair (q, q + 2): lanes 64..127 (up) hand over to lanes 0..63 (gate)
             const int pr = q & 1, xb = static_cast<int>(xchunk & 1u);
@@ -615,11 +606,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           } else {
             // the CTA's 128 columns of the chunk's 32 tokens, gathered from the
             // four epilogue warps into one tile, then written as whole 256-byte
-            // token rows.  With the same gather in the SwiGLU epilogue, against
-            // each warp storing its own pieces (one line per lane and store),
-            // measured on the V3 routed call: 4% fewer SM cycles, cold-start
-            // steps 6.96 -> 6.90 ms; bit-identical.  The store transactions
-            // share the SM's L1 data path with the MMA's operand reads.
+            // token rows instead of each lane storing 64 bytes of a different
+            // row (the store transactions share the SM's L1 data path with the
+            // MMA's operand reads; bit-identical).  The SwiGLU epilogue keeps
+            // per-warp stores: there the extra meeting per chunk cost the
+            // mid layer 1.9% (its 32-k-block items leave the epilogue little
+            // slack) and gained nothing measurable at the V3 shape.
             __nv_bfloat16* tile =
                 reinterpret_cast<__nv_bfloat16*>(xpose) + (xchunk & 1u) * (32 * 128);
 #pragma unroll
