@@ -557,7 +557,11 @@ __global__ void __launch_bounds__(kThreads, 1)
               const float other = __shfl_xor_sync(0xFFFFFFFFu, mine, 1);
               const float gate = odd ? other : __uint_as_float(v[k]);
               const float up = odd ? __uint_as_float(v[16 + k]) : other;
-              const float hv = gate * __frcp_rn(1.0f + __expf(-gate)) * up;
+              // silu(gate) * up; the fast division (about 2 ulp in fp32, far
+              // below the bf16 rounding of h) instead of a correctly rounded
+              // reciprocal: the SwiGLU epilogue is on the critical path of
+              // short items (mid layer: 0.686 -> 0.624 ms per step)
+              const float hv = __fdividef(gate, 1.0f + __expf(-gate)) * up;
               st[((odd ? 16 : 0) + k) * 16 + (lane >> 1)] = __float2bfloat16_rn(hv);
             }
             __syncwarp();
@@ -597,7 +601,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
               for (int j = 0; j < 32; ++j) {
                 const float a = __uint_as_float(v[j]);
-                v[j] = __float_as_uint(a * __frcp_rn(1.0f + __expf(-a)) * xrow[j]);
+                v[j] = __float_as_uint(__fdividef(a, 1.0f + __expf(-a)) * xrow[j]);  // as above
               }
               __syncwarp();
               if (lane == 0) mbar_arrive(xempty_bar(pr, xb));
